@@ -1,0 +1,147 @@
+// extern "C" entry points of libspecverify.so: argument checks, workspace
+// sizing and error reporting around the kernels' launchers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "sv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sv_status fail(sv_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+constexpr int kMaxK = 20;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int sv_version(void) { return 100; }
+
+size_t sv_workspace_size(int B, int K, int V, sv_dtype dt) {
+  if (B < 1 || K < 0 || K > kMaxK || V < 1 || (dt != SV_F32 && dt != SV_BF16)) return 0;
+  return sv::verify_workspace_bytes(B, K);
+}
+
+size_t sv_lmhead_workspace_size(int M, int H) {
+  if (M < 1 || H < 1) return 0;
+  return sv::lmhead_workspace_bytes(M, H);
+}
+
+sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
+                         int64_t target_pos_stride, const void* draft_logits,
+                         int64_t draft_seq_stride, int64_t draft_pos_stride, sv_dtype dtype,
+                         int B, int K, int V, const int32_t* draft_tokens,
+                         const int32_t* k_per_row, const float* temperature, float top_p,
+                         const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                         int32_t* n_accepted, float* diag, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
+  if (B < 1 || K < 0 || K > kMaxK || V < 1)
+    return fail(SV_ERR_SHAPE, "need B >= 1, 0 <= K <= 20, V >= 1");
+  if (!target_logits || !uniforms || !out_tokens || !n_accepted)
+    return fail(SV_ERR_ARG, "target_logits, uniforms, out_tokens and n_accepted are required");
+  if (K > 0 && !draft_tokens) return fail(SV_ERR_ARG, "draft_tokens is required when K > 0");
+  if (K > 0 && !draft_logits && !mode)
+    return fail(SV_ERR_ARG, "draft_logits may be NULL only when every row is greedy (mode given)");
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(SV_ERR_ARG, "top_p must be in (0, 1]");
+  const int es = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)))
+    return fail(SV_ERR_ARG, "logit pointers must be aligned to their element size");
+  const long long Vl = V;
+  long long ts = target_seq_stride ? target_seq_stride : (long long)(K + 1) * Vl;
+  long long tp = target_pos_stride ? target_pos_stride : Vl;
+  long long ds = draft_seq_stride ? draft_seq_stride : (long long)K * Vl;
+  long long dp = draft_pos_stride ? draft_pos_stride : Vl;
+  if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
+  if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
+  if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
+  if (top_p < 1.0f) return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is not implemented in this build");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < sv::verify_workspace_bytes(B, K))
+    return fail(SV_ERR_WORKSPACE, "workspace smaller than sv_workspace_size()");
+  sv::VerifyLaunch L;
+  L.target = target_logits;
+  L.t_seq = ts;
+  L.t_pos = tp;
+  L.draft = draft_logits;
+  L.d_seq = ds;
+  L.d_pos = dp;
+  L.dtype = dtype;
+  L.B = B;
+  L.K = K;
+  L.V = V;
+  L.tokens = draft_tokens;
+  L.kpr = k_per_row;
+  L.temp = temperature;
+  L.top_p = top_p;
+  L.unif = uniforms;
+  L.mode = mode;
+  L.out = out_tokens;
+  L.nacc = n_accepted;
+  L.diag = diag;
+  L.workspace = workspace;
+  L.stream = stream;
+  std::string err;
+  int s = sv::verify_launch(L, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
+sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
+                       int B, int K, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (!seq_lens || !n_accepted) return fail(SV_ERR_ARG, "seq_lens and n_accepted are required");
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256)
+    return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL, 256-byte aligned, >= 256 bytes");
+  std::string err;
+  int s = sv::commit_launch(seq_lens, n_accepted, capacity, B, K,
+                            static_cast<uint32_t*>(workspace), stream, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
+sv_status sv_lmhead_rmsnorm(const void* hidden, const void* norm_w, float eps, const void* W,
+                            void* logits, sv_dtype out_dtype, int M, int H, int V,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (out_dtype != SV_F32 && out_dtype != SV_BF16) return fail(SV_ERR_DTYPE, "bad out_dtype");
+  if (M < 1 || H < 64 || H % 64 != 0 || V < 16 || V % 16 != 0)
+    return fail(SV_ERR_SHAPE, "need M >= 1, H % 64 == 0, V % 16 == 0");
+  if (!hidden || !norm_w || !W || !logits) return fail(SV_ERR_ARG, "null pointer");
+  if (!(eps >= 0.0f)) return fail(SV_ERR_ARG, "eps must be >= 0");
+  if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(logits, 16) || !aligned(norm_w, 2))
+    return fail(SV_ERR_ARG, "hidden, W and logits must be 16-byte aligned");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < sv::lmhead_workspace_bytes(M, H))
+    return fail(SV_ERR_WORKSPACE, "workspace smaller than sv_lmhead_workspace_size()");
+  std::string err;
+  int s = sv::lmhead_launch(hidden, norm_w, eps, W, logits, out_dtype, M, H, V, workspace,
+                            workspace_bytes, stream, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
+sv_status sv_read_device_flags(const void* workspace, uint32_t* flags_host, void* stream) {
+  if (!workspace || !flags_host) return fail(SV_ERR_ARG, "null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flags_host, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, std::string("reading flags: ") + cudaGetErrorString(e));
+  if (*flags_host == 0) return SV_OK;
+  if (*flags_host & SV_FLAG_TIMEOUT) return fail(SV_ERR_TIMEOUT, "a bounded device wait ran out");
+  return fail(SV_ERR_DEVICE_FLAG, "device flag word is non-zero");
+}
+
+const char* sv_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

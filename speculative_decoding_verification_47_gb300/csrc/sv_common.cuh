@@ -1,0 +1,132 @@
+// Device helpers shared by the verify, commit and LM-head kernels (sm_103a).
+//
+// Bulk asynchronous copies (the TMA engine's 1-D form), mbarrier completion,
+// thread-block-cluster distributed shared memory, and double-float ("two
+// float") accumulation.  The double-float sum keeps a row's normaliser and the
+// residual CDF accurate to ~1e-9 relative, which the verify step needs so that
+// its token decisions agree with exact arithmetic except when the exact
+// decision itself sits within ~1e-9 of its threshold.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cooperative_groups.h>
+
+namespace sv {
+
+namespace cg = cooperative_groups;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk copy (global -> shared), 16-byte aligned, size % 16 == 0
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: every try_wait suspends for a hardware-chosen interval; after
+// `limit` failed tries the caller gets false and must report a timeout
+// instead of waiting forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t limit = (1u << 22)) {
+  for (uint32_t it = 0; it < limit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// Exponential: 2^x on the MUFU unit (flush-to-zero below 2^-126).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// Double-float accumulation (Knuth's two-sum; no reassociation: this file is
+// compiled without fast-math).
+// ---------------------------------------------------------------------------
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// acc += x, keeping the rounding error in acc.lo (renormalised lazily).
+__device__ __forceinline__ void df_acc(DF& acc, float x) {
+  float s, e;
+  two_sum(acc.hi, x, s, e);
+  acc.hi = s;
+  acc.lo = __fadd_rn(acc.lo, e);
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  float hi = __fadd_rn(s, e);
+  return DF{hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ DF df_shfl_xor(DF v, int mask) {
+  return DF{__shfl_xor_sync(0xffffffffu, v.hi, mask), __shfl_xor_sync(0xffffffffu, v.lo, mask)};
+}
+
+__device__ __forceinline__ DF df_warp_sum(DF v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v = df_add(v, df_shfl_xor(v, m));
+  return v;
+}
+
+__device__ __forceinline__ double df_to_double(DF v) { return (double)v.hi + (double)v.lo; }
+
+// ---------------------------------------------------------------------------
+// bf16 unpacking: word w holds element 2k in its low half, 2k+1 in its high.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+}  // namespace sv

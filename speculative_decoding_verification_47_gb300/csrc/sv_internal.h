@@ -1,0 +1,44 @@
+// Host-side interfaces between the C ABI (sv_api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+struct VerifyLaunch {
+  const void* target;
+  long long t_seq, t_pos;  // elements
+  const void* draft;
+  long long d_seq, d_pos;  // elements
+  sv_dtype dtype;
+  int B, K, V;
+  const int32_t* tokens;
+  const int32_t* kpr;
+  const float* temp;
+  float top_p;
+  const float* unif;
+  const uint8_t* mode;
+  int32_t* out;
+  int32_t* nacc;
+  float* diag;
+  void* workspace;
+  void* stream;
+};
+
+// Enqueue the verify step.  Returns an sv_status; fills *err on failure.
+int verify_launch(const VerifyLaunch& L, std::string* err);
+size_t verify_workspace_bytes(int B, int K);
+
+int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
+                  int K, uint32_t* flags, void* stream, std::string* err);
+
+int lmhead_launch(const void* hidden, const void* norm_w, float eps, const void* W, void* logits,
+                  sv_dtype out_dtype, int M, int H, int V, void* workspace, size_t ws_bytes,
+                  void* stream, std::string* err);
+size_t lmhead_workspace_bytes(int M, int H);
+
+}  // namespace sv
