@@ -246,20 +246,43 @@ struct Weight {
   }
 };
 
+// Element e of a slice read back from shared memory one at a time (used when
+// the draft row's 16-byte phase differs from the target row's).
 template <int ES>
-__device__ __forceinline__ float unit_weight_sum(const SliceMap<ES>& s, const char* bt,
+__device__ __forceinline__ float slice_elem(const SliceMap<ES>& s, const char* buf, int e) {
+  const char* p = buf + (s.g0 - s.base16) + (size_t)(e - s.e0) * ES;
+  return ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(p))
+                 : *reinterpret_cast<const float*>(p);
+}
+
+// Target and draft slices of one position: unit u of the target buffer holds
+// elements [ebase0 + u*EPU, ...).  When both rows start at the same offset
+// modulo 16 bytes the draft buffer's unit u holds the same elements.
+template <int ES>
+struct PairMap {
+  const SliceMap<ES>* st;
+  const SliceMap<ES>* sd;
+  bool same_phase;
+};
+
+template <int ES>
+__device__ __forceinline__ float unit_weight_sum(const PairMap<ES>& pm, const char* bt,
                                                  const char* bd, int u, const Weight& W) {
   constexpr int EPU = 16 / ES;
+  const SliceMap<ES>& s = *pm.st;
   if (u >= s.n_units) return 0.f;
   uint4 vt = *reinterpret_cast<const uint4*>(bt + 16 * u);
-  uint4 vd = W.p_only ? vt : *reinterpret_cast<const uint4*>(bd + 16 * u);
+  const bool vec_d = W.p_only || pm.same_phase;
+  uint4 vd = vec_d ? (W.p_only ? vt : *reinterpret_cast<const uint4*>(bd + 16 * u)) : vt;
   int eb = s.ebase0 + u * EPU;
   float e[EPU];
   bool full = eb >= s.e0 && eb + EPU <= s.e1;
 #pragma unroll
   for (int j = 0; j < EPU; ++j) {
     bool ok = full || (eb + j >= s.e0 && eb + j < s.e1);
-    e[j] = ok ? W(unit_elem<ES>(vt, j), unit_elem<ES>(vd, j)) : 0.f;
+    float zd = 0.f;
+    if (ok) zd = vec_d ? unit_elem<ES>(vd, j) : slice_elem<ES>(*pm.sd, bd, eb + j);
+    e[j] = ok ? W(unit_elem<ES>(vt, j), zd) : 0.f;
   }
   if (EPU == 8) return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
   return (e[0] + e[1]) + (e[2] + e[3]);
@@ -267,12 +290,12 @@ __device__ __forceinline__ float unit_weight_sum(const SliceMap<ES>& s, const ch
 
 // Per-tile (256 units), per-warp partial sums of the weights of a slice.
 template <int ES>
-__device__ void slice_weight_partials(const SliceMap<ES>& s, const char* bt, const char* bd,
+__device__ void slice_weight_partials(const PairMap<ES>& pm, const char* bt, const char* bd,
                                       const Weight& W, DF (*tw)[kWarps]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = (s.n_units + kThreads - 1) / kThreads;
+  const int tiles = (pm.st->n_units + kThreads - 1) / kThreads;
   for (int t = 0; t < tiles; ++t) {
-    float us = unit_weight_sum<ES>(s, bt, bd, t * kThreads + threadIdx.x, W);
+    float us = unit_weight_sum<ES>(pm, bt, bd, t * kThreads + threadIdx.x, W);
     DF v = df_warp_sum(DF{us, 0.f});
     if (lane == 0) tw[t][warp] = v;
   }
@@ -635,10 +658,14 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
     W.rho_lo = (float)(rho - (double)W.rho_hi);
   }
   const int tiles = (st.n_units + kThreads - 1) / kThreads;
+  PairMap<ES> pm;
+  pm.st = &st;
+  pm.sd = &sd;
+  pm.same_phase = bonus || st.ebase0 == sd.ebase0;
   DF slice_w{0.f, 0.f};
   for (int pass = 0; pass < 2; ++pass) {
     if (pass) cluster.sync();  // every CTA has read the first pass's slots
-    slice_weight_partials<ES>(st, buf_t, buf_d, W, sh.tw);
+    slice_weight_partials<ES>(pm, buf_t, buf_d, W, sh.tw);
     __syncthreads();
     if (tid < C) {
       DF a{0.f, 0.f};
@@ -703,7 +730,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   if (warp != wsel) return;
   // lanes of the selected warp: inclusive scan of their unit sums
   const int u = tsel * kThreads + wsel * 32 + lane;
-  float us = unit_weight_sum<ES>(st, buf_t, buf_d, u, W);
+  float us = unit_weight_sum<ES>(pm, buf_t, buf_d, u, W);
   double inc = (double)us;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -717,14 +744,16 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   if (lane == sel && u < st.n_units) {
     constexpr int EPU = 16 / ES;
     uint4 vt = *reinterpret_cast<const uint4*>(buf_t + 16 * u);
-    uint4 vd = W.p_only ? vt : *reinterpret_cast<const uint4*>(buf_d + 16 * u);
+    const bool vec_d = W.p_only || pm.same_phase;
+    uint4 vd = vec_d ? (W.p_only ? vt : *reinterpret_cast<const uint4*>(buf_d + 16 * u)) : vt;
     int eb = st.ebase0 + u * EPU;
     double c = exc;
     int y = -1, ylast = -1;
     for (int q = 0; q < EPU; ++q) {
       int e = eb + q;
       if (e < st.e0 || e >= st.e1) continue;
-      float wv = W(unit_elem<ES>(vt, q), unit_elem<ES>(vd, q));
+      float zd = vec_d ? unit_elem<ES>(vd, q) : slice_elem<ES>(sd, buf_d, e);
+      float wv = W(unit_elem<ES>(vt, q), zd);
       if (wv > 0.f) ylast = e;
       c += (double)wv;
       if (wv > 0.f && c > rem) {
