@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched speculative-decoding verify step on GB300.
+
+One step = sv_spec_verify + sv_kv_commit over one batch of the headline
+workload (B=256 sequences, K=8 with ragged k_b in 2..8, V=128256 bf16 logits,
+per-row temperature in {0.1, 0.7, 1.0} and draft noise in {0.3, 1, 2};
+sampled mode).  Inputs are resident in HBM when timing starts and are
+rotated over three identical copies (3.3 GB > the 129 MB L2) so no step
+reuses data cached by the previous one.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on bounded samples of the same workload instead.  Under torchrun each
+rank runs an independent replica (weak scaling, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/s and spec_verify HBM GB/s (% of GB300 peak) at 1 GPU"
+WORKLOAD = ("headline verify batch: B=256, K=8, ragged k_b~U{2..8}, V=128256 bf16 logits, "
+            "T_b in {0.1,0.7,1.0}, draft noise in {0.3,1,2}, sampled; + kv_commit")
+COPIES = 3
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg (bounded sample, spawn pool, sequences regenerated per worker)
+# --------------------------------------------------------------------------
+def _oracle_worker(args):
+    seqs, B = args
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    from oracle import verify as ov
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    k, T, s = wl.c2_row_params(B)
+    V, K = 128256, 8
+    rows = []
+    for b in seqs:
+        t, d, x, u = wl._gen_sequence(b, B, K, V, wl.BF16, int(k[b]), float(T[b]), float(s[b]),
+                                      wl.SAMPLED, (1002, 2002, 2))
+        rows.append((b, t, d, x, u))
+    t0 = time.perf_counter()
+    pos = 0
+    for b, t, d, x, u in rows:
+        ov.verify_sequence(ov._LazyRows(t, "bf16"), ov._LazyRows(d, "bf16"), x, int(k[b]), K, V,
+                           float(T[b]), 1.0, u.astype(np.float64), 0)
+        pos += int(k[b])
+    return pos, time.perf_counter() - t0
+
+
+def cpu_oracle(sample_seqs: int, workers: int):
+    import multiprocessing as mp
+    B = 256
+    seqs = list(range(sample_seqs))
+    chunks = [seqs[i::workers] for i in range(workers)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_worker, [(c, B) for c in chunks if c])
+    pos = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    return pos, wall, len([c for c in chunks if c])
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from speculative_decoding_verification_47_gb300 import binding as sb
+    from speculative_decoding_verification_47_gb300 import build as bld
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    if pg is not None:
+        pg.barrier()
+
+    # CPU baseline first (spawn pool, before any GPU work of the main loop)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        workers = min(16, len(os.sched_getaffinity(0)))
+        pos, wall, used = cpu_oracle(args.cpu_sample, workers)
+        cpu = {"value": pos / wall, "unit": "positions/s", "cores": used, "kind": "oracle",
+               "sample": f"first {args.cpu_sample} of the 256 sequences of the same workload, "
+                         f"float64 oracle, {used} spawn workers, wall {wall:.2f} s"}
+
+    w = wl.config_c2(B=args.B)
+    B, K, V = w.B, w.K, w.V
+    es = 2
+    dev = torch.device("cuda", local)
+    tg = torch.from_numpy(w.target.view(np.int16))
+    dr = torch.from_numpy(w.draft.view(np.int16))
+    tgts = [tg.to(dev) for _ in range(COPIES)]
+    drfs = [dr.to(dev) for _ in range(COPIES)]
+    tok = torch.from_numpy(w.draft_tokens).to(dev)
+    kpr = torch.from_numpy(w.k_per_row).to(dev)
+    tmp = torch.from_numpy(w.temperature).to(dev)
+    uni = torch.from_numpy(w.uniforms).to(dev)
+    mode = torch.from_numpy(w.mode).to(dev)
+    seq0 = torch.from_numpy(w.seq_lens).to(dev)
+    seq = seq0.clone()
+    cap = torch.full((B,), 2**30, dtype=torch.int32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    wsb = sb.sv_workspace_size(B, K, V, sb.SV_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(c):
+        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
+                          uni, mode, out, nacc, None, ws, wsb, stream)
+        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+
+    for it in range(args.warmup):
+        step(it % COPIES)
+    torch.cuda.synchronize()
+    flags = sb.sv_read_device_flags(ws)
+    n_host = nacc.cpu().numpy()
+    kb = w.k_per_row.astype(np.int64)
+    positions = int(kb.sum())
+    rows_needed = int(np.where(n_host < kb, 2 * (n_host + 1), 2 * kb + 1).sum())
+    rows_all = int((2 * kb + 1).sum())
+    small_bytes = B * 4 * (K + 1) * 2 + B * 16  # tokens, uniforms, outputs, per-row knobs
+    bytes_needed = rows_needed * V * es + small_bytes
+    bytes_all = rows_all * V * es + small_bytes
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for it in range(args.steps):
+        c = it % COPIES
+        ev[it][0].record(stream)
+        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
+                          uni, mode, out, nacc, None, ws, wsb, stream)
+        ev[it][1].record(stream)
+        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    if pg is not None:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    verify_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_step = ms / args.steps
+    value = positions * world / (ms_step * 1e-3)
+
+    # end to end: pinned host inputs -> device, verify + commit, outputs -> host
+    e2e = None
+    if not args.no_e2e:
+        h_t = torch.from_numpy(w.target.view(np.int16)).pin_memory()
+        h_d = torch.from_numpy(w.draft.view(np.int16)).pin_memory()
+        h_small = [torch.from_numpy(a).pin_memory() for a in
+                   (w.draft_tokens, w.k_per_row, w.temperature, w.uniforms, w.mode, w.seq_lens)]
+        d_small = [tok, kpr, tmp, uni, mode, seq]
+        o_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        o_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+        o_seq = torch.empty((B,), dtype=torch.int32).pin_memory()
+        steps_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            tgts[0].copy_(h_t, non_blocking=True)
+            drfs[0].copy_(h_d, non_blocking=True)
+            for d_, h_ in zip(d_small, h_small):
+                d_.copy_(h_, non_blocking=True)
+            sb.sv_spec_verify(tgts[0], 0, 0, drfs[0], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp,
+                              1.0, uni, mode, out, nacc, None, ws, wsb, stream)
+            sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+            o_out.copy_(out, non_blocking=True)
+            o_n.copy_(nacc, non_blocking=True)
+            o_seq.copy_(seq, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b)
+        if pg is not None:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = (h_t.numel() + h_d.numel()) * 2 + sum(x.numel() * x.element_size() for x in h_small)
+        d2h = (o_out.numel() + o_n.numel() + o_seq.numel()) * 4
+        e2e = {"value": positions * world / (ems / steps_e2e * 1e-3), "unit": "positions/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": steps_e2e}
+
+    peak, peak_src = peaks()
+    achieved = bytes_needed / (verify_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "input_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "K": K, "V": V,
+                   "positions_per_step": positions, "target_rows": int((kb + 1).sum()),
+                   "l2": f"{COPIES} rotating input copies ({COPIES * (w.target.nbytes + w.draft.nbytes) / 1e9:.1f} GB) > 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "hbm": {"bytes_needed_per_call": bytes_needed,
+                "bytes_all_rows_per_call": bytes_all,
+                "rows_needed": rows_needed, "rows_all": rows_all,
+                "gbs_needed": achieved,
+                "gbs_all_rows_equivalent": bytes_all / (verify_ms * 1e-3) / 1e9,
+                "frac_of_peak": achieved / peak, "peak_gbs": peak, "peak_source": peak_src},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": args.traffic,
+                     "kernel": "verify_kernel<2> (+ its init kernel)",
+                     "launch_ms": verify_ms, "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "device_flags": flags,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_reference(args):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    workers = min(16, len(os.sched_getaffinity(0)))
+    for _ in range(args.warmup):
+        cpu_oracle(workers, workers)  # one sequence per worker
+    tot_pos, tot_wall = 0, 0.0
+    for _ in range(args.steps):
+        pos, wall, used = cpu_oracle(args.ref_sample, workers)
+        tot_pos += pos
+        tot_wall += wall
+    value = tot_pos / tot_wall
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot_wall / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": 256, "K": 8, "V": 128256,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": used, "kind": "oracle",
+                         "sample": f"each step: first {args.ref_sample} of the 256 sequences, "
+                                   f"float64 oracle over {used} spawn workers"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--B", type=int, default=256,
+                    help="sequences (256 for the headline batch; smaller only for profiling)")
+    ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--ref-sample", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per verify launch, if measured for this kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

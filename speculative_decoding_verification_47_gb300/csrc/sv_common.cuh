@@ -62,13 +62,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: every try_wait suspends for a hardware-chosen interval; after
-// `limit` failed tries the caller gets false and must report a timeout
+// try_wait that may suspend the thread for up to `hint_ns` before returning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by ONE thread (the others sleep at the following CTA barrier
+// instead of spinning): each try suspends for up to 0.5 ms; after `limit`
+// failed tries (about a second) the caller gets false and reports a timeout
 // instead of waiting forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t limit = (1u << 22)) {
+                                                  uint32_t limit = 2048) {
   for (uint32_t it = 0; it < limit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, 500000u)) return true;
   return false;
 }
 
@@ -121,7 +134,64 @@ __device__ __forceinline__ DF df_warp_sum(DF v) {
   return v;
 }
 
-__device__ __forceinline__ double df_to_double(DF v) { return (double)v.hi + (double)v.lo; }
+__device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
+
+__device__ __forceinline__ DF df_sub(DF a, DF b) { return df_add(a, df_neg(b)); }
+
+// sign of a - b (double-float compare without FP64 instructions)
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  DF d = df_sub(a, b);
+  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+
+__device__ __forceinline__ bool df_pos(DF a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+
+// a * x for a float x (Dekker product with FMA)
+__device__ __forceinline__ DF df_mul_f(DF a, float x) {
+  float p = __fmul_rn(a.hi, x);
+  float e = __fmaf_rn(a.hi, x, -p);
+  e = __fmaf_rn(a.lo, x, e);
+  float hi = __fadd_rn(p, e);
+  return DF{hi, __fsub_rn(e, __fsub_rn(hi, p))};
+}
+
+// a / b in double-float: quotient, exact remainder, corrected quotient (the
+// double-length division of T. J. Dekker, "A floating-point technique for
+// extending the available precision", 1971), with float instructions only
+__device__ __forceinline__ DF df_div(DF a, DF b) {
+  float q1 = __fdiv_rn(a.hi, b.hi);
+  DF r = df_sub(a, df_mul_f(b, q1));
+  float q2 = __fdiv_rn(r.hi, b.hi);
+  float hi = __fadd_rn(q1, q2);
+  return DF{hi, __fsub_rn(q2, __fsub_rn(hi, q1))};
+}
+
+__device__ __forceinline__ float df_to_float(DF v) { return __fadd_rn(v.hi, v.lo); }
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (Blackwell f32x2 FMA / ADD: two lanes per instruction,
+// each lane rounded exactly like its scalar counterpart).
+// ---------------------------------------------------------------------------
+typedef unsigned long long F2;
+
+__device__ __forceinline__ F2 f2_pack(float a, float b) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(F2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 
 // ---------------------------------------------------------------------------
 // bf16 unpacking: word w holds element 2k in its low half, 2k+1 in its high.

@@ -11,10 +11,13 @@
 // Work decomposition.  One "item" is a (sequence b, position i) pair: the
 // target row i and, for i < k_b on a sampled row, the draft row i.  An item
 // runs on a thread-block cluster of C CTAs; CTA r owns the vocabulary slice
-// [r*L, (r+1)*L) of both rows and keeps it resident in its shared memory
-// (bulk-copy engine loads, one mbarrier per row).  Passes over a row (max;
-// exp-sum with the exact max; residual CDF) then read shared memory, and the
-// cluster combines per-slice partials through distributed shared memory.
+// [r*L, (r+1)*L) of both rows and streams it through a 3-stage ring in shared
+// memory fed by the bulk-copy engine (one mbarrier per stage).  Each row is
+// reduced in ONE pass: the running max, and the sum of 2^(z*c - R) where the
+// reference exponent R is an integer that only grows; when it grows the
+// partial sum is rescaled by an exact power of two, so the online pass adds
+// no rounding beyond the exponentials themselves.  The cluster combines the
+// per-slice results through distributed shared memory.
 //
 // Items are launched position-major (all sequences' position 0 first).  Each
 // item publishes {done, rejected, error} bits for its position in one 64-bit
@@ -22,9 +25,10 @@
 // sequence has been rejected exits without reading its rows: those rows
 // cannot change the result.  The item whose publication completes the
 // prefix 0..j (j = first rejection, or k_b when all were accepted) is the
-// sequence's finisher: it draws the resample / bonus token, from its own
-// resident slices when j is its own position, else after loading row(s) j.
-// No item ever waits for another one.
+// sequence's finisher: it streams row(s) j again (usually still in L2) to
+// sum the residual max(0, p - q) (or p for the bonus) per chunk, then reads
+// back the one chunk that holds the inverse-CDF point.  No item ever waits
+// for another one.
 #include <cstdint>
 #include <cstdio>
 
@@ -33,15 +37,20 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCmax = 16;
-constexpr int kMaxTiles = 24;  // slice <= 24 * 256 units of 16 B
-constexpr int kWordBits = 21;  // positions per field of the sequence word
+constexpr int kChunkUnits = 256;                   // 16-byte units of one row per chunk
+constexpr int kHalfBytes = kChunkUnits * 16;       // 4 KB of one row
+constexpr int kStageBytes = 2 * kHalfBytes;        // target half + draft half
+constexpr int kStages = 3;
+constexpr int kMaxChunks = 32;                     // slice <= 128 KB of a row per CTA
+constexpr int kUnitsPerThread = kChunkUnits / kThreads;
+constexpr int kWordBits = 21;                      // positions per field of the sequence word
 
 struct ItemStats {
-  float m_t, st_hi, st_lo, m_d;
-  float sd_hi, sd_lo;
+  float m_t, R_t, st_hi, st_lo;
+  float m_d, R_d, sd_hi, sd_lo;
   int argmax;
   uint32_t errbits;
 };
@@ -64,69 +73,56 @@ struct VerifyParams {
   uint32_t* flags;
   unsigned long long* words;
   ItemStats* stats;
-  int slice_len;      // elements per CTA slice
-  int rowbuf_bytes;   // shared-memory bytes per row buffer
+  int slice_len;  // elements per CTA slice
 };
 
 // ---------------------------------------------------------------------------
-// One CTA's slice of one logit row, mapped to 16-byte units in shared memory.
-// Unit u holds global bytes [base16 + 16u, base16 + 16u + 16); element e of
-// the row lies in unit (e*ES + row - base16) / 16.
+// One CTA's slice [e0, e1) of one logit row, in 16-byte units: unit u holds
+// global bytes [base16 + 16u, base16 + 16u + 16).  Units inside the aligned
+// body [a0, a1) are fully valid and arrive by bulk copy; the (at most two)
+// partial units at the ends are read element by element from global memory.
 // ---------------------------------------------------------------------------
 template <int ES>
-struct SliceMap {
-  const char* row;  // row start (global)
-  int e0, e1;       // elements owned by this CTA
-  uintptr_t g0, g1, base16, a0, a1;
-  int n_units;
-  int ebase0;  // element index of the first lane of unit 0 (may be < e0)
+struct RowSlice {
+  const char* row;
+  int e0, e1;
+  uintptr_t base16, a0, a1;
+  int n_units, ebase0, n_chunks;
 
   __device__ void init(const char* row_, int e0_, int e1_) {
     row = row_;
     e0 = e0_;
     e1 = e1_;
-    g0 = reinterpret_cast<uintptr_t>(row) + (uintptr_t)e0 * ES;
-    g1 = reinterpret_cast<uintptr_t>(row) + (uintptr_t)e1 * ES;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(row) + (uintptr_t)e0 * ES;
+    const uintptr_t g1 = reinterpret_cast<uintptr_t>(row) + (uintptr_t)e1 * ES;
     base16 = g0 & ~uintptr_t(15);
     a0 = (g0 + 15) & ~uintptr_t(15);
     a1 = g1 & ~uintptr_t(15);
     if (a1 < a0) a1 = a0;
     n_units = e1 > e0 ? (int)((g1 - base16 + 15) / 16) : 0;
     ebase0 = e0 - (int)((g0 & 15) / ES);
+    n_chunks = (n_units + kChunkUnits - 1) / kChunkUnits;
+  }
+  __device__ __forceinline__ bool unit_bulk(int u) const {
+    const uintptr_t a = base16 + 16 * (uintptr_t)u;
+    return a >= a0 && a + 16 <= a1;
+  }
+    // units [ub0, ub1) are fully inside the aligned body
+  __device__ __forceinline__ int ub0() const { return (int)((a0 - base16) / 16); }
+  __device__ __forceinline__ int ub1() const { return (int)((a1 - base16) / 16); }
+  // bulk-copied byte range of chunk c
+  __device__ __forceinline__ void chunk_body(int c, uintptr_t* lo, uintptr_t* hi) const {
+    const uintptr_t c0 = base16 + (uintptr_t)c * kHalfBytes, c1 = c0 + kHalfBytes;
+    *lo = c0 > a0 ? c0 : a0;
+    *hi = c1 < a1 ? c1 : a1;
+    if (*hi < *lo) *hi = *lo;
+  }
+  __device__ __forceinline__ float elem(int e) const {  // from global memory
+    return ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2))
+                   : *reinterpret_cast<const float*>(row + (size_t)e * 4);
   }
 };
 
-// Issue the loads of a slice into `buf`: the 16-byte-aligned body with bulk
-// copies on `bar` (thread 0), the unaligned head and tail with plain loads
-// (all threads).  Returns nothing; consumers wait on `bar` and a
-// __syncthreads() that follows this call.
-template <int ES>
-__device__ void issue_slice(const SliceMap<ES>& s, char* buf, uint64_t* bar) {
-  const int tid = threadIdx.x;
-  const uint32_t body = (uint32_t)(s.a1 - s.a0);
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, body);
-    constexpr uint32_t kChunk = 8192;
-    for (uint32_t off = 0; off < body; off += kChunk) {
-      uint32_t n = body - off < kChunk ? body - off : kChunk;
-      bulk_copy_g2s(buf + (s.a0 - s.base16) + off, reinterpret_cast<const void*>(s.a0 + off), n,
-                    bar);
-    }
-  }
-  // head [g0, a0) and tail [a1, g1) (or everything when there is no body)
-  const int n_head = (int)((body ? s.a0 : s.g1) - s.g0) / ES;
-  const int n_tail = body ? (int)(s.g1 - s.a1) / ES : 0;
-  for (int k = tid; k < n_head + n_tail; k += kThreads) {
-    uintptr_t ga = k < n_head ? s.g0 + (uintptr_t)k * ES : s.a1 + (uintptr_t)(k - n_head) * ES;
-    char* dst = buf + (ga - s.base16);
-    if (ES == 2)
-      *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(ga);
-    else
-      *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(ga);
-  }
-}
-
-// element j (0..16/ES-1) of a 16-byte unit as float
 template <int ES>
 __device__ __forceinline__ float unit_elem(const uint4& v, int j) {
   if (ES == 4) {
@@ -138,195 +134,359 @@ __device__ __forceinline__ float unit_elem(const uint4& v, int j) {
   }
 }
 
+// max that propagates NaN (one instruction)
 __device__ __forceinline__ float nanmax(float a, float b) {
-  return (a != a || b != b) ? __int_as_float(0x7fc00000) : fmaxf(a, b);
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
-// Row max of a slice held in shared memory (NaN propagates).
+// "no finite element yet" value of the reference exponent R: finite, so that
+// z*c - R stays -inf (never NaN) for z = -inf, and far below any real R.
+constexpr float kRnone = -3.0e38f;
+
+// max of a full unit, NaN-propagating
 template <int ES>
-__device__ float slice_max(const SliceMap<ES>& s, const char* buf) {
-  constexpr int EPU = 16 / ES;
-  float m = -__int_as_float(0x7f800000);
+__device__ __forceinline__ float unit_max(const uint4& v) {
   if (ES == 2) {
-    __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-    for (int u = threadIdx.x; u < s.n_units; u += kThreads) {
-      uint4 v = *reinterpret_cast<const uint4*>(buf + 16 * u);
-      int eb = s.ebase0 + u * EPU;
-      if (eb >= s.e0 && eb + EPU <= s.e1) {
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-        m2 = __hmax2_nan(m2, __hmax2_nan(__hmax2_nan(p[0], p[1]), __hmax2_nan(p[2], p[3])));
-      } else {
-        for (int j = 0; j < EPU; ++j)
-          if (eb + j >= s.e0 && eb + j < s.e1) m = nanmax(m, unit_elem<ES>(v, j));
-      }
-    }
-    m = nanmax(m, nanmax(__low2float(m2), __high2float(m2)));
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+    __nv_bfloat162 m2 = __hmax2_nan(__hmax2_nan(p[0], p[1]), __hmax2_nan(p[2], p[3]));
+    return nanmax(__low2float(m2), __high2float(m2));
   } else {
-    bool nan = false;
-    for (int u = threadIdx.x; u < s.n_units; u += kThreads) {
-      uint4 v = *reinterpret_cast<const uint4*>(buf + 16 * u);
-      int eb = s.ebase0 + u * EPU;
-#pragma unroll
-      for (int j = 0; j < EPU; ++j) {
-        float z = unit_elem<ES>(v, j);
-        bool ok = eb + j >= s.e0 && eb + j < s.e1;
-        if (ok) {
-          nan |= (z != z);
-          m = fmaxf(m, z);
-        }
-      }
-    }
-    if (nan) m = __int_as_float(0x7fc00000);
+    float a = __uint_as_float(v.x), b = __uint_as_float(v.y), c = __uint_as_float(v.z),
+          d = __uint_as_float(v.w);
+    return nanmax(nanmax(a, b), nanmax(c, d));
   }
-  return m;
 }
 
-// exp((z - m)/T) as 2^((z - m) * c) with c = log2(e)/T held as hi + lo, so
-// the temperature is applied without a rounded reciprocal.  d is clamped at
-// dmin (where the result underflows anyway) so that -inf logits give 0.
+// c = log2(e)/T as chi + clo with chi <= c (so clo > 0), from float operations
+// only: q1 = hi/T, then the quotient of the exact remainder.  exp((z - m)/T)
+// is then 2^(z*chi + z*clo - m*c), and no rounded reciprocal of T enters it.
+constexpr float kLog2eHi = 1.44269502162933349609375f;
+constexpr float kLog2eLo = 1.925963033500011079e-08f;
+
 struct Expo {
-  float m, chi, clo, dmin;
-  __device__ __forceinline__ float operator()(float z) const {
-    float d = fmaxf(z - m, dmin);
-    return ex2(fmaf(d, chi, d * clo));
+  float chi, clo;
+};
+
+__device__ __forceinline__ Expo make_expo(float T) {
+  const float q1 = __fdiv_rn(kLog2eHi, T);
+  const float r = __fadd_rn(__fmaf_rn(-q1, T, kLog2eHi), kLog2eLo);
+  const float q2 = __fdiv_rn(r, T);
+  float hi = __fadd_rn(q1, q2);
+  float lo = __fsub_rn(q2, __fsub_rn(hi, q1));
+  if (lo < 0.f) {  // step hi one ulp down so that lo is positive
+    const float h2 = __int_as_float(__float_as_int(hi) - 1);
+    lo = __fadd_rn(lo, __fsub_rn(hi, h2));
+    hi = h2;
   }
-  __device__ __forceinline__ double arg_exact(float z) const {
-    return ((double)z - (double)m) * ((double)chi + (double)clo);
+  if (!(lo > 0.f)) lo = 1e-30f;  // keeps -inf * lo = -inf (never NaN)
+  return Expo{hi, lo};
+}
+
+// base-2 exponent of element z against reference R: z*c - R, one rounding
+// for the large part (FMA), the small correction z*clo added after.
+__device__ __forceinline__ float earg(float z, const Expo& x, float R) {
+  return __fmaf_rn(z, x.clo, __fmaf_rn(z, x.chi, -R));
+}
+
+// 2^k for an integer-valued k <= 0; 0 below 2^-126.
+__device__ __forceinline__ float pow2i(float k) {
+  if (!(k >= -126.f)) return 0.f;
+  return __int_as_float((127 + (int)k) << 23);
+}
+
+// ---------------------------------------------------------------------------
+// Per-thread row accumulator
+// ---------------------------------------------------------------------------
+struct RowAcc {
+  float mx;  // running max of the raw logits (NaN propagates)
+  float R;   // integer reference exponent, kRnone until a finite element
+  DF s;      // sum of 2^(z*c - R)
+  int amax;  // index of the first maximum (greedy rows)
+};
+
+__device__ __forceinline__ RowAcc acc_init() {
+  return RowAcc{-INFINITY, kRnone, DF{0.f, 0.f}, 0x7fffffff};
+}
+
+__device__ __forceinline__ void acc_raise(RowAcc& a, float Rn) {
+  const float p = pow2i(a.R - Rn);  // exact power of two (0 from kRnone)
+  a.s.hi *= p;
+  a.s.lo *= p;
+  a.R = Rn;
+}
+
+__device__ __forceinline__ float e2(float z, const Expo& x, float nR) {
+  return ex2(__fmaf_rn(z, x.clo, __fmaf_rn(z, x.chi, nR)));
+}
+
+// 2^(z*c - R) for a pair of logits held as an f32x2 (same arithmetic as e2)
+__device__ __forceinline__ F2 e2x2(F2 z, F2 C, F2 L, F2 N) {
+  float p, q;
+  f2_unpack(f2_fma(z, L, f2_fma(z, C, N)), p, q);
+  return f2_pack(ex2(p), ex2(q));
+}
+
+__device__ __forceinline__ F2 bf16x2_to_f2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
+
+template <int ES>
+__device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
+  const float g = unit_max<ES>(v);
+  a.mx = nanmax(a.mx, g);
+  const float gc = g * x.chi;
+  if (gc > a.R) acc_raise(a, ceilf(gc));
+  const F2 C = f2_pack(x.chi, x.chi), L = f2_pack(x.clo, x.clo);
+  const F2 N = f2_pack(-a.R, -a.R);
+  F2 s;
+  if (ES == 2) {
+    const F2 e0 = e2x2(bf16x2_to_f2(v.x), C, L, N), e1 = e2x2(bf16x2_to_f2(v.y), C, L, N);
+    const F2 e2_ = e2x2(bf16x2_to_f2(v.z), C, L, N), e3 = e2x2(bf16x2_to_f2(v.w), C, L, N);
+    s = f2_add(f2_add(e0, e1), f2_add(e2_, e3));
+  } else {
+    const F2 e0 = e2x2(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)), C, L, N);
+    const F2 e1 = e2x2(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)), C, L, N);
+    s = f2_add(e0, e1);
+  }
+  float sx, sy;
+  f2_unpack(s, sx, sy);
+  df_acc(a.s, sx + sy);
+}
+
+__device__ __forceinline__ void sampled_elem(RowAcc& a, float z, const Expo& x) {
+  a.mx = nanmax(a.mx, z);
+  const float zc = z * x.chi;
+  if (zc > a.R) acc_raise(a, ceilf(zc));
+  df_acc(a.s, e2(z, x, -a.R));
+}
+
+template <int ES>
+__device__ __forceinline__ void greedy_unit(RowAcc& a, const uint4& v, int eb) {
+  constexpr int EPU = 16 / ES;
+  const float g = unit_max<ES>(v);
+  if (g != g) {
+    a.mx = g;
+  } else if (g > a.mx) {  // strict: the first occurrence in index order stays
+    int first = EPU - 1;
+#pragma unroll
+    for (int j = EPU - 1; j >= 0; --j)
+      if (unit_elem<ES>(v, j) == g) first = j;
+    a.mx = g;
+    a.amax = eb + first;
+  }
+}
+
+__device__ __forceinline__ void greedy_elem(RowAcc& a, float z, int e) {
+  if (z != z) {
+    a.mx = z;
+  } else if (z > a.mx) {
+    a.mx = z;
+    a.amax = e;
+  }
+}
+
+template <int ES>
+__device__ __forceinline__ void row_unit(RowAcc& a, const RowSlice<ES>& rs, const char* half, int c,
+                                         int u, int ub0, int ub1, bool greedy, const Expo& x) {
+  constexpr int EPU = 16 / ES;
+  const int eb = rs.ebase0 + u * EPU;
+  if (u >= ub0 && u < ub1) {
+    const uint4 v = *reinterpret_cast<const uint4*>(half + 16 * (u - c * kChunkUnits));
+    if (greedy)
+      greedy_unit<ES>(a, v, eb);
+    else
+      sampled_unit<ES>(a, v, x);
+  } else if (u < rs.n_units) {
+    for (int j = 0; j < EPU; ++j) {
+      const int e = eb + j;
+      if (e < rs.e0 || e >= rs.e1) continue;
+      const float z = rs.elem(e);
+      if (greedy)
+        greedy_elem(a, z, e);
+      else
+        sampled_elem(a, z, x);
+    }
+  }
+}
+
+// Combine row accumulators over the lanes of a warp (lanes with valid ==
+// false contribute nothing).  The butterfly leaves the same bits on every
+// lane, so every CTA that combines the same values gets the same result.
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_nanmax(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = nanmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_min(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ RowAcc lanes_combine(RowAcc v, bool valid, bool greedy) {
+  if (!valid) v = acc_init();
+  const float m = warp_nanmax(v.mx);
+  if (greedy) {
+    const int cand = (v.mx == m) ? v.amax : 0x7fffffff;
+    return RowAcc{m, -INFINITY, DF{0.f, 0.f}, warp_min(cand)};
+  }
+  const float Rw = warp_maxf(v.R);
+  DF s = DF{0.f, 0.f};
+  if (v.R > kRnone && Rw > kRnone) {
+    const float p = pow2i(v.R - Rw);
+    s = DF{v.s.hi * p, v.s.lo * p};
+  }
+  s = df_warp_sum(s);
+  return RowAcc{m, Rw, s, 0x7fffffff};
+}
+
+__device__ __forceinline__ DF df_shfl(DF v, int src) {
+  return DF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// Inclusive prefix over lanes in double-float.
+__device__ __forceinline__ DF df_warp_scan(DF v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    DF n = DF{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = df_add(v, n);
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Residual / bonus weights: w = max(0, e_t - rho * e_d) with e = 2^(z*c - R)
+// and rho = S_t / S_d (hi + lo), or e_t alone ("p only": the bonus, or the
+// all-zero residual fallback).  w / S_t = max(0, p - q).
+// ---------------------------------------------------------------------------
+struct Weight {
+  Expo x;
+  float Rt, Rd, rho_hi, rho_lo;
+  bool p_only;
+  __device__ __forceinline__ float operator()(float zt, float zd) const {
+    const float a = e2(zt, x, -Rt);
+    if (p_only) return a;
+    const float b = e2(zd, x, -Rd);
+    return fmaxf(0.f, __fmaf_rn(-rho_lo, b, __fmaf_rn(-rho_hi, b, a)));
+  }
+  __device__ __forceinline__ float pair(float zt, float zd) const {
+    const float a = e2(zt, x, -Rt), b = e2(zd, x, -Rd);
+    return fmaxf(0.f, __fmaf_rn(-rho_lo, b, __fmaf_rn(-rho_hi, b, a)));
+  }
+  // two elements at once (f32x2), lane by lane the same arithmetic as pair()
+  __device__ __forceinline__ float pair2(F2 zt, F2 zd, F2 C, F2 L, F2 Nt, F2 Nd, F2 RH,
+                                         F2 RL) const {
+    const F2 a = e2x2(zt, C, L, Nt), b = e2x2(zd, C, L, Nd);
+    float w0, w1;
+    f2_unpack(f2_fma(RL, b, f2_fma(RH, b, a)), w0, w1);
+    return fmaxf(0.f, w0) + fmaxf(0.f, w1);
   }
 };
 
-__device__ Expo make_expo(float m, float T) {
-  double c = 1.4426950408889634074 / (double)T;
-  Expo e;
-  e.m = m;
-  e.chi = (float)c;
-  e.clo = (float)(c - (double)e.chi);
-  e.dmin = -256.0f / e.chi;
-  return e;
-}
-
-// Sum of exp over a slice (double-float).
+// Sum of the weights of unit u (target units), with the draft read from its
+// own half when both rows share the 16-byte phase, else element-wise.
 template <int ES>
-__device__ DF slice_sumexp(const SliceMap<ES>& s, const char* buf, const Expo& ex) {
+__device__ __forceinline__ float unit_wsum(const RowSlice<ES>& st, const RowSlice<ES>& sd,
+                                           const char* ht, const char* hd, int c, int u,
+                                           const Weight& W, bool same_phase) {
   constexpr int EPU = 16 / ES;
-  DF acc{0.f, 0.f};
-  for (int u = threadIdx.x; u < s.n_units; u += kThreads) {
-    uint4 v = *reinterpret_cast<const uint4*>(buf + 16 * u);
-    int eb = s.ebase0 + u * EPU;
-    float e[EPU];
-    if (eb >= s.e0 && eb + EPU <= s.e1) {
-#pragma unroll
-      for (int j = 0; j < EPU; ++j) e[j] = ex(unit_elem<ES>(v, j));
-    } else {
-#pragma unroll
-      for (int j = 0; j < EPU; ++j)
-        e[j] = (eb + j >= s.e0 && eb + j < s.e1) ? ex(unit_elem<ES>(v, j)) : 0.f;
+  if (u >= st.n_units) return 0.f;
+  const int eb = st.ebase0 + u * EPU;
+  if (st.unit_bulk(u) && (W.p_only || same_phase)) {
+    const int off = 16 * (u - c * kChunkUnits);
+    const uint4 vt = *reinterpret_cast<const uint4*>(ht + off);
+    if (W.p_only) {
+      const float nR = -W.Rt;
+      if (ES == 2) {
+        const float e0 = e2(bf16_lo(vt.x), W.x, nR), e1 = e2(bf16_hi(vt.x), W.x, nR);
+        const float f0 = e2(bf16_lo(vt.y), W.x, nR), f1 = e2(bf16_hi(vt.y), W.x, nR);
+        const float g0 = e2(bf16_lo(vt.z), W.x, nR), g1 = e2(bf16_hi(vt.z), W.x, nR);
+        const float h0 = e2(bf16_lo(vt.w), W.x, nR), h1 = e2(bf16_hi(vt.w), W.x, nR);
+        return ((e0 + e1) + (f0 + f1)) + ((g0 + g1) + (h0 + h1));
+      }
+      const float e0 = e2(__uint_as_float(vt.x), W.x, nR), e1 = e2(__uint_as_float(vt.y), W.x, nR);
+      const float f0 = e2(__uint_as_float(vt.z), W.x, nR), f1 = e2(__uint_as_float(vt.w), W.x, nR);
+      return (e0 + e1) + (f0 + f1);
     }
-    float us;
-    if (EPU == 8)
-      us = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    else
-      us = (e[0] + e[1]) + (e[2] + e[3]);
-    df_acc(acc, us);
+    const uint4 vd = *reinterpret_cast<const uint4*>(hd + off);
+    const F2 C = f2_pack(W.x.chi, W.x.chi), L = f2_pack(W.x.clo, W.x.clo);
+    const F2 Nt = f2_pack(-W.Rt, -W.Rt), Nd = f2_pack(-W.Rd, -W.Rd);
+    const F2 RH = f2_pack(-W.rho_hi, -W.rho_hi), RL = f2_pack(-W.rho_lo, -W.rho_lo);
+    if (ES == 2) {
+      const float e = W.pair2(bf16x2_to_f2(vt.x), bf16x2_to_f2(vd.x), C, L, Nt, Nd, RH, RL);
+      const float f = W.pair2(bf16x2_to_f2(vt.y), bf16x2_to_f2(vd.y), C, L, Nt, Nd, RH, RL);
+      const float g = W.pair2(bf16x2_to_f2(vt.z), bf16x2_to_f2(vd.z), C, L, Nt, Nd, RH, RL);
+      const float h = W.pair2(bf16x2_to_f2(vt.w), bf16x2_to_f2(vd.w), C, L, Nt, Nd, RH, RL);
+      return (e + f) + (g + h);
+    }
+    const float e = W.pair2(f2_pack(__uint_as_float(vt.x), __uint_as_float(vt.y)),
+                            f2_pack(__uint_as_float(vd.x), __uint_as_float(vd.y)), C, L, Nt, Nd, RH, RL);
+    const float f = W.pair2(f2_pack(__uint_as_float(vt.z), __uint_as_float(vt.w)),
+                            f2_pack(__uint_as_float(vd.z), __uint_as_float(vd.w)), C, L, Nt, Nd, RH, RL);
+    return e + f;
+  }
+  float acc = 0.f;
+  for (int j = 0; j < EPU; ++j) {
+    const int e = eb + j;
+    if (e < st.e0 || e >= st.e1) continue;
+    acc += W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
   }
   return acc;
 }
 
-// Residual / bonus weight of one element: w' = max(0, e_t - rho * e_d) with
-// rho = S_t/S_d (hi + lo), or e_t alone when rho_hi < 0 marks "p only".
-struct Weight {
-  Expo et, ed;
-  float rho_hi, rho_lo;
-  bool p_only;
-  __device__ __forceinline__ float operator()(float zt, float zd) const {
-    float a = et(zt);
-    if (p_only) return a;
-    float b = ed(zd);
-    return fmaxf(0.f, fmaf(-rho_lo, b, fmaf(-rho_hi, b, a)));
-  }
-};
-
-// Element e of a slice read back from shared memory one at a time (used when
-// the draft row's 16-byte phase differs from the target row's).
+// weight of element e of unit u (same reads as unit_wsum)
 template <int ES>
-__device__ __forceinline__ float slice_elem(const SliceMap<ES>& s, const char* buf, int e) {
-  const char* p = buf + (s.g0 - s.base16) + (size_t)(e - s.e0) * ES;
-  return ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(p))
-                 : *reinterpret_cast<const float*>(p);
-}
-
-// Target and draft slices of one position: unit u of the target buffer holds
-// elements [ebase0 + u*EPU, ...).  When both rows start at the same offset
-// modulo 16 bytes the draft buffer's unit u holds the same elements.
-template <int ES>
-struct PairMap {
-  const SliceMap<ES>* st;
-  const SliceMap<ES>* sd;
-  bool same_phase;
-};
-
-template <int ES>
-__device__ __forceinline__ float unit_weight_sum(const PairMap<ES>& pm, const char* bt,
-                                                 const char* bd, int u, const Weight& W) {
+__device__ __forceinline__ float elem_w(const RowSlice<ES>& st, const RowSlice<ES>& sd,
+                                        const char* ht, const char* hd, int c, int u, int e,
+                                        const Weight& W, bool same_phase) {
   constexpr int EPU = 16 / ES;
-  const SliceMap<ES>& s = *pm.st;
-  if (u >= s.n_units) return 0.f;
-  uint4 vt = *reinterpret_cast<const uint4*>(bt + 16 * u);
-  const bool vec_d = W.p_only || pm.same_phase;
-  uint4 vd = vec_d ? (W.p_only ? vt : *reinterpret_cast<const uint4*>(bd + 16 * u)) : vt;
-  int eb = s.ebase0 + u * EPU;
-  float e[EPU];
-  bool full = eb >= s.e0 && eb + EPU <= s.e1;
-#pragma unroll
-  for (int j = 0; j < EPU; ++j) {
-    bool ok = full || (eb + j >= s.e0 && eb + j < s.e1);
-    float zd = 0.f;
-    if (ok) zd = vec_d ? unit_elem<ES>(vd, j) : slice_elem<ES>(*pm.sd, bd, eb + j);
-    e[j] = ok ? W(unit_elem<ES>(vt, j), zd) : 0.f;
+  if (st.unit_bulk(u) && (W.p_only || same_phase)) {
+    const int off = 16 * (u - c * kChunkUnits);
+    const uint4 vt = *reinterpret_cast<const uint4*>(ht + off);
+    const uint4 vd = W.p_only ? vt : *reinterpret_cast<const uint4*>(hd + off);
+    const int j = e - (st.ebase0 + u * EPU);
+    return W(unit_elem<ES>(vt, j), unit_elem<ES>(vd, j));
   }
-  if (EPU == 8) return ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-  return (e[0] + e[1]) + (e[2] + e[3]);
-}
-
-// Per-tile (256 units), per-warp partial sums of the weights of a slice.
-template <int ES>
-__device__ void slice_weight_partials(const PairMap<ES>& pm, const char* bt, const char* bd,
-                                      const Weight& W, DF (*tw)[kWarps]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = (pm.st->n_units + kThreads - 1) / kThreads;
-  for (int t = 0; t < tiles; ++t) {
-    float us = unit_weight_sum<ES>(pm, bt, bd, t * kThreads + threadIdx.x, W);
-    DF v = df_warp_sum(DF{us, 0.f});
-    if (lane == 0) tw[t][warp] = v;
-  }
+  return W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
 }
 
 struct Shared {
-  uint64_t bar[2];
-  uint32_t bar_phase[2];
+  uint64_t full[kStages];
   // all-gather slots, indexed by the writing CTA's rank
-  float g_mt[kCmax], g_md[kCmax];
-  DF g_st[kCmax], g_sd[kCmax], g_w[kCmax];
-  int g_amax[kCmax];
-  // block reduction scratch
-  float r_f[kWarps][2];
-  DF r_df[kWarps][2];
+  RowAcc g_t[kCmax], g_d[kCmax];
+  DF g_w[kCmax];
+  // per-warp partials
+  RowAcc r_t[kWarps], r_d[kWarps];
+  DF tw[kMaxChunks][kWarps];
+  DF scan[2][kWarps];
   int r_i[kWarps];
-  DF tw[kMaxTiles][kWarps];
-  // broadcast values
-  int skip;
+  // item scalars, written by warp 0 and read by the whole CTA
+  RowAcc row_t, row_d;
+  DF S_w;
+  int skip, skip_seen;
   int fin, fin_j, fin_err;
-  float bc_f[4];
+  int owner, csel;
+  DF rem;
+  int timeout;
+  int x;
+  float u_i, zt_x, zd_x;
 };
 
 __device__ __forceinline__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
   const unsigned long long mask = (1ull << kWordBits) - 1;
-  unsigned long long D = w & mask;
-  unsigned long long Rj = (w >> kWordBits) & mask;
-  unsigned long long E = (w >> (2 * kWordBits)) & mask;
-  unsigned long long R = Rj | E;
-  int j = R ? __ffsll((long long)R) - 1 : kb;
-  unsigned long long need = (j + 1 >= 64) ? ~0ull : ((1ull << (j + 1)) - 1);
+  const unsigned long long D = w & mask;
+  const unsigned long long Rj = (w >> kWordBits) & mask;
+  const unsigned long long E = (w >> (2 * kWordBits)) & mask;
+  const unsigned long long R = Rj | E;
+  const int j = R ? __ffsll((long long)R) - 1 : kb;
+  const unsigned long long need = (j + 1 >= 64) ? ~0ull : ((1ull << (j + 1)) - 1);
   *j_out = j;
   *err = (E >> j) & 1;
   return (D & need) == need;
@@ -342,8 +502,63 @@ __device__ void write_outputs(const VerifyParams& P, int b, int n, int y, bool e
   P.nacc[b] = err ? 0 : n;
 }
 
+// ---------------------------------------------------------------------------
+// The ring: chunk c of the current pass is ring entry q = q0 + c, stage
+// q % kStages, mbarrier phase (q / kStages) & 1.  Thread 0 issues the bulk
+// copies and waits; the others sleep at the CTA barrier.
+// ---------------------------------------------------------------------------
 template <int ES>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) {
+__device__ __forceinline__ void ring_issue(Shared& sh, char* ring, uint32_t q, int c,
+                                           const RowSlice<ES>& st, bool with_d,
+                                           const RowSlice<ES>& sd) {
+  const int s = q % kStages;
+  char* stage = ring + s * kStageBytes;
+  uintptr_t tl = 0, th = 0, dl = 0, dh = 0;
+  if (c < st.n_chunks) st.chunk_body(c, &tl, &th);
+  if (with_d && c < sd.n_chunks) sd.chunk_body(c, &dl, &dh);
+  mbar_arrive_expect_tx(&sh.full[s], (uint32_t)((th - tl) + (dh - dl)));
+  if (th > tl)
+    bulk_copy_g2s(stage + (tl - (st.base16 + (uintptr_t)c * kHalfBytes)),
+                  reinterpret_cast<const void*>(tl), (uint32_t)(th - tl), &sh.full[s]);
+  if (dh > dl)
+    bulk_copy_g2s(stage + kHalfBytes + (dl - (sd.base16 + (uintptr_t)c * kHalfBytes)),
+                  reinterpret_cast<const void*>(dl), (uint32_t)(dh - dl), &sh.full[s]);
+}
+
+// Stream chunks 0..NC-1 of (st[, sd]) and call body(c, stage) for each, with
+// every thread.  Returns false if a bounded wait ran out (the caller reports
+// SV_FLAG_TIMEOUT and treats the data as invalid).
+template <int ES, typename Body>
+__device__ __forceinline__ bool ring_pass(Shared& sh, char* ring, uint32_t& q0, int NC,
+                                          const RowSlice<ES>& st, bool with_d,
+                                          const RowSlice<ES>& sd, Body body) {
+  const int tid = threadIdx.x;
+  if (tid == 0)
+    for (int c = 0; c < NC && c < kStages; ++c) ring_issue<ES>(sh, ring, q0 + c, c, st, with_d, sd);
+  bool ok_all = true;
+  for (int c = 0; c < NC; ++c) {
+    const uint32_t q = q0 + c;
+    const int s = q % kStages;
+    const uint32_t par = (q / kStages) & 1;
+    bool ok = true;
+    if (tid == 0) ok = mbar_wait_bounded(&sh.full[s], par);
+    // everyone is done with chunk c-1 and chunk c has landed
+    if (__syncthreads_or(!ok)) {
+      ok_all = false;
+      break;
+    }
+    if (tid == 0 && c >= 1 && c - 1 + kStages < NC)
+      ring_issue<ES>(sh, ring, q + kStages - 1, c - 1 + kStages, st, with_d, sd);
+    mbar_try_wait(&sh.full[s], par);  // this thread's acquire of the landed data
+    body(c, ring + s * kStageBytes);
+  }
+  __syncthreads();
+  q0 += NC;
+  return ok_all;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -351,9 +566,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   const int item = blockIdx.x / C;
   const int i = item / P.B, b = item % P.B;
 
-  extern __shared__ __align__(128) char dyn[];
-  char* buf_t = dyn;
-  char* buf_d = dyn + P.rowbuf_bytes;
+  extern __shared__ __align__(128) char ring[];
   __shared__ Shared sh;
 
   // ---- per-row parameters (identical in every CTA of the cluster) ----
@@ -375,205 +588,164 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   if (i > kb) return;
   const bool greedy = md == 1;
   const bool has_draft = !greedy && i < kb;
+  const Expo X = greedy ? Expo{1.f, 1e-30f} : make_expo(T);
 
-  // Every CTA of the cluster must be running before any distributed
-  // shared-memory access: arrive now, wait after the local set-up.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // ---- set-up; rank 0 reads the sequence word ----
   if (tid == 0) {
-    mbar_init(&sh.bar[0], 1);
-    mbar_init(&sh.bar[1], 1);
-    sh.bar_phase[0] = sh.bar_phase[1] = 0;
+    for (int s = 0; s < kStages; ++s) mbar_init(&sh.full[s], 1);
     fence_mbar_init();
-  }
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  // ---- agree on skipping: an earlier position already rejected ----
-  if (rank == 0 && tid == 0) {
-    unsigned long long w = __ldcg(P.words + b);
-    unsigned long long R = ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
-    int skip = (R & ((1ull << i) - 1)) != 0;
-    for (int r = 0; r < C; ++r) *cluster.map_shared_rank(&sh.skip, r) = skip;
-  }
-  cluster.sync();
-  if (sh.skip) return;
-
-  // ---- load the slices ----
-  const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
-  SliceMap<ES> st, sd;
-  st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
-  issue_slice<ES>(st, buf_t, &sh.bar[0]);
-  if (has_draft) {
-    sd.init(P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos, e0, e1);
-    issue_slice<ES>(sd, buf_d, &sh.bar[1]);
-  }
-  __syncthreads();
-  bool timed_out = false;
-  timed_out |= !mbar_wait_bounded(&sh.bar[0], 0);
-  if (has_draft) timed_out |= !mbar_wait_bounded(&sh.bar[1], 0);
-  if (timed_out && tid == 0) atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
-  if (tid == 0) {
-    sh.bar_phase[0] = 1;
-    if (has_draft) sh.bar_phase[1] = 1;
-  }
-
-  // ---- pass 1: row maxima ----
-  float mt = slice_max<ES>(st, buf_t);
-  float mdx = has_draft ? slice_max<ES>(sd, buf_d) : -INFINITY;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mt = nanmax(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-    mdx = nanmax(mdx, __shfl_xor_sync(0xffffffffu, mdx, o));
-  }
-  if (lane == 0) {
-    sh.r_f[warp][0] = mt;
-    sh.r_f[warp][1] = mdx;
-  }
-  __syncthreads();
-  if (tid < C) {
-    float a = sh.r_f[0][0], d = sh.r_f[0][1];
-    for (int w = 1; w < kWarps; ++w) {
-      a = nanmax(a, sh.r_f[w][0]);
-      d = nanmax(d, sh.r_f[w][1]);
+    if (rank == 0) {
+      const unsigned long long w = __ldcg(P.words + b);
+      const unsigned long long R =
+          ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
+      sh.skip = (R & ((1ull << i) - 1)) != 0;
     }
-    if (timed_out) a = __int_as_float(0x7fc00000);
-    *cluster.map_shared_rank(&sh.g_mt[rank], tid) = a;
-    *cluster.map_shared_rank(&sh.g_md[rank], tid) = d;
   }
+  // every CTA is running (distributed shared memory is safe) and rank 0's
+  // skip flag is visible to all of them
   cluster.sync();
-  float m_t = sh.g_mt[0], m_d = sh.g_md[0];
-  for (int r = 1; r < C; ++r) {
-    m_t = nanmax(m_t, sh.g_mt[r]);
-    m_d = nanmax(m_d, sh.g_md[r]);
+  if (tid == 0) sh.skip_seen = *cluster.map_shared_rank(&sh.skip, 0);
+  __syncthreads();
+  if (sh.skip_seen) {
+    cluster.sync();  // rank 0 stays until every CTA has read its flag
+    return;
   }
-  // Row validity: no NaN, no +inf, not all -inf.
-  const bool bad_t = !(m_t > -INFINITY && m_t < INFINITY);
-  const bool bad_d = has_draft && !(m_d > -INFINITY && m_d < INFINITY);
-  // (a bounded-wait timeout poisoned its CTA's max with NaN above)
-
-  uint32_t errbits = 0;
-  if (bad_t || bad_d) errbits |= SV_FLAG_NONFINITE;
-  int x = -1;
-  if (i < kb) {
-    x = P.tokens[(size_t)b * P.K + i];
-    if (x < 0 || x >= P.V) errbits |= SV_FLAG_BAD_TOKEN;
-  }
-  bool reject = false;
-  int amax = -1;
-  float diag_px = NAN, diag_qx = NAN, diag_r = NAN;
-  DF S_t{0.f, 0.f}, S_d{0.f, 0.f};
-  Expo ext{}, exd{};
-
-  if (greedy) {
-    // ---- pass 2 (greedy): lowest index holding the max ----
-    int best = 0x7fffffff;
-    if (!bad_t) {
-      constexpr int EPU = 16 / ES;
-      for (int u = tid; u < st.n_units && best == 0x7fffffff; u += kThreads) {
-        uint4 v = *reinterpret_cast<const uint4*>(buf_t + 16 * u);
-        int eb = st.ebase0 + u * EPU;
-        for (int j = 0; j < EPU; ++j) {
-          int e = eb + j;
-          if (e >= st.e0 && e < st.e1 && unit_elem<ES>(v, j) == m_t) {
-            best = e;
-            break;
-          }
+  // decision inputs, fetched by one thread of warp 1 while the rows stream
+  if (rank == 0 && tid == 32) {
+    int x = -1;
+    float u = 0.f, zt = 0.f, zd = 0.f;
+    if (i < kb) {
+      x = P.tokens[(size_t)b * P.K + i];
+      if (!greedy) u = P.unif[(size_t)b * (P.K + 1) + i];
+      if (x >= 0 && x < P.V) {
+        const char* rt = P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos;
+        zt = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rt + (size_t)x * 2))
+                     : *reinterpret_cast<const float*>(rt + (size_t)x * 4);
+        if (has_draft) {
+          const char* rd = P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos;
+          zd = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rd + (size_t)x * 2))
+                       : *reinterpret_cast<const float*>(rd + (size_t)x * 4);
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
-    if (lane == 0) sh.r_i[warp] = best;
-    __syncthreads();
-    if (tid < C) {
-      int a = sh.r_i[0];
-      for (int w = 1; w < kWarps; ++w) a = min(a, sh.r_i[w]);
-      *cluster.map_shared_rank(&sh.g_amax[rank], tid) = a;
-    }
-    cluster.sync();
-    amax = sh.g_amax[0];
-    for (int r = 1; r < C; ++r) amax = min(amax, sh.g_amax[r]);
-    if (i < kb && !errbits) reject = (x != amax);
-  } else {
-    // ---- pass 2 (sampled): normalisers with the exact row max ----
-    float u_i = 0.f;
-    if (i < kb) {
-      u_i = P.unif[(size_t)b * (P.K + 1) + i];
-      if (!(u_i >= 0.f && u_i < 1.f)) errbits |= SV_FLAG_BAD_UNIFORM;
-    }
-    ext = make_expo(bad_t ? 0.f : m_t, T);
-    exd = make_expo(bad_d ? 0.f : m_d, T);
-    DF at = bad_t ? DF{0.f, 0.f} : slice_sumexp<ES>(st, buf_t, ext);
-    DF ad = (has_draft && !bad_d) ? slice_sumexp<ES>(sd, buf_d, exd) : DF{0.f, 0.f};
-    at = df_warp_sum(at);
-    ad = df_warp_sum(ad);
-    if (lane == 0) {
-      sh.r_df[warp][0] = at;
-      sh.r_df[warp][1] = ad;
-    }
-    __syncthreads();
-    if (tid < C) {
-      DF a = sh.r_df[0][0], d = sh.r_df[0][1];
-      for (int w = 1; w < kWarps; ++w) {
-        a = df_add(a, sh.r_df[w][0]);
-        d = df_add(d, sh.r_df[w][1]);
-      }
-      *cluster.map_shared_rank(&sh.g_st[rank], tid) = a;
-      *cluster.map_shared_rank(&sh.g_sd[rank], tid) = d;
-    }
-    cluster.sync();
-    S_t = sh.g_st[0];
-    S_d = sh.g_sd[0];
-    for (int r = 1; r < C; ++r) {
-      S_t = df_add(S_t, sh.g_st[r]);
-      S_d = df_add(S_d, sh.g_sd[r]);
-    }
-    if (has_draft && !errbits) {
-      // ratio p(x)/q(x) = 2^(a_t - a_d) * S_d / S_t, in the exponent domain so
-      // that neither factor underflows on its own; q(x) = 0 only where the
-      // exact value underflows double precision.
-      const char* rt = P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos;
-      const char* rd = P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos;
-      float zt = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rt + (size_t)x * 2))
-                         : *reinterpret_cast<const float*>(rt + (size_t)x * 4);
-      float zd = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rd + (size_t)x * 2))
-                         : *reinterpret_cast<const float*>(rd + (size_t)x * 4);
-      double at_x = ext.arg_exact(zt), ad_x = exd.arg_exact(zd);
-      float r;
-      if (!(ad_x > -1074.0) || !(at_x > -1074.0)) {
-        r = 0.f;
-      } else {
-        float ratio_s = (float)(df_to_double(S_d) / df_to_double(S_t));
-        r = ex2((float)(at_x - ad_x)) * ratio_s;
-      }
-      diag_px = ext(zt) / S_t.hi;
-      diag_qx = exd(zd) / S_d.hi;
-      diag_r = r;
-      reject = !(u_i < r);
-    }
+    sh.x = x;
+    sh.u_i = u;
+    sh.zt_x = zt;
+    sh.zd_x = zd;
   }
 
-  // ---- publish; find out whether this item finishes the sequence ----
+  // ---- stream the slices: one pass per row ----
+  const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
+  RowSlice<ES> st, sd;
+  st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
+  if (has_draft) sd.init(P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos, e0, e1);
+  else sd = st;
+  uint32_t q0 = 0;
+  RowAcc at = acc_init(), ad = acc_init();
+  const int NC = has_draft ? max(st.n_chunks, sd.n_chunks) : st.n_chunks;
+  const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
+  const bool ok = ring_pass<ES>(sh, ring, q0, NC, st, has_draft, sd, [&](int c, const char* stage) {
+#pragma unroll
+    for (int h = 0; h < kUnitsPerThread; ++h) {
+      const int u = c * kChunkUnits + h * kThreads + tid;
+      row_unit<ES>(at, st, stage, c, u, tb0, tb1, greedy, X);
+      if (has_draft) row_unit<ES>(ad, sd, stage + kHalfBytes, c, u, db0, db1, false, X);
+    }
+  });
+  if (!ok && tid == 0) atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
+
+  // ---- combine: warps -> CTA -> cluster (warp 0 of every CTA) ----
+  {
+    const RowAcc wt = lanes_combine(at, true, greedy);
+    const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
+    if (lane == 0) {
+      sh.r_t[warp] = wt;
+      sh.r_d[warp] = wd;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    RowAcc ct = lanes_combine(lane < kWarps ? sh.r_t[lane] : acc_init(), lane < kWarps, greedy);
+    const RowAcc cd = lanes_combine(lane < kWarps ? sh.r_d[lane] : acc_init(), lane < kWarps, false);
+    if (!ok) ct.mx = __int_as_float(0x7fc00000);  // a timed-out slice poisons the row
+    if (lane < C) {
+      *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
+      *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
+    }
+  }
+  cluster.sync();
+  if (warp == 0) {
+    const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy);
+    const RowAcc rd = lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false);
+    if (lane == 0) {
+      sh.row_t = rt;
+      sh.row_d = rd;
+    }
+  }
+  __syncthreads();
+  const RowAcc row_t = sh.row_t, row_d = sh.row_d;
+  // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
+  const bool bad_t = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
+                     (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
+  const bool bad_d = has_draft && (!(row_d.mx > -INFINITY && row_d.mx < INFINITY) ||
+                                   !(row_d.R > kRnone && row_d.R < INFINITY));
+
+  // ---- decision and publication (rank 0, one thread) ----
   if (rank == 0 && tid == 0) {
+    const int x = sh.x;
+    const float u_i = sh.u_i, zt_x = sh.zt_x, zd_x = sh.zd_x;
+    uint32_t errbits = 0;
+    if (bad_t || bad_d) errbits |= SV_FLAG_NONFINITE;
+    if (i < kb && (x < 0 || x >= P.V)) errbits |= SV_FLAG_BAD_TOKEN;
+    bool reject = false;
+    float diag_px = NAN, diag_qx = NAN, diag_r = NAN;
+    if (greedy) {
+      if (i < kb && !errbits) reject = (x != row_t.amax);
+    } else if (has_draft) {
+      if (!(u_i >= 0.f && u_i < 1.f)) errbits |= SV_FLAG_BAD_UNIFORM;
+      if (!errbits) {
+        // p(x)/q(x) = 2^((z_t - z_d)*c + R_d - R_t) * S_d / S_t, formed in the
+        // exponent domain so that neither factor underflows on its own;
+        // zero where the exact probability underflows double precision.
+        const float lt = (zt_x - row_t.mx) * X.chi, ld = (zd_x - row_d.mx) * X.chi;
+        float r;
+        if (!(ld > -1074.f) || !(lt > -1074.f)) {
+          r = 0.f;
+        } else {
+          const float a = zt_x - zd_x;
+          const float ex = __fmaf_rn(a, X.chi, a * X.clo) + (row_d.R - row_t.R);
+          r = ex2(ex) * df_to_float(df_div(row_d.s, row_t.s));
+        }
+        diag_px = ex2(earg(zt_x, X, row_t.R)) / row_t.s.hi;
+        diag_qx = ex2(earg(zd_x, X, row_d.R)) / row_d.s.hi;
+        diag_r = r;
+        reject = !(u_i < r);
+      }
+    }
     ItemStats s;
-    s.m_t = m_t;
-    s.st_hi = S_t.hi;
-    s.st_lo = S_t.lo;
-    s.m_d = m_d;
-    s.sd_hi = S_d.hi;
-    s.sd_lo = S_d.lo;
-    s.argmax = amax;
+    s.m_t = row_t.mx;
+    s.R_t = row_t.R;
+    s.st_hi = row_t.s.hi;
+    s.st_lo = row_t.s.lo;
+    s.m_d = row_d.mx;
+    s.R_d = row_d.R;
+    s.sd_hi = row_d.s.hi;
+    s.sd_lo = row_d.s.lo;
+    s.argmax = row_t.amax;
     s.errbits = errbits;
     P.stats[(size_t)b * (P.K + 1) + i] = s;
     if (P.diag) {
       float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
-      dg[SV_DIAG_M_T] = m_t;
+      dg[SV_DIAG_M_T] = row_t.mx;
       if (greedy) {
-        dg[SV_DIAG_ARGMAX] = (float)amax;
-      } else {
-        dg[SV_DIAG_S_T] = S_t.hi + S_t.lo;
+        dg[SV_DIAG_ARGMAX] = (float)row_t.amax;
+      } else if (!bad_t) {
+        // normaliser relative to the row max: S_R * 2^(R - m*c)
+        dg[SV_DIAG_S_T] = df_to_float(row_t.s) * ex2(-earg(row_t.mx, X, row_t.R));
         dg[SV_DIAG_MASS_T] = 1.f;
-        if (has_draft) {
-          dg[SV_DIAG_M_D] = m_d;
-          dg[SV_DIAG_S_D] = S_d.hi + S_d.lo;
+        if (has_draft && !bad_d) {
+          dg[SV_DIAG_M_D] = row_d.mx;
+          dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
           dg[SV_DIAG_MASS_D] = 1.f;
           dg[SV_DIAG_P_X] = diag_px;
           dg[SV_DIAG_Q_X] = diag_qx;
@@ -585,13 +757,13 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
     unsigned long long bits = 1ull << i;
     if (errbits) bits |= 1ull << (2 * kWordBits + i);
     else if (reject) bits |= 1ull << (kWordBits + i);
-    unsigned long long old = atomicOr(P.words + b, bits);
+    const unsigned long long old = atomicOr(P.words + b, bits);
     __threadfence();
     int j0, j1;
     bool e0_, e1_;
-    bool was = resolvable(old, kb, &j0, &e0_);
-    bool now = resolvable(old | bits, kb, &j1, &e1_);
-    int fin = (!was && now) ? 1 : 0;
+    const bool was = resolvable(old, kb, &j0, &e0_);
+    const bool now = resolvable(old | bits, kb, &j1, &e1_);
+    const int fin = (!was && now) ? 1 : 0;
     for (int r = 0; r < C; ++r) {
       Shared* rs = cluster.map_shared_rank(&sh, r);
       rs->fin = fin;
@@ -606,7 +778,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   const int j = sh.fin_j;
   if (sh.fin_err) {
     if (rank == 0 && tid == 0) {
-      uint32_t eb = j == i ? errbits : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].errbits);
+      const uint32_t eb = __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].errbits);
       write_outputs(P, b, 0, -1, true);
       atomicOr(P.flags, eb);
     }
@@ -614,7 +786,7 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
   }
   if (greedy) {
     if (rank == 0 && tid == 0) {
-      int a = j == i ? amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].argmax);
+      const int a = j == i ? row_t.amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].argmax);
       write_outputs(P, b, j, a, false);
     }
     return;
@@ -628,146 +800,191 @@ __global__ void __launch_bounds__(kThreads) verify_kernel(const VerifyParams P) 
     return;
   }
   const bool bonus = (j == kb);
-  // statistics and resident rows of position j
-  Weight W;
+  float Rt = row_t.R, Rd = row_d.R;
+  DF S_t = row_t.s, S_d = row_d.s;
   if (j != i) {
     const ItemStats* sj = P.stats + (size_t)b * (P.K + 1) + j;
-    float jm_t = __ldcg(&sj->m_t), jm_d = __ldcg(&sj->m_d);
+    Rt = __ldcg(&sj->R_t);
+    Rd = __ldcg(&sj->R_d);
     S_t = DF{__ldcg(&sj->st_hi), __ldcg(&sj->st_lo)};
     S_d = DF{__ldcg(&sj->sd_hi), __ldcg(&sj->sd_lo)};
-    ext = make_expo(jm_t, T);
-    exd = make_expo(jm_d, T);
-    __syncthreads();  // everyone is done with the old contents
-    st.init(P.tgt + (long long)b * P.t_seq + (long long)j * P.t_pos, e0, e1);
-    issue_slice<ES>(st, buf_t, &sh.bar[0]);
-    if (!bonus) {
-      sd.init(P.drf + (long long)b * P.d_seq + (long long)j * P.d_pos, e0, e1);
-      issue_slice<ES>(sd, buf_d, &sh.bar[1]);
-    }
-    __syncthreads();
-    bool ok = mbar_wait_bounded(&sh.bar[0], sh.bar_phase[0]);
-    if (!bonus) ok &= mbar_wait_bounded(&sh.bar[1], sh.bar_phase[1]);
-    if (!ok && tid == 0) atomicOr(P.flags, SV_FLAG_TIMEOUT);
   }
-  W.et = ext;
-  W.ed = exd;
+  st.init(P.tgt + (long long)b * P.t_seq + (long long)j * P.t_pos, e0, e1);
+  if (!bonus) sd.init(P.drf + (long long)b * P.d_seq + (long long)j * P.d_pos, e0, e1);
+  else sd = st;
+  const bool same_phase = st.ebase0 == sd.ebase0;
+  const bool load_d = !bonus && same_phase;  // else the draft is read element-wise
+  Weight W;
+  W.x = X;
+  W.Rt = Rt;
+  W.Rd = Rd;
   W.p_only = bonus;
   {
-    double rho = df_to_double(S_t) / df_to_double(S_d);
-    W.rho_hi = (float)rho;
-    W.rho_lo = (float)(rho - (double)W.rho_hi);
+    const DF rho = bonus ? DF{0.f, 0.f} : df_div(S_t, S_d);
+    W.rho_hi = rho.hi;
+    W.rho_lo = rho.lo;
   }
-  const int tiles = (st.n_units + kThreads - 1) / kThreads;
-  PairMap<ES> pm;
-  pm.st = &st;
-  pm.sd = &sd;
-  pm.same_phase = bonus || st.ebase0 == sd.ebase0;
+  const int NCj = st.n_chunks;
   DF slice_w{0.f, 0.f};
   for (int pass = 0; pass < 2; ++pass) {
     if (pass) cluster.sync();  // every CTA has read the first pass's slots
-    slice_weight_partials<ES>(pm, buf_t, buf_d, W, sh.tw);
-    __syncthreads();
-    if (tid < C) {
+    const bool okp = ring_pass<ES>(sh, ring, q0, NCj, st, load_d && !W.p_only, sd,
+                                   [&](int c, const char* stage) {
+      float v = 0.f;
+#pragma unroll
+      for (int h = 0; h < kUnitsPerThread; ++h)
+        v += unit_wsum<ES>(st, sd, stage, stage + kHalfBytes, c, c * kChunkUnits + h * kThreads + tid,
+                           W, same_phase);
+      const DF wsum = df_warp_sum(DF{v, 0.f});
+      if (lane == 0) sh.tw[c][warp] = wsum;
+    });
+    if (!okp && tid == 0) atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
+    if (warp == 0) {
       DF a{0.f, 0.f};
-      for (int t = 0; t < tiles; ++t)
-        for (int w = 0; w < kWarps; ++w) a = df_add(a, sh.tw[t][w]);
-      *cluster.map_shared_rank(&sh.g_w[rank], tid) = a;
+      if (lane < NCj)
+        for (int w = 0; w < kWarps; ++w) a = df_add(a, sh.tw[lane][w]);
+      a = df_warp_sum(a);
+      if (lane < C) *cluster.map_shared_rank(&sh.g_w[rank], lane) = a;
     }
     cluster.sync();
-    DF tot = sh.g_w[0];
-    for (int r = 1; r < C; ++r) tot = df_add(tot, sh.g_w[r]);
-    if (tot.hi > 0.f || W.p_only) {
+    if (warp == 0) {
+      const DF tot = df_warp_sum(lane < C ? sh.g_w[lane] : DF{0.f, 0.f});
+      if (lane == 0) sh.S_w = tot;
+    }
+    __syncthreads();
+    const DF tot = sh.S_w;
+    if (df_pos(tot) || W.p_only) {
       slice_w = tot;
       break;
     }
     W.p_only = true;  // residual all zero: draw from p  [SSD §4.3]
-    __syncthreads();
   }
-  // locate the owner of u * total (ranks in order, then tiles, warps, lanes)
-  const double total = df_to_double(slice_w);
-  const double tgt = (double)uK * total;
-  double pre = 0.0;
-  int owner = -1, last_pos = 0;
-  for (int r = 0; r < C; ++r) {
-    double v = df_to_double(sh.g_w[r]);
-    if (v > 0.0) last_pos = r;
-    if (owner < 0 && pre + v > tgt && v > 0.0) owner = r;
-    if (owner < 0) pre += v;
-  }
-  if (owner < 0) {
-    owner = last_pos;
-    pre = 0.0;
-    for (int r = 0; r < last_pos; ++r) pre += df_to_double(sh.g_w[r]);
-  }
-  if (rank == 0 && tid == 0 && P.diag) {
-    float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
-    dg[SV_DIAG_S_W] = W.p_only ? 1.f : (float)(total / df_to_double(S_t));
-  }
-  if (rank != owner) return;
-  // tile and warp inside the owner (everyone computes the same answer)
-  double rem = tgt - pre;
-  int tsel = -1, wsel = 0, tlast = 0, wlast = 0;
-  for (int t = 0; t < tiles && tsel < 0; ++t)
-    for (int w = 0; w < kWarps; ++w) {
-      double v = df_to_double(sh.tw[t][w]);
-      if (v > 0.0) {
-        tlast = t;
-        wlast = w;
-      }
-      if (v > rem && v > 0.0) {
-        tsel = t;
-        wsel = w;
-        break;
-      }
-      rem -= v;
+  // ---- locate u * total: rank, then chunk (warp 0), then unit, element ----
+  const DF tgt = df_mul_f(slice_w, uK);
+  if (warp == 0) {
+    const DF v = lane < C ? sh.g_w[lane] : DF{0.f, 0.f};
+    const DF inc = df_warp_scan(v, lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < C && df_pos(v) && df_gt(inc, tgt));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < C && df_pos(v));
+    const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const DF v_own = df_shfl(v, owner);
+    // past the end by rounding: the last positive slice, just inside its end
+    DF rem = hit ? df_sub(tgt, df_sub(df_shfl(inc, owner), v_own)) : df_mul_f(v_own, 0.999999f);
+    if (rank == 0 && lane == 0 && P.diag) {
+      float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
+      dg[SV_DIAG_S_W] = W.p_only ? 1.f : df_to_float(df_div(slice_w, S_t));
     }
-  if (tsel < 0) {  // rounding pushed the target past the end: last positive
-    tsel = tlast;
-    wsel = wlast;
-    rem = df_to_double(sh.tw[tlast][wlast]);
-    rem = rem > 0.0 ? rem * 0.999999 : 0.0;
+    if (owner == rank) {
+      DF cv{0.f, 0.f};
+      if (lane < NCj)
+        for (int w = 0; w < kWarps; ++w) cv = df_add(cv, sh.tw[lane][w]);
+      const DF cinc = df_warp_scan(cv, lane);
+      const unsigned ch = __ballot_sync(0xffffffffu, lane < NCj && df_pos(cv) && df_gt(cinc, rem));
+      const unsigned cp = __ballot_sync(0xffffffffu, lane < NCj && df_pos(cv));
+      const int csel = ch ? __ffs(ch) - 1 : (cp ? 31 - __clz(cp) : 0);
+      const DF cv_sel = df_shfl(cv, csel);
+      rem = ch ? df_sub(rem, df_sub(df_shfl(cinc, csel), cv_sel)) : df_mul_f(cv_sel, 0.999999f);
+      if (lane == 0) {
+        sh.csel = csel;
+        sh.rem = rem;
+      }
+    }
+    if (lane == 0) sh.owner = owner;
   }
-  if (warp != wsel) return;
-  // lanes of the selected warp: inclusive scan of their unit sums
-  const int u = tsel * kThreads + wsel * 32 + lane;
-  float us = unit_weight_sum<ES>(pm, buf_t, buf_d, u, W);
-  double inc = (double)us;
+  __syncthreads();
+  if (sh.owner != rank) return;
+  // read back chunk csel and scan its units in index order
+  const int csel = sh.csel;
+  const DF rem = sh.rem;
+  const int s_last = q0 % kStages;
+  const uint32_t par_last = (q0 / kStages) & 1;
+  const char* stage = ring + s_last * kStageBytes;
+  if (tid == 0) {
+    ring_issue<ES>(sh, ring, q0, csel, st, load_d && !W.p_only, sd);
+    if (!mbar_wait_bounded(&sh.full[s_last], par_last)) {
+      atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
+      sh.timeout = 1;
+    } else {
+      sh.timeout = 0;
+    }
+  }
+  __syncthreads();
+  if (sh.timeout) {
+    if (tid == 0) write_outputs(P, b, 0, -1, true);
+    return;
+  }
+  mbar_try_wait(&sh.full[s_last], par_last);
+  const int ubase = csel * kChunkUnits;
+  float v[kUnitsPerThread];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    double n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
+  for (int h = 0; h < kUnitsPerThread; ++h)
+    v[h] = unit_wsum<ES>(st, sd, stage, stage + kHalfBytes, csel, ubase + h * kThreads + tid, W,
+                         same_phase);
+  // block-wide inclusive prefix of the unit sums, units 0..255 in order:
+  // half h holds units h*kThreads + tid
+  DF inc[kUnitsPerThread];
+  DF carry{0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < kUnitsPerThread; ++h) {
+    const DF wi = df_warp_scan(DF{v[h], 0.f}, lane);
+    if (lane == 31) sh.scan[h & 1][warp] = wi;
+    __syncthreads();
+    DF before = carry;
+    for (int w = 0; w < warp; ++w) before = df_add(before, sh.scan[h & 1][w]);
+    DF total = carry;
+    for (int w = 0; w < kWarps; ++w) total = df_add(total, sh.scan[h & 1][w]);
+    inc[h] = df_add(before, wi);
+    carry = total;
   }
-  const double exc = inc - (double)us;
-  unsigned hit = __ballot_sync(0xffffffffu, inc > rem && us > 0.f);
-  unsigned pos = __ballot_sync(0xffffffffu, us > 0.f);
-  int sel = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-  if (lane == sel && u < st.n_units) {
-    constexpr int EPU = 16 / ES;
-    uint4 vt = *reinterpret_cast<const uint4*>(buf_t + 16 * u);
-    const bool vec_d = W.p_only || pm.same_phase;
-    uint4 vd = vec_d ? (W.p_only ? vt : *reinterpret_cast<const uint4*>(buf_d + 16 * u)) : vt;
-    int eb = st.ebase0 + u * EPU;
-    double c = exc;
-    int y = -1, ylast = -1;
-    for (int q = 0; q < EPU; ++q) {
-      int e = eb + q;
-      if (e < st.e0 || e >= st.e1) continue;
-      float zd = vec_d ? unit_elem<ES>(vd, q) : slice_elem<ES>(sd, buf_d, e);
-      float wv = W(unit_elem<ES>(vt, q), zd);
-      if (wv > 0.f) ylast = e;
-      c += (double)wv;
-      if (wv > 0.f && c > rem) {
-        y = e;
-        break;
-      }
+  int cand = 0x7fffffff, lastpos = -1;
+#pragma unroll
+  for (int h = kUnitsPerThread - 1; h >= 0; --h) {
+    const int uo = h * kThreads + tid;  // unit offset in the chunk
+    if (v[h] > 0.f) {
+      lastpos = max(lastpos, uo);
+      if (df_gt(inc[h], rem)) cand = uo;
     }
-    if (y < 0) y = ylast;
-    write_outputs(P, b, j, y, false);
   }
+  cand = warp_min(cand);
+  lastpos = -warp_min(-lastpos);
+  if (lane == 0) sh.r_i[warp] = cand;
+  __syncthreads();
+  int usel = 0x7fffffff;
+  for (int w = 0; w < kWarps; ++w) usel = min(usel, sh.r_i[w]);
+  __syncthreads();
+  if (lane == 0) sh.r_i[warp] = lastpos;
+  __syncthreads();
+  bool past_end = false;
+  if (usel == 0x7fffffff) {  // rounding: the last positive unit
+    past_end = true;
+    usel = -1;
+    for (int w = 0; w < kWarps; ++w) usel = max(usel, sh.r_i[w]);
+    if (usel < 0) usel = 0;
+  }
+  const int hsel = usel / kThreads, tsel = usel % kThreads;
+  if (tid != tsel) return;
+  constexpr int EPU = 16 / ES;
+  const int u = ubase + usel;
+  DF cum = past_end ? DF{0.f, 0.f} : df_sub(inc[hsel], DF{v[hsel], 0.f});
+  int y = -1, ylast = -1;
+  const int eb = st.ebase0 + u * EPU;
+  for (int q = 0; q < EPU; ++q) {
+    const int e = eb + q;
+    if (e < st.e0 || e >= st.e1) continue;
+    const float wv = elem_w<ES>(st, sd, stage, stage + kHalfBytes, csel, u, e, W, same_phase);
+    if (wv > 0.f) ylast = e;
+    cum = df_add(cum, DF{wv, 0.f});
+    if (!past_end && wv > 0.f && df_gt(cum, rem)) {
+      y = e;
+      break;
+    }
+  }
+  if (y < 0) y = ylast;
+  write_outputs(P, b, j, y, false);
 }
 
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, int B) {
-  int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t == 0) *flags = 0u;
   for (int b = t; b < B; b += gridDim.x * blockDim.x) words[b] = 0ull;
 }
@@ -788,21 +1005,17 @@ size_t ws_layout(int B, int K, size_t* words_off, size_t* stats_off) {
 static int g_configured[2] = {0, 0};
 
 template <int ES>
-static cudaError_t configure(size_t max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)max_smem);
-  if (e != cudaSuccess) return e;
+static cudaError_t configure() {
   return cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 template <int ES>
-static cudaError_t launch(const VerifyParams& P0, int C, size_t smem, int items,
-                          cudaStream_t stream) {
+static cudaError_t launch(const VerifyParams& P0, int C, int items, cudaStream_t stream) {
   VerifyParams P = P0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items * (unsigned)C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = kStages * kStageBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -814,10 +1027,10 @@ static cudaError_t launch(const VerifyParams& P0, int C, size_t smem, int items,
   return cudaLaunchKernelEx(&cfg, verify_kernel<ES>, P);
 }
 
-// Cluster width: about 16 KB of each row per CTA, at most 16 CTAs.
-static void choose_geometry(int V, int ES, int* C_out, int* slice_out, int* rowbuf_out) {
+// Cluster width: about 32 KB of each row per CTA, at most 16 CTAs.
+static void choose_geometry(int V, int ES, int* C_out, int* slice_out) {
   const long long row_bytes = (long long)V * ES;
-  int C = (int)((row_bytes + 16383) / 16384);
+  int C = (int)((row_bytes + 32767) / 32768);
   if (C < 1) C = 1;
   if (C > kCmax) C = kCmax;
   int slice = (V + C - 1) / C;
@@ -826,23 +1039,20 @@ static void choose_geometry(int V, int ES, int* C_out, int* slice_out, int* rowb
   if (C < 1) C = 1;
   *C_out = C;
   *slice_out = slice;
-  *rowbuf_out = (int)(((long long)slice * ES + 32 + 127) / 128 * 128);
 }
 
 int verify_launch(const VerifyLaunch& L, std::string* err) {
   const int ES = L.dtype == SV_BF16 ? 2 : 4;
-  int C, slice, rowbuf;
-  choose_geometry(L.V, ES, &C, &slice, &rowbuf);
-  if ((long long)slice * ES > (long long)kMaxTiles * kThreads * 16 - 32) {
+  int C, slice;
+  choose_geometry(L.V, ES, &C, &slice);
+  if ((long long)slice * ES + 32 > (long long)kMaxChunks * kHalfBytes) {
     *err = "vocabulary too large for the cluster slice layout";
     return SV_ERR_SHAPE;
   }
-  const size_t smem = 2 * (size_t)rowbuf;
-  const size_t max_smem = 2 * (size_t)(((long long)kMaxTiles * kThreads * 16 + 32 + 127) / 128 * 128);
   cudaError_t e;
-  int gi = ES == 2 ? 0 : 1;
+  const int gi = ES == 2 ? 0 : 1;
   if (!g_configured[gi]) {
-    e = ES == 2 ? configure<2>(max_smem) : configure<4>(max_smem);
+    e = ES == 2 ? configure<2>() : configure<4>();
     if (e != cudaSuccess) {
       *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return SV_ERR_CUDA;
@@ -875,10 +1085,9 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   P.words = reinterpret_cast<unsigned long long*>(ws + words_off);
   P.stats = reinterpret_cast<ItemStats*>(ws + stats_off);
   P.slice_len = slice;
-  P.rowbuf_bytes = rowbuf;
   cudaStream_t stream = static_cast<cudaStream_t>(L.stream);
 
-  int ib = (L.B + 255) / 256;
+  const int ib = (L.B + 255) / 256;
   verify_init_kernel<<<ib < 1 ? 1 : ib, 256, 0, stream>>>(P.flags, P.words, L.B);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -886,7 +1095,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     return SV_ERR_CUDA;
   }
   const int items = (L.K + 1) * L.B;
-  e = ES == 2 ? launch<2>(P, C, smem, items, stream) : launch<4>(P, C, smem, items, stream);
+  e = ES == 2 ? launch<2>(P, C, items, stream) : launch<4>(P, C, items, stream);
   if (e != cudaSuccess) {
     *err = std::string("verify launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
