@@ -37,15 +37,11 @@
 
 namespace sv {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCmax = 16;
-constexpr int kChunkUnits = 256;                   // 16-byte units of one row per chunk
-constexpr int kHalfBytes = kChunkUnits * 16;       // 4 KB of one row
-constexpr int kStageBytes = 2 * kHalfBytes;        // target half + draft half
-constexpr int kStages = 3;
-constexpr int kMaxChunks = 32;                     // slice <= 128 KB of a row per CTA
-constexpr int kUnitsPerThread = kChunkUnits / kThreads;
+constexpr int kLoadsInFlight = 4;                  // 16-byte loads per row per thread per step
+constexpr int kMaxRounds = 64;                     // slice <= 64 * 256 units = 256 KB of a row
 constexpr int kWordBits = 21;                      // positions per field of the sequence word
 
 struct ItemStats {
@@ -87,7 +83,7 @@ struct RowSlice {
   const char* row;
   int e0, e1;
   uintptr_t base16, a0, a1;
-  int n_units, ebase0, n_chunks;
+  int n_units, ebase0;
 
   __device__ void init(const char* row_, int e0_, int e1_) {
     row = row_;
@@ -101,7 +97,6 @@ struct RowSlice {
     if (a1 < a0) a1 = a0;
     n_units = e1 > e0 ? (int)((g1 - base16 + 15) / 16) : 0;
     ebase0 = e0 - (int)((g0 & 15) / ES);
-    n_chunks = (n_units + kChunkUnits - 1) / kChunkUnits;
   }
   __device__ __forceinline__ bool unit_bulk(int u) const {
     const uintptr_t a = base16 + 16 * (uintptr_t)u;
@@ -110,13 +105,6 @@ struct RowSlice {
     // units [ub0, ub1) are fully inside the aligned body
   __device__ __forceinline__ int ub0() const { return (int)((a0 - base16) / 16); }
   __device__ __forceinline__ int ub1() const { return (int)((a1 - base16) / 16); }
-  // bulk-copied byte range of chunk c
-  __device__ __forceinline__ void chunk_body(int c, uintptr_t* lo, uintptr_t* hi) const {
-    const uintptr_t c0 = base16 + (uintptr_t)c * kHalfBytes, c1 = c0 + kHalfBytes;
-    *lo = c0 > a0 ? c0 : a0;
-    *hi = c1 < a1 ? c1 : a1;
-    if (*hi < *lo) *hi = *lo;
-  }
   __device__ __forceinline__ float elem(int e) const {  // from global memory
     return ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2))
                    : *reinterpret_cast<const float*>(row + (size_t)e * 4);
@@ -200,21 +188,52 @@ __device__ __forceinline__ float pow2i(float k) {
 // Per-thread row accumulator
 // ---------------------------------------------------------------------------
 struct RowAcc {
-  float mx;  // running max of the raw logits (NaN propagates)
-  float R;   // integer reference exponent, kRnone until a finite element
-  DF s;      // sum of 2^(z*c - R)
-  int amax;  // index of the first maximum (greedy rows)
+  float mx;      // running max of the raw logits (NaN propagates)
+  float R;       // integer reference exponent, kRnone until a finite element
+  DF s;          // sum of 2^(z*c - R)
+  int amax;      // index of the first maximum (greedy rows)
+  float pend;    // unit sums not yet added into s (same reference R)
+  uint32_t mx2;  // bf16 sampled rows: running max as a packed bf16x2
 };
 
+constexpr uint32_t kBf16x2NegInf = 0xff80ff80u;
+
 __device__ __forceinline__ RowAcc acc_init() {
-  return RowAcc{-INFINITY, kRnone, DF{0.f, 0.f}, 0x7fffffff};
+  return RowAcc{-INFINITY, kRnone, DF{0.f, 0.f}, 0x7fffffff, 0.f, kBf16x2NegInf};
 }
 
 __device__ __forceinline__ void acc_raise(RowAcc& a, float Rn) {
   const float p = pow2i(a.R - Rn);  // exact power of two (0 from kRnone)
   a.s.hi *= p;
   a.s.lo *= p;
+  a.pend *= p;
   a.R = Rn;
+}
+
+// A unit whose sum exceeds this has an element more than 2^17 above the
+// reference: the reference is raised (rare after the first unit, which
+// always overflows from kRnone) and the unit recomputed.
+constexpr float kRaiseAbove = 1048576.f;
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// move pending unit sums into the compensated total
+__device__ __forceinline__ void acc_flush(RowAcc& a) {
+  df_acc(a.s, a.pend);
+  a.pend = 0.f;
+}
+
+// running max of a sampled row as a float (after the pass)
+template <int ES>
+__device__ __forceinline__ void acc_finish_max(RowAcc& a) {
+  if (ES == 2) {
+    const float lo = bf16_lo(a.mx2), hi = bf16_hi(a.mx2);
+    a.mx = nanmax(a.mx, nanmax(lo, hi));
+  }
 }
 
 __device__ __forceinline__ float e2(float z, const Expo& x, float nR) {
@@ -230,14 +249,11 @@ __device__ __forceinline__ F2 e2x2(F2 z, F2 C, F2 L, F2 N) {
 
 __device__ __forceinline__ F2 bf16x2_to_f2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
 
+// sum over a full unit of 2^(z*c - R) (f32x2 lanes)
 template <int ES>
-__device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
-  const float g = unit_max<ES>(v);
-  a.mx = nanmax(a.mx, g);
-  const float gc = g * x.chi;
-  if (gc > a.R) acc_raise(a, ceilf(gc));
+__device__ __forceinline__ float unit_sumexp(const uint4& v, const Expo& x, float R) {
   const F2 C = f2_pack(x.chi, x.chi), L = f2_pack(x.clo, x.clo);
-  const F2 N = f2_pack(-a.R, -a.R);
+  const F2 N = f2_pack(-R, -R);
   F2 s;
   if (ES == 2) {
     const F2 e0 = e2x2(bf16x2_to_f2(v.x), C, L, N), e1 = e2x2(bf16x2_to_f2(v.y), C, L, N);
@@ -250,14 +266,35 @@ __device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Ex
   }
   float sx, sy;
   f2_unpack(s, sx, sy);
-  df_acc(a.s, sx + sy);
+  return sx + sy;
+}
+
+template <int ES>
+__device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
+  uint32_t um = 0;
+  if (ES == 2) {
+    um = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+    a.mx2 = bf16x2_max_nan(a.mx2, um);
+  } else {
+    a.mx = nanmax(a.mx, unit_max<ES>(v));
+  }
+  float us = unit_sumexp<ES>(v, x, a.R);
+  if (!(us <= kRaiseAbove)) {
+    const float g = ES == 2 ? nanmax(bf16_lo(um), bf16_hi(um)) : unit_max<ES>(v);
+    const float gc = g * x.chi;
+    if (gc > a.R) {
+      acc_raise(a, ceilf(gc));
+      us = unit_sumexp<ES>(v, x, a.R);
+    }
+  }
+  a.pend += us;
 }
 
 __device__ __forceinline__ void sampled_elem(RowAcc& a, float z, const Expo& x) {
   a.mx = nanmax(a.mx, z);
   const float zc = z * x.chi;
   if (zc > a.R) acc_raise(a, ceilf(zc));
-  df_acc(a.s, e2(z, x, -a.R));
+  a.pend += e2(z, x, -a.R);
 }
 
 template <int ES>
@@ -285,13 +322,21 @@ __device__ __forceinline__ void greedy_elem(RowAcc& a, float z, int e) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Loads: 16-byte units straight into registers (read-only path).  Units
+// outside the aligned body [ub0, ub1) are read element by element.
+// ---------------------------------------------------------------------------
 template <int ES>
-__device__ __forceinline__ void row_unit(RowAcc& a, const RowSlice<ES>& rs, const char* half, int c,
-                                         int u, int ub0, int ub1, bool greedy, const Expo& x) {
+__device__ __forceinline__ uint4 ldg_unit(const RowSlice<ES>& rs, int u) {
+  return __ldg(reinterpret_cast<const uint4*>(rs.base16 + 16 * (uintptr_t)u));
+}
+
+template <int ES>
+__device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, int u, int ub0,
+                                           int ub1, const uint4& v, bool greedy, const Expo& x) {
   constexpr int EPU = 16 / ES;
   const int eb = rs.ebase0 + u * EPU;
   if (u >= ub0 && u < ub1) {
-    const uint4 v = *reinterpret_cast<const uint4*>(half + 16 * (u - c * kChunkUnits));
     if (greedy)
       greedy_unit<ES>(a, v, eb);
     else
@@ -347,6 +392,32 @@ __device__ __forceinline__ RowAcc lanes_combine(RowAcc v, bool valid, bool greed
   return RowAcc{m, Rw, s, 0x7fffffff};
 }
 
+// Lane l of warp 0 folds the accumulators of threads l, l + 32, ... into one
+// (exact power-of-two rescaling to the largest reference, compensated sums).
+__device__ __forceinline__ RowAcc acc_merge_lanes(const RowAcc* acc, int lane, bool greedy) {
+  RowAcc a = acc[lane];
+  for (int t = lane + 32; t < kThreads; t += 32) {
+    const RowAcc b = acc[t];
+    if (greedy) {
+      if (b.mx != b.mx) a.mx = b.mx;
+      else if (b.mx > a.mx || (b.mx == a.mx && b.amax < a.amax)) {
+        a.mx = b.mx;
+        a.amax = b.amax;
+      }
+      continue;
+    }
+    a.mx = nanmax(a.mx, b.mx);
+    if (b.R > a.R) {
+      acc_raise(a, b.R);
+      a.s = df_add(a.s, b.s);
+    } else if (b.R > kRnone) {
+      const float p = pow2i(b.R - a.R);
+      a.s = df_add(a.s, DF{b.s.hi * p, b.s.lo * p});
+    }
+  }
+  return a;
+}
+
 __device__ __forceinline__ DF df_shfl(DF v, int src) {
   return DF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
@@ -390,91 +461,88 @@ struct Weight {
   }
 };
 
-// Sum of the weights of unit u (target units), with the draft read from its
-// own half when both rows share the 16-byte phase, else element-wise.
+// Weight sum of one full unit (both rows hold the same elements in it).
 template <int ES>
-__device__ __forceinline__ float unit_wsum(const RowSlice<ES>& st, const RowSlice<ES>& sd,
-                                           const char* ht, const char* hd, int c, int u,
-                                           const Weight& W, bool same_phase) {
-  constexpr int EPU = 16 / ES;
-  if (u >= st.n_units) return 0.f;
-  const int eb = st.ebase0 + u * EPU;
-  if (st.unit_bulk(u) && (W.p_only || same_phase)) {
-    const int off = 16 * (u - c * kChunkUnits);
-    const uint4 vt = *reinterpret_cast<const uint4*>(ht + off);
-    if (W.p_only) {
-      const float nR = -W.Rt;
-      if (ES == 2) {
-        const float e0 = e2(bf16_lo(vt.x), W.x, nR), e1 = e2(bf16_hi(vt.x), W.x, nR);
-        const float f0 = e2(bf16_lo(vt.y), W.x, nR), f1 = e2(bf16_hi(vt.y), W.x, nR);
-        const float g0 = e2(bf16_lo(vt.z), W.x, nR), g1 = e2(bf16_hi(vt.z), W.x, nR);
-        const float h0 = e2(bf16_lo(vt.w), W.x, nR), h1 = e2(bf16_hi(vt.w), W.x, nR);
-        return ((e0 + e1) + (f0 + f1)) + ((g0 + g1) + (h0 + h1));
-      }
-      const float e0 = e2(__uint_as_float(vt.x), W.x, nR), e1 = e2(__uint_as_float(vt.y), W.x, nR);
-      const float f0 = e2(__uint_as_float(vt.z), W.x, nR), f1 = e2(__uint_as_float(vt.w), W.x, nR);
-      return (e0 + e1) + (f0 + f1);
-    }
-    const uint4 vd = *reinterpret_cast<const uint4*>(hd + off);
-    const F2 C = f2_pack(W.x.chi, W.x.chi), L = f2_pack(W.x.clo, W.x.clo);
-    const F2 Nt = f2_pack(-W.Rt, -W.Rt), Nd = f2_pack(-W.Rd, -W.Rd);
-    const F2 RH = f2_pack(-W.rho_hi, -W.rho_hi), RL = f2_pack(-W.rho_lo, -W.rho_lo);
+__device__ __forceinline__ float wsum_full(const uint4& vt, const uint4& vd, const Weight& W) {
+  if (W.p_only) {
+    const float nR = -W.Rt;
     if (ES == 2) {
-      const float e = W.pair2(bf16x2_to_f2(vt.x), bf16x2_to_f2(vd.x), C, L, Nt, Nd, RH, RL);
-      const float f = W.pair2(bf16x2_to_f2(vt.y), bf16x2_to_f2(vd.y), C, L, Nt, Nd, RH, RL);
-      const float g = W.pair2(bf16x2_to_f2(vt.z), bf16x2_to_f2(vd.z), C, L, Nt, Nd, RH, RL);
-      const float h = W.pair2(bf16x2_to_f2(vt.w), bf16x2_to_f2(vd.w), C, L, Nt, Nd, RH, RL);
-      return (e + f) + (g + h);
+      const float e0 = e2(bf16_lo(vt.x), W.x, nR), e1 = e2(bf16_hi(vt.x), W.x, nR);
+      const float f0 = e2(bf16_lo(vt.y), W.x, nR), f1 = e2(bf16_hi(vt.y), W.x, nR);
+      const float g0 = e2(bf16_lo(vt.z), W.x, nR), g1 = e2(bf16_hi(vt.z), W.x, nR);
+      const float h0 = e2(bf16_lo(vt.w), W.x, nR), h1 = e2(bf16_hi(vt.w), W.x, nR);
+      return ((e0 + e1) + (f0 + f1)) + ((g0 + g1) + (h0 + h1));
     }
-    const float e = W.pair2(f2_pack(__uint_as_float(vt.x), __uint_as_float(vt.y)),
-                            f2_pack(__uint_as_float(vd.x), __uint_as_float(vd.y)), C, L, Nt, Nd, RH, RL);
-    const float f = W.pair2(f2_pack(__uint_as_float(vt.z), __uint_as_float(vt.w)),
-                            f2_pack(__uint_as_float(vd.z), __uint_as_float(vd.w)), C, L, Nt, Nd, RH, RL);
-    return e + f;
+    const float e0 = e2(__uint_as_float(vt.x), W.x, nR), e1 = e2(__uint_as_float(vt.y), W.x, nR);
+    const float f0 = e2(__uint_as_float(vt.z), W.x, nR), f1 = e2(__uint_as_float(vt.w), W.x, nR);
+    return (e0 + e1) + (f0 + f1);
   }
-  float acc = 0.f;
-  for (int j = 0; j < EPU; ++j) {
-    const int e = eb + j;
-    if (e < st.e0 || e >= st.e1) continue;
-    acc += W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+  const F2 C = f2_pack(W.x.chi, W.x.chi), L = f2_pack(W.x.clo, W.x.clo);
+  const F2 Nt = f2_pack(-W.Rt, -W.Rt), Nd = f2_pack(-W.Rd, -W.Rd);
+  const F2 RH = f2_pack(-W.rho_hi, -W.rho_hi), RL = f2_pack(-W.rho_lo, -W.rho_lo);
+  if (ES == 2) {
+    const float e = W.pair2(bf16x2_to_f2(vt.x), bf16x2_to_f2(vd.x), C, L, Nt, Nd, RH, RL);
+    const float f = W.pair2(bf16x2_to_f2(vt.y), bf16x2_to_f2(vd.y), C, L, Nt, Nd, RH, RL);
+    const float g = W.pair2(bf16x2_to_f2(vt.z), bf16x2_to_f2(vd.z), C, L, Nt, Nd, RH, RL);
+    const float h = W.pair2(bf16x2_to_f2(vt.w), bf16x2_to_f2(vd.w), C, L, Nt, Nd, RH, RL);
+    return (e + f) + (g + h);
   }
-  return acc;
+  const float e = W.pair2(f2_pack(__uint_as_float(vt.x), __uint_as_float(vt.y)),
+                          f2_pack(__uint_as_float(vd.x), __uint_as_float(vd.y)), C, L, Nt, Nd, RH, RL);
+  const float f = W.pair2(f2_pack(__uint_as_float(vt.z), __uint_as_float(vt.w)),
+                          f2_pack(__uint_as_float(vd.z), __uint_as_float(vd.w)), C, L, Nt, Nd, RH, RL);
+  return e + f;
 }
 
-// weight of element e of unit u (same reads as unit_wsum)
+// Rows of the cut position as the finisher reads them (usually from L2: they
+// were streamed moments earlier).  Full units of both rows are read as 16-byte
+// vectors when the rows share their 16-byte phase, else element by element.
 template <int ES>
-__device__ __forceinline__ float elem_w(const RowSlice<ES>& st, const RowSlice<ES>& sd,
-                                        const char* ht, const char* hd, int c, int u, int e,
-                                        const Weight& W, bool same_phase) {
-  constexpr int EPU = 16 / ES;
-  if (st.unit_bulk(u) && (W.p_only || same_phase)) {
-    const int off = 16 * (u - c * kChunkUnits);
-    const uint4 vt = *reinterpret_cast<const uint4*>(ht + off);
-    const uint4 vd = W.p_only ? vt : *reinterpret_cast<const uint4*>(hd + off);
-    const int j = e - (st.ebase0 + u * EPU);
-    return W(unit_elem<ES>(vt, j), unit_elem<ES>(vd, j));
+struct PairRead {
+  RowSlice<ES> st, sd;
+  int ub0, ub1;
+  bool vec;
+  __device__ __forceinline__ bool full(int u) const { return vec && u >= ub0 && u < ub1; }
+  __device__ __forceinline__ void load(int u, const Weight& W, uint4& vt, uint4& vd) const {
+    if (full(u)) {
+      vt = ldg_unit(st, u);
+      if (!W.p_only) vd = ldg_unit(sd, u);
+    }
   }
-  return W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
-}
+  __device__ __forceinline__ float value(int u, const Weight& W, const uint4& vt,
+                                         const uint4& vd) const {
+    constexpr int EPU = 16 / ES;
+    if (u >= st.n_units) return 0.f;
+    if (full(u)) return wsum_full<ES>(vt, W.p_only ? vt : vd, W);
+    float acc = 0.f;
+    const int eb = st.ebase0 + u * EPU;
+    for (int j = 0; j < EPU; ++j) {
+      const int e = eb + j;
+      if (e < st.e0 || e >= st.e1) continue;
+      acc += W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+    }
+    return acc;
+  }
+  __device__ __forceinline__ float elem_w(int e, const Weight& W) const {
+    return W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+  }
+};
 
 struct Shared {
-  uint64_t full[kStages];
   // all-gather slots, indexed by the writing CTA's rank
   RowAcc g_t[kCmax], g_d[kCmax];
   DF g_w[kCmax];
   // per-warp partials
-  RowAcc r_t[kWarps], r_d[kWarps];
-  DF tw[kMaxChunks][kWarps];
-  DF scan[2][kWarps];
+  RowAcc l_t[kThreads], l_d[kThreads];
+  DF rtot[kMaxRounds];
+  DF scan[kWarps];
   int r_i[kWarps];
-  // item scalars, written by warp 0 and read by the whole CTA
+  // item scalars, written by one thread and read by the whole CTA
   RowAcc row_t, row_d;
-  DF S_w;
+  DF S_w, rem;
   int skip, skip_seen;
   int fin, fin_j, fin_err;
-  int owner, csel;
-  DF rem;
-  int timeout;
+  int owner, rsel;
   int x;
   float u_i, zt_x, zd_x;
 };
@@ -503,62 +571,256 @@ __device__ void write_outputs(const VerifyParams& P, int b, int n, int y, bool e
 }
 
 // ---------------------------------------------------------------------------
-// The ring: chunk c of the current pass is ring entry q = q0 + c, stage
-// q % kStages, mbarrier phase (q / kStages) & 1.  Thread 0 issues the bulk
-// copies and waits; the others sleep at the CTA barrier.
+// Finisher: draw the resample (or bonus) token of sequence b at cut j with
+// the uniform uK.  Every CTA of the cluster takes part.  Pass over the rows:
+// each thread's unit sums go to shared memory in index order (round r holds
+// units r*kThreads .. r*kThreads + kThreads-1); then round totals, the
+// cluster-wide owner of u*total, the round, the unit and the element.
 // ---------------------------------------------------------------------------
 template <int ES>
-__device__ __forceinline__ void ring_issue(Shared& sh, char* ring, uint32_t q, int c,
-                                           const RowSlice<ES>& st, bool with_d,
-                                           const RowSlice<ES>& sd) {
-  const int s = q % kStages;
-  char* stage = ring + s * kStageBytes;
-  uintptr_t tl = 0, th = 0, dl = 0, dh = 0;
-  if (c < st.n_chunks) st.chunk_body(c, &tl, &th);
-  if (with_d && c < sd.n_chunks) sd.chunk_body(c, &dl, &dh);
-  mbar_arrive_expect_tx(&sh.full[s], (uint32_t)((th - tl) + (dh - dl)));
-  if (th > tl)
-    bulk_copy_g2s(stage + (tl - (st.base16 + (uintptr_t)c * kHalfBytes)),
-                  reinterpret_cast<const void*>(tl), (uint32_t)(th - tl), &sh.full[s]);
-  if (dh > dl)
-    bulk_copy_g2s(stage + kHalfBytes + (dl - (sd.base16 + (uintptr_t)c * kHalfBytes)),
-                  reinterpret_cast<const void*>(dl), (uint32_t)(dh - dl), &sh.full[s]);
-}
-
-// Stream chunks 0..NC-1 of (st[, sd]) and call body(c, stage) for each, with
-// every thread.  Returns false if a bounded wait ran out (the caller reports
-// SV_FLAG_TIMEOUT and treats the data as invalid).
-template <int ES, typename Body>
-__device__ __forceinline__ bool ring_pass(Shared& sh, char* ring, uint32_t& q0, int NC,
-                                          const RowSlice<ES>& st, bool with_d,
-                                          const RowSlice<ES>& sd, Body body) {
-  const int tid = threadIdx.x;
-  if (tid == 0)
-    for (int c = 0; c < NC && c < kStages; ++c) ring_issue<ES>(sh, ring, q0 + c, c, st, with_d, sd);
-  bool ok_all = true;
-  for (int c = 0; c < NC; ++c) {
-    const uint32_t q = q0 + c;
-    const int s = q % kStages;
-    const uint32_t par = (q / kStages) & 1;
-    bool ok = true;
-    if (tid == 0) ok = mbar_wait_bounded(&sh.full[s], par);
-    // everyone is done with chunk c-1 and chunk c has landed
-    if (__syncthreads_or(!ok)) {
-      ok_all = false;
+__device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals,
+                                    cg::cluster_group& cluster, int C, int rank, int b, int kb,
+                                    float T, int j, float uK, int e0, int e1, float Rt, float Rd,
+                                    DF S_t, DF S_d) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool bonus = (j == kb);
+  const Expo X = make_expo(T);
+  PairRead<ES> pr;
+  pr.st.init(P.tgt + (long long)b * P.t_seq + (long long)j * P.t_pos, e0, e1);
+  if (!bonus) pr.sd.init(P.drf + (long long)b * P.d_seq + (long long)j * P.d_pos, e0, e1);
+  else pr.sd = pr.st;
+  pr.ub0 = pr.st.ub0();
+  pr.ub1 = pr.st.ub1();
+  const bool same_phase = pr.st.ebase0 == pr.sd.ebase0;
+  Weight W;
+  W.x = X;
+  W.Rt = Rt;
+  W.Rd = Rd;
+  W.p_only = bonus;
+  {
+    const DF rho = bonus ? DF{0.f, 0.f} : df_div(S_t, S_d);
+    W.rho_hi = rho.hi;
+    W.rho_lo = rho.lo;
+  }
+  const int NU = pr.st.n_units;
+  const int rounds = (NU + kThreads - 1) / kThreads;
+  DF slice_w{0.f, 0.f};
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass) cluster.sync();  // every CTA has read the first pass's slots
+    pr.vec = W.p_only || same_phase;
+    for (int u0 = tid; u0 < rounds * kThreads; u0 += kThreads * kLoadsInFlight) {
+      uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
+#pragma unroll
+      for (int k = 0; k < kLoadsInFlight; ++k) {
+        vt[k] = vd[k] = make_uint4(0, 0, 0, 0);
+        pr.load(u0 + k * kThreads, W, vt[k], vd[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kLoadsInFlight; ++k) {
+        const int u = u0 + k * kThreads;
+        if (u < rounds * kThreads) vals[u] = pr.value(u, W, vt[k], vd[k]);
+      }
+    }
+    __syncthreads();
+    for (int r = warp; r < rounds; r += kWarps) {
+      DF a{0.f, 0.f};
+      for (int t = lane; t < kThreads; t += 32) df_acc(a, vals[r * kThreads + t]);
+      a = df_warp_sum(a);
+      if (lane == 0) sh.rtot[r] = a;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      DF a{0.f, 0.f};
+      for (int r = lane; r < rounds; r += 32) a = df_add(a, sh.rtot[r]);
+      a = df_warp_sum(a);
+      if (lane < C) *cluster.map_shared_rank(&sh.g_w[rank], lane) = a;
+    }
+    cluster.sync();
+    if (warp == 0) {
+      const DF tot = df_warp_sum(lane < C ? sh.g_w[lane] : DF{0.f, 0.f});
+      if (lane == 0) sh.S_w = tot;
+    }
+    __syncthreads();
+    const DF tot = sh.S_w;
+    if (df_pos(tot) || W.p_only) {
+      slice_w = tot;
       break;
     }
-    if (tid == 0 && c >= 1 && c - 1 + kStages < NC)
-      ring_issue<ES>(sh, ring, q + kStages - 1, c - 1 + kStages, st, with_d, sd);
-    mbar_try_wait(&sh.full[s], par);  // this thread's acquire of the landed data
-    body(c, ring + s * kStageBytes);
+    W.p_only = true;  // residual all zero: draw from p  [SSD §4.3]
+  }
+  // ---- locate u * total: rank (warp 0), round (one thread), unit, element ----
+  const DF tgt = df_mul_f(slice_w, uK);
+  if (warp == 0) {
+    const DF v = lane < C ? sh.g_w[lane] : DF{0.f, 0.f};
+    const DF inc = df_warp_scan(v, lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < C && df_pos(v) && df_gt(inc, tgt));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < C && df_pos(v));
+    const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const DF v_own = df_shfl(v, owner);
+    // past the end by rounding: the last positive slice, just inside its end
+    DF rem = hit ? df_sub(tgt, df_sub(df_shfl(inc, owner), v_own)) : df_mul_f(v_own, 0.999999f);
+    if (rank == 0 && lane == 0 && P.diag) {
+      float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
+      dg[SV_DIAG_S_W] = W.p_only ? 1.f : df_to_float(df_div(slice_w, S_t));
+    }
+    if (lane == 0) {
+      sh.owner = owner;
+      if (owner == rank) {
+        int rsel = -1, rlast = 0;
+        for (int r = 0; r < rounds; ++r) {
+          const DF rv = sh.rtot[r];
+          if (!df_pos(rv)) continue;
+          rlast = r;
+          if (df_gt(rv, rem)) {
+            rsel = r;
+            break;
+          }
+          rem = df_sub(rem, rv);
+        }
+        if (rsel < 0) {
+          rsel = rlast;
+          rem = df_mul_f(sh.rtot[rlast], 0.999999f);
+        }
+        sh.rsel = rsel;
+        sh.rem = rem;
+      }
+    }
   }
   __syncthreads();
-  q0 += NC;
-  return ok_all;
+  if (sh.owner != rank) return;  // (uniform inside this CTA)
+  const int rsel = sh.rsel;
+  const DF rem = sh.rem;
+  // block-wide inclusive prefix of round rsel's unit sums (thread order)
+  const float v = vals[rsel * kThreads + tid];
+  const DF wi = df_warp_scan(DF{v, 0.f}, lane);
+  if (lane == 31) sh.scan[warp] = wi;
+  __syncthreads();
+  DF inc = wi;
+  for (int w = 0; w < warp; ++w) inc = df_add(sh.scan[w], inc);
+  int cand = (v > 0.f && df_gt(inc, rem)) ? tid : 0x7fffffff;
+  int lastpos = v > 0.f ? tid : -1;
+  cand = warp_min(cand);
+  lastpos = -warp_min(-lastpos);
+  __syncthreads();
+  if (lane == 0) {
+    sh.r_i[warp] = cand;
+    sh.scan[warp].hi = __int_as_float(lastpos);
+  }
+  __syncthreads();
+  int tsel = 0x7fffffff, tlast = -1;
+  for (int w = 0; w < kWarps; ++w) {
+    tsel = min(tsel, sh.r_i[w]);
+    tlast = max(tlast, __float_as_int(sh.scan[w].hi));
+  }
+  const bool past_end = tsel == 0x7fffffff;  // rounding: the last positive unit
+  if (past_end) tsel = tlast < 0 ? 0 : tlast;
+  if (tid != tsel) return;
+  constexpr int EPU = 16 / ES;
+  const int u = rsel * kThreads + tid;
+  DF cum = past_end ? DF{0.f, 0.f} : df_sub(inc, DF{v, 0.f});
+  int y = -1, ylast = -1;
+  const int eb = pr.st.ebase0 + u * EPU;
+  for (int q = 0; q < EPU; ++q) {
+    const int e = eb + q;
+    if (e < pr.st.e0 || e >= pr.st.e1) continue;
+    const float wv = pr.elem_w(e, W);
+    if (wv > 0.f) ylast = e;
+    cum = df_add(cum, DF{wv, 0.f});
+    if (!past_end && wv > 0.f && df_gt(cum, rem)) {
+      y = e;
+      break;
+    }
+  }
+  if (y < 0) y = ylast;
+  write_outputs(P, b, j, y, false);
+}
+
+// Decision of one item and its publication in the sequence word (rank 0,
+// thread 0).  Returns 1 if this item completes the sequence's prefix, with
+// the cut position and whether it is an error in *j_out / *err_out.
+template <int ES>
+__device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int b, int kb,
+                                   bool greedy, bool has_draft, const Expo& X, const RowAcc& row_t,
+                                   const RowAcc& row_d, bool bad_t, bool bad_d, int* j_out,
+                                   int* err_out) {
+  const int x = sh.x;
+  const float u_i = sh.u_i, zt_x = sh.zt_x, zd_x = sh.zd_x;
+  uint32_t errbits = 0;
+  if (bad_t || bad_d) errbits |= SV_FLAG_NONFINITE;
+  if (i < kb && (x < 0 || x >= P.V)) errbits |= SV_FLAG_BAD_TOKEN;
+  bool reject = false;
+  float diag_px = NAN, diag_qx = NAN, diag_r = NAN;
+  if (greedy) {
+    if (i < kb && !errbits) reject = (x != row_t.amax);
+  } else if (has_draft) {
+    if (!(u_i >= 0.f && u_i < 1.f)) errbits |= SV_FLAG_BAD_UNIFORM;
+    if (!errbits) {
+      // p(x)/q(x) = 2^((z_t - z_d)*c + R_d - R_t) * S_d / S_t, formed in the
+      // exponent domain so that neither factor underflows on its own;
+      // zero where the exact probability underflows double precision.
+      const float lt = (zt_x - row_t.mx) * X.chi, ld = (zd_x - row_d.mx) * X.chi;
+      float r;
+      if (!(ld > -1074.f) || !(lt > -1074.f)) {
+        r = 0.f;
+      } else {
+        const float a = zt_x - zd_x;
+        const float ex = __fmaf_rn(a, X.chi, a * X.clo) + (row_d.R - row_t.R);
+        r = ex2(ex) * df_to_float(df_div(row_d.s, row_t.s));
+      }
+      diag_px = ex2(earg(zt_x, X, row_t.R)) / row_t.s.hi;
+      diag_qx = ex2(earg(zd_x, X, row_d.R)) / row_d.s.hi;
+      diag_r = r;
+      reject = !(u_i < r);
+    }
+  }
+  ItemStats s;
+  s.m_t = row_t.mx;
+  s.R_t = row_t.R;
+  s.st_hi = row_t.s.hi;
+  s.st_lo = row_t.s.lo;
+  s.m_d = row_d.mx;
+  s.R_d = row_d.R;
+  s.sd_hi = row_d.s.hi;
+  s.sd_lo = row_d.s.lo;
+  s.argmax = row_t.amax;
+  s.errbits = errbits;
+  P.stats[(size_t)b * (P.K + 1) + i] = s;
+  if (P.diag) {
+    float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
+    dg[SV_DIAG_M_T] = row_t.mx;
+    if (greedy) {
+      dg[SV_DIAG_ARGMAX] = (float)row_t.amax;
+    } else if (!bad_t) {
+      // normaliser relative to the row max: S_R * 2^(R - m*c)
+      dg[SV_DIAG_S_T] = df_to_float(row_t.s) * ex2(-earg(row_t.mx, X, row_t.R));
+      dg[SV_DIAG_MASS_T] = 1.f;
+      if (has_draft && !bad_d) {
+        dg[SV_DIAG_M_D] = row_d.mx;
+        dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
+        dg[SV_DIAG_MASS_D] = 1.f;
+        dg[SV_DIAG_P_X] = diag_px;
+        dg[SV_DIAG_Q_X] = diag_qx;
+        dg[SV_DIAG_RATIO] = diag_r;
+      }
+    }
+  }
+  __threadfence();
+  unsigned long long bits = 1ull << i;
+  if (errbits) bits |= 1ull << (2 * kWordBits + i);
+  else if (reject) bits |= 1ull << (kWordBits + i);
+  const unsigned long long old = atomicOr(P.words + b, bits);
+  __threadfence();
+  int j0, j1;
+  bool e0_, e1_;
+  const bool was = resolvable(old, kb, &j0, &e0_);
+  const bool now = resolvable(old | bits, kb, &j1, &e1_);
+  *j_out = j1;
+  *err_out = e1_ ? 1 : 0;
+  return (!was && now) ? 1 : 0;
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -566,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
   const int item = blockIdx.x / C;
   const int i = item / P.B, b = item % P.B;
 
-  extern __shared__ __align__(128) char ring[];
+  extern __shared__ __align__(16) float vals[];  // finisher's unit sums
   __shared__ Shared sh;
 
   // ---- per-row parameters (identical in every CTA of the cluster) ----
@@ -590,27 +852,39 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
   const bool has_draft = !greedy && i < kb;
   const Expo X = greedy ? Expo{1.f, 1e-30f} : make_expo(T);
 
-  // ---- set-up; rank 0 reads the sequence word ----
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&sh.full[s], 1);
-    fence_mbar_init();
-    if (rank == 0) {
+  // ---- rank 0 decides whether an earlier rejection makes this item moot ----
+  if (C > 1) {
+    if (rank == 0 && tid == 0) {
       const unsigned long long w = __ldcg(P.words + b);
       const unsigned long long R =
           ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
       sh.skip = (R & ((1ull << i) - 1)) != 0;
     }
+    cluster.sync();  // every CTA runs (distributed shared memory is safe)
+    if (tid == 0) sh.skip_seen = *cluster.map_shared_rank(&sh.skip, 0);
+    __syncthreads();
+    if (sh.skip_seen) {
+      cluster.sync();  // rank 0 stays until every CTA has read its flag
+      return;
+    }
+  } else {
+    if (tid == 0) {
+      const unsigned long long w = __ldcg(P.words + b);
+      const unsigned long long R =
+          ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
+      sh.skip_seen = (R & ((1ull << i) - 1)) != 0;
+    }
+    __syncthreads();
+    if (sh.skip_seen) return;
   }
-  // every CTA is running (distributed shared memory is safe) and rank 0's
-  // skip flag is visible to all of them
-  cluster.sync();
-  if (tid == 0) sh.skip_seen = *cluster.map_shared_rank(&sh.skip, 0);
-  __syncthreads();
-  if (sh.skip_seen) {
-    cluster.sync();  // rank 0 stays until every CTA has read its flag
-    return;
-  }
-  // decision inputs, fetched by one thread of warp 1 while the rows stream
+
+  // ---- stream the slices: one pass per row, loads straight to registers ----
+  const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
+  RowSlice<ES> st, sd;
+  st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
+  if (has_draft) sd.init(P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos, e0, e1);
+  else sd = st;
+  // rank 0, warp 1: the decision's inputs, fetched while the rows stream
   if (rank == 0 && tid == 32) {
     int x = -1;
     float u = 0.f, zt = 0.f, zd = 0.f;
@@ -618,14 +892,8 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
       x = P.tokens[(size_t)b * P.K + i];
       if (!greedy) u = P.unif[(size_t)b * (P.K + 1) + i];
       if (x >= 0 && x < P.V) {
-        const char* rt = P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos;
-        zt = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rt + (size_t)x * 2))
-                     : *reinterpret_cast<const float*>(rt + (size_t)x * 4);
-        if (has_draft) {
-          const char* rd = P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos;
-          zd = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(rd + (size_t)x * 2))
-                       : *reinterpret_cast<const float*>(rd + (size_t)x * 4);
-        }
+        zt = st.elem(x);
+        if (has_draft) zd = sd.elem(x);
       }
     }
     sh.x = x;
@@ -633,53 +901,59 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
     sh.zt_x = zt;
     sh.zd_x = zd;
   }
-
-  // ---- stream the slices: one pass per row ----
-  const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
-  RowSlice<ES> st, sd;
-  st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
-  if (has_draft) sd.init(P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos, e0, e1);
-  else sd = st;
-  uint32_t q0 = 0;
   RowAcc at = acc_init(), ad = acc_init();
-  const int NC = has_draft ? max(st.n_chunks, sd.n_chunks) : st.n_chunks;
-  const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-  const bool ok = ring_pass<ES>(sh, ring, q0, NC, st, has_draft, sd, [&](int c, const char* stage) {
-#pragma unroll
-    for (int h = 0; h < kUnitsPerThread; ++h) {
-      const int u = c * kChunkUnits + h * kThreads + tid;
-      row_unit<ES>(at, st, stage, c, u, tb0, tb1, greedy, X);
-      if (has_draft) row_unit<ES>(ad, sd, stage + kHalfBytes, c, u, db0, db1, false, X);
-    }
-  });
-  if (!ok && tid == 0) atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
-
-  // ---- combine: warps -> CTA -> cluster (warp 0 of every CTA) ----
   {
-    const RowAcc wt = lanes_combine(at, true, greedy);
-    const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
-    if (lane == 0) {
-      sh.r_t[warp] = wt;
-      sh.r_d[warp] = wd;
+    const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
+    const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
+    for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight) {
+      uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
+#pragma unroll
+      for (int k = 0; k < kLoadsInFlight; ++k) {
+        const int u = u0 + k * kThreads;
+        vt[k] = (u >= tb0 && u < tb1) ? ldg_unit(st, u) : make_uint4(0, 0, 0, 0);
+        vd[k] = (has_draft && u >= db0 && u < db1) ? ldg_unit(sd, u) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kLoadsInFlight; ++k) {
+        const int u = u0 + k * kThreads;
+        row_unit_v<ES>(at, st, u, tb0, tb1, vt[k], greedy, X);
+        if (has_draft) row_unit_v<ES>(ad, sd, u, db0, db1, vd[k], false, X);
+      }
+      if (!greedy) acc_flush(at);
+      if (has_draft) acc_flush(ad);
     }
   }
+  if (!greedy) acc_finish_max<ES>(at);
+  if (has_draft) acc_finish_max<ES>(ad);
+
+  // ---- combine: threads -> CTA (warp 0, through shared memory) -> cluster ----
+  sh.l_t[tid] = at;
+  if (has_draft) sh.l_d[tid] = ad;
   __syncthreads();
   if (warp == 0) {
-    RowAcc ct = lanes_combine(lane < kWarps ? sh.r_t[lane] : acc_init(), lane < kWarps, greedy);
-    const RowAcc cd = lanes_combine(lane < kWarps ? sh.r_d[lane] : acc_init(), lane < kWarps, false);
-    if (!ok) ct.mx = __int_as_float(0x7fc00000);  // a timed-out slice poisons the row
-    if (lane < C) {
-      *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
-      *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
+    RowAcc ct = acc_merge_lanes(sh.l_t, lane, greedy);
+    RowAcc cd = has_draft ? acc_merge_lanes(sh.l_d, lane, false) : acc_init();
+    ct = lanes_combine(ct, true, greedy);
+    cd = lanes_combine(cd, true, false);
+    if (C > 1) {
+      if (lane < C) {
+        *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
+        *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
+      }
+    } else if (lane == 0) {
+      sh.row_t = ct;
+      sh.row_d = cd;
     }
   }
-  cluster.sync();
-  if (warp == 0) {
-    const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy);
-    const RowAcc rd = lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false);
-    if (lane == 0) {
-      sh.row_t = rt;
-      sh.row_d = rd;
+  if (C > 1) {
+    cluster.sync();
+    if (warp == 0) {
+      const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy);
+      const RowAcc rd = lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false);
+      if (lane == 0) {
+        sh.row_t = rt;
+        sh.row_d = rd;
+      }
     }
   }
   __syncthreads();
@@ -692,86 +966,24 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
 
   // ---- decision and publication (rank 0, one thread) ----
   if (rank == 0 && tid == 0) {
-    const int x = sh.x;
-    const float u_i = sh.u_i, zt_x = sh.zt_x, zd_x = sh.zd_x;
-    uint32_t errbits = 0;
-    if (bad_t || bad_d) errbits |= SV_FLAG_NONFINITE;
-    if (i < kb && (x < 0 || x >= P.V)) errbits |= SV_FLAG_BAD_TOKEN;
-    bool reject = false;
-    float diag_px = NAN, diag_qx = NAN, diag_r = NAN;
-    if (greedy) {
-      if (i < kb && !errbits) reject = (x != row_t.amax);
-    } else if (has_draft) {
-      if (!(u_i >= 0.f && u_i < 1.f)) errbits |= SV_FLAG_BAD_UNIFORM;
-      if (!errbits) {
-        // p(x)/q(x) = 2^((z_t - z_d)*c + R_d - R_t) * S_d / S_t, formed in the
-        // exponent domain so that neither factor underflows on its own;
-        // zero where the exact probability underflows double precision.
-        const float lt = (zt_x - row_t.mx) * X.chi, ld = (zd_x - row_d.mx) * X.chi;
-        float r;
-        if (!(ld > -1074.f) || !(lt > -1074.f)) {
-          r = 0.f;
-        } else {
-          const float a = zt_x - zd_x;
-          const float ex = __fmaf_rn(a, X.chi, a * X.clo) + (row_d.R - row_t.R);
-          r = ex2(ex) * df_to_float(df_div(row_d.s, row_t.s));
-        }
-        diag_px = ex2(earg(zt_x, X, row_t.R)) / row_t.s.hi;
-        diag_qx = ex2(earg(zd_x, X, row_d.R)) / row_d.s.hi;
-        diag_r = r;
-        reject = !(u_i < r);
+    int j1, e1_;
+    const int fin = decide<ES>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
+                               &j1, &e1_);
+    if (C > 1) {
+      for (int r = 0; r < C; ++r) {
+        Shared* rs = cluster.map_shared_rank(&sh, r);
+        rs->fin = fin;
+        rs->fin_j = j1;
+        rs->fin_err = e1_;
       }
-    }
-    ItemStats s;
-    s.m_t = row_t.mx;
-    s.R_t = row_t.R;
-    s.st_hi = row_t.s.hi;
-    s.st_lo = row_t.s.lo;
-    s.m_d = row_d.mx;
-    s.R_d = row_d.R;
-    s.sd_hi = row_d.s.hi;
-    s.sd_lo = row_d.s.lo;
-    s.argmax = row_t.amax;
-    s.errbits = errbits;
-    P.stats[(size_t)b * (P.K + 1) + i] = s;
-    if (P.diag) {
-      float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
-      dg[SV_DIAG_M_T] = row_t.mx;
-      if (greedy) {
-        dg[SV_DIAG_ARGMAX] = (float)row_t.amax;
-      } else if (!bad_t) {
-        // normaliser relative to the row max: S_R * 2^(R - m*c)
-        dg[SV_DIAG_S_T] = df_to_float(row_t.s) * ex2(-earg(row_t.mx, X, row_t.R));
-        dg[SV_DIAG_MASS_T] = 1.f;
-        if (has_draft && !bad_d) {
-          dg[SV_DIAG_M_D] = row_d.mx;
-          dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
-          dg[SV_DIAG_MASS_D] = 1.f;
-          dg[SV_DIAG_P_X] = diag_px;
-          dg[SV_DIAG_Q_X] = diag_qx;
-          dg[SV_DIAG_RATIO] = diag_r;
-        }
-      }
-    }
-    __threadfence();
-    unsigned long long bits = 1ull << i;
-    if (errbits) bits |= 1ull << (2 * kWordBits + i);
-    else if (reject) bits |= 1ull << (kWordBits + i);
-    const unsigned long long old = atomicOr(P.words + b, bits);
-    __threadfence();
-    int j0, j1;
-    bool e0_, e1_;
-    const bool was = resolvable(old, kb, &j0, &e0_);
-    const bool now = resolvable(old | bits, kb, &j1, &e1_);
-    const int fin = (!was && now) ? 1 : 0;
-    for (int r = 0; r < C; ++r) {
-      Shared* rs = cluster.map_shared_rank(&sh, r);
-      rs->fin = fin;
-      rs->fin_j = j1;
-      rs->fin_err = e1_ ? 1 : 0;
+    } else {
+      sh.fin = fin;
+      sh.fin_j = j1;
+      sh.fin_err = e1_;
     }
   }
-  cluster.sync();
+  if (C > 1) cluster.sync();
+  else __syncthreads();
   if (!sh.fin) return;
 
   // ======================= finisher =======================
@@ -799,7 +1011,6 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
     }
     return;
   }
-  const bool bonus = (j == kb);
   float Rt = row_t.R, Rd = row_d.R;
   DF S_t = row_t.s, S_d = row_d.s;
   if (j != i) {
@@ -809,178 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 8) verify_kernel(const VerifyParams 
     S_t = DF{__ldcg(&sj->st_hi), __ldcg(&sj->st_lo)};
     S_d = DF{__ldcg(&sj->sd_hi), __ldcg(&sj->sd_lo)};
   }
-  st.init(P.tgt + (long long)b * P.t_seq + (long long)j * P.t_pos, e0, e1);
-  if (!bonus) sd.init(P.drf + (long long)b * P.d_seq + (long long)j * P.d_pos, e0, e1);
-  else sd = st;
-  const bool same_phase = st.ebase0 == sd.ebase0;
-  const bool load_d = !bonus && same_phase;  // else the draft is read element-wise
-  Weight W;
-  W.x = X;
-  W.Rt = Rt;
-  W.Rd = Rd;
-  W.p_only = bonus;
-  {
-    const DF rho = bonus ? DF{0.f, 0.f} : df_div(S_t, S_d);
-    W.rho_hi = rho.hi;
-    W.rho_lo = rho.lo;
-  }
-  const int NCj = st.n_chunks;
-  DF slice_w{0.f, 0.f};
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass) cluster.sync();  // every CTA has read the first pass's slots
-    const bool okp = ring_pass<ES>(sh, ring, q0, NCj, st, load_d && !W.p_only, sd,
-                                   [&](int c, const char* stage) {
-      float v = 0.f;
-#pragma unroll
-      for (int h = 0; h < kUnitsPerThread; ++h)
-        v += unit_wsum<ES>(st, sd, stage, stage + kHalfBytes, c, c * kChunkUnits + h * kThreads + tid,
-                           W, same_phase);
-      const DF wsum = df_warp_sum(DF{v, 0.f});
-      if (lane == 0) sh.tw[c][warp] = wsum;
-    });
-    if (!okp && tid == 0) atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
-    if (warp == 0) {
-      DF a{0.f, 0.f};
-      if (lane < NCj)
-        for (int w = 0; w < kWarps; ++w) a = df_add(a, sh.tw[lane][w]);
-      a = df_warp_sum(a);
-      if (lane < C) *cluster.map_shared_rank(&sh.g_w[rank], lane) = a;
-    }
-    cluster.sync();
-    if (warp == 0) {
-      const DF tot = df_warp_sum(lane < C ? sh.g_w[lane] : DF{0.f, 0.f});
-      if (lane == 0) sh.S_w = tot;
-    }
-    __syncthreads();
-    const DF tot = sh.S_w;
-    if (df_pos(tot) || W.p_only) {
-      slice_w = tot;
-      break;
-    }
-    W.p_only = true;  // residual all zero: draw from p  [SSD §4.3]
-  }
-  // ---- locate u * total: rank, then chunk (warp 0), then unit, element ----
-  const DF tgt = df_mul_f(slice_w, uK);
-  if (warp == 0) {
-    const DF v = lane < C ? sh.g_w[lane] : DF{0.f, 0.f};
-    const DF inc = df_warp_scan(v, lane);
-    const unsigned hit = __ballot_sync(0xffffffffu, lane < C && df_pos(v) && df_gt(inc, tgt));
-    const unsigned pos = __ballot_sync(0xffffffffu, lane < C && df_pos(v));
-    const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-    const DF v_own = df_shfl(v, owner);
-    // past the end by rounding: the last positive slice, just inside its end
-    DF rem = hit ? df_sub(tgt, df_sub(df_shfl(inc, owner), v_own)) : df_mul_f(v_own, 0.999999f);
-    if (rank == 0 && lane == 0 && P.diag) {
-      float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
-      dg[SV_DIAG_S_W] = W.p_only ? 1.f : df_to_float(df_div(slice_w, S_t));
-    }
-    if (owner == rank) {
-      DF cv{0.f, 0.f};
-      if (lane < NCj)
-        for (int w = 0; w < kWarps; ++w) cv = df_add(cv, sh.tw[lane][w]);
-      const DF cinc = df_warp_scan(cv, lane);
-      const unsigned ch = __ballot_sync(0xffffffffu, lane < NCj && df_pos(cv) && df_gt(cinc, rem));
-      const unsigned cp = __ballot_sync(0xffffffffu, lane < NCj && df_pos(cv));
-      const int csel = ch ? __ffs(ch) - 1 : (cp ? 31 - __clz(cp) : 0);
-      const DF cv_sel = df_shfl(cv, csel);
-      rem = ch ? df_sub(rem, df_sub(df_shfl(cinc, csel), cv_sel)) : df_mul_f(cv_sel, 0.999999f);
-      if (lane == 0) {
-        sh.csel = csel;
-        sh.rem = rem;
-      }
-    }
-    if (lane == 0) sh.owner = owner;
-  }
-  __syncthreads();
-  if (sh.owner != rank) return;
-  // read back chunk csel and scan its units in index order
-  const int csel = sh.csel;
-  const DF rem = sh.rem;
-  const int s_last = q0 % kStages;
-  const uint32_t par_last = (q0 / kStages) & 1;
-  const char* stage = ring + s_last * kStageBytes;
-  if (tid == 0) {
-    ring_issue<ES>(sh, ring, q0, csel, st, load_d && !W.p_only, sd);
-    if (!mbar_wait_bounded(&sh.full[s_last], par_last)) {
-      atomicOr(P.flags, (uint32_t)SV_FLAG_TIMEOUT);
-      sh.timeout = 1;
-    } else {
-      sh.timeout = 0;
-    }
-  }
-  __syncthreads();
-  if (sh.timeout) {
-    if (tid == 0) write_outputs(P, b, 0, -1, true);
-    return;
-  }
-  mbar_try_wait(&sh.full[s_last], par_last);
-  const int ubase = csel * kChunkUnits;
-  float v[kUnitsPerThread];
-#pragma unroll
-  for (int h = 0; h < kUnitsPerThread; ++h)
-    v[h] = unit_wsum<ES>(st, sd, stage, stage + kHalfBytes, csel, ubase + h * kThreads + tid, W,
-                         same_phase);
-  // block-wide inclusive prefix of the unit sums, units 0..255 in order:
-  // half h holds units h*kThreads + tid
-  DF inc[kUnitsPerThread];
-  DF carry{0.f, 0.f};
-#pragma unroll
-  for (int h = 0; h < kUnitsPerThread; ++h) {
-    const DF wi = df_warp_scan(DF{v[h], 0.f}, lane);
-    if (lane == 31) sh.scan[h & 1][warp] = wi;
-    __syncthreads();
-    DF before = carry;
-    for (int w = 0; w < warp; ++w) before = df_add(before, sh.scan[h & 1][w]);
-    DF total = carry;
-    for (int w = 0; w < kWarps; ++w) total = df_add(total, sh.scan[h & 1][w]);
-    inc[h] = df_add(before, wi);
-    carry = total;
-  }
-  int cand = 0x7fffffff, lastpos = -1;
-#pragma unroll
-  for (int h = kUnitsPerThread - 1; h >= 0; --h) {
-    const int uo = h * kThreads + tid;  // unit offset in the chunk
-    if (v[h] > 0.f) {
-      lastpos = max(lastpos, uo);
-      if (df_gt(inc[h], rem)) cand = uo;
-    }
-  }
-  cand = warp_min(cand);
-  lastpos = -warp_min(-lastpos);
-  if (lane == 0) sh.r_i[warp] = cand;
-  __syncthreads();
-  int usel = 0x7fffffff;
-  for (int w = 0; w < kWarps; ++w) usel = min(usel, sh.r_i[w]);
-  __syncthreads();
-  if (lane == 0) sh.r_i[warp] = lastpos;
-  __syncthreads();
-  bool past_end = false;
-  if (usel == 0x7fffffff) {  // rounding: the last positive unit
-    past_end = true;
-    usel = -1;
-    for (int w = 0; w < kWarps; ++w) usel = max(usel, sh.r_i[w]);
-    if (usel < 0) usel = 0;
-  }
-  const int hsel = usel / kThreads, tsel = usel % kThreads;
-  if (tid != tsel) return;
-  constexpr int EPU = 16 / ES;
-  const int u = ubase + usel;
-  DF cum = past_end ? DF{0.f, 0.f} : df_sub(inc[hsel], DF{v[hsel], 0.f});
-  int y = -1, ylast = -1;
-  const int eb = st.ebase0 + u * EPU;
-  for (int q = 0; q < EPU; ++q) {
-    const int e = eb + q;
-    if (e < st.e0 || e >= st.e1) continue;
-    const float wv = elem_w<ES>(st, sd, stage, stage + kHalfBytes, csel, u, e, W, same_phase);
-    if (wv > 0.f) ylast = e;
-    cum = df_add(cum, DF{wv, 0.f});
-    if (!past_end && wv > 0.f && df_gt(cum, rem)) {
-      y = e;
-      break;
-    }
-  }
-  if (y < 0) y = ylast;
-  write_outputs(P, b, j, y, false);
+  finish<ES>(P, sh, vals, cluster, C, rank, b, kb, T, j, uK, e0, e1, Rt, Rd, S_t, S_d);
 }
 
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, int B) {
@@ -1006,16 +1046,19 @@ static int g_configured[2] = {0, 0};
 
 template <int ES>
 static cudaError_t configure() {
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxRounds * kThreads * (int)sizeof(float));
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 template <int ES>
-static cudaError_t launch(const VerifyParams& P0, int C, int items, cudaStream_t stream) {
+static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem, cudaStream_t stream) {
   VerifyParams P = P0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)items * (unsigned)C, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kStages * kStageBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1027,10 +1070,26 @@ static cudaError_t launch(const VerifyParams& P0, int C, int items, cudaStream_t
   return cudaLaunchKernelEx(&cfg, verify_kernel<ES>, P);
 }
 
-// Cluster width: about 32 KB of each row per CTA, at most 16 CTAs.
-static void choose_geometry(int V, int ES, int* C_out, int* slice_out) {
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  }
+  return n;
+}
+
+// Cluster width: enough CTAs per position level (B items each) to give every
+// SM about three, as wide as small batches need for latency, and at least wide
+// enough that a slice fits kMaxRounds rounds; at most 16 CTAs.
+static void choose_geometry(int V, int ES, int B, int* C_out, int* slice_out) {
   const long long row_bytes = (long long)V * ES;
-  int C = (int)((row_bytes + 32767) / 32768);
+  const long long max_slice = (long long)kMaxRounds * kThreads * 16 - 64;
+  int C = (3 * sm_count() + B - 1) / (B > 0 ? B : 1);
+  const int cmin = (int)((row_bytes + max_slice - 1) / max_slice);
+  if (C < cmin) C = cmin;
   if (C < 1) C = 1;
   if (C > kCmax) C = kCmax;
   int slice = (V + C - 1) / C;
@@ -1044,11 +1103,14 @@ static void choose_geometry(int V, int ES, int* C_out, int* slice_out) {
 int verify_launch(const VerifyLaunch& L, std::string* err) {
   const int ES = L.dtype == SV_BF16 ? 2 : 4;
   int C, slice;
-  choose_geometry(L.V, ES, &C, &slice);
-  if ((long long)slice * ES + 32 > (long long)kMaxChunks * kHalfBytes) {
+  choose_geometry(L.V, ES, L.B, &C, &slice);
+  const long long units = ((long long)slice * ES + 30) / 16 + 1;
+  const long long rounds = (units + kThreads - 1) / kThreads;
+  if (rounds > kMaxRounds) {
     *err = "vocabulary too large for the cluster slice layout";
     return SV_ERR_SHAPE;
   }
+  const size_t smem = (size_t)rounds * kThreads * sizeof(float);
   cudaError_t e;
   const int gi = ES == 2 ? 0 : 1;
   if (!g_configured[gi]) {
@@ -1095,7 +1157,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     return SV_ERR_CUDA;
   }
   const int items = (L.K + 1) * L.B;
-  e = ES == 2 ? launch<2>(P, C, items, stream) : launch<4>(P, C, items, stream);
+  e = ES == 2 ? launch<2>(P, C, items, smem, stream) : launch<4>(P, C, items, smem, stream);
   if (e != cudaSuccess) {
     *err = std::string("verify launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
