@@ -149,6 +149,39 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
                          size_t workspace_bytes, void* stream);
 
 /*
+ * sv_spec_verify_noalloc - sv_spec_verify for callers that cannot allocate
+ * device memory.  The pages describe no such call; it exists for embedders
+ * such as plugins inside an inference server whose device memory is owned
+ * and budgeted by the host framework, or real-time loops that must not take
+ * the synchronisation a cudaMalloc implies, and that therefore have no
+ * workspace to hand over.
+ *
+ * Same arguments, meaning and results as sv_spec_verify, minus the
+ * workspace: the scratch lives in a 2 MiB array inside the library, present
+ * on every GPU that loads it until the process exits.  The call allocates
+ * nothing and frees nothing.
+ *   - Limit: sv_workspace_size(B, K, V, dtype) must be <= 2 MiB (for example
+ *     B = 256 with K <= 20, or B = 4096 with K <= 11); larger batches return
+ *     SV_ERR_WORKSPACE without launching anything.
+ *   - The first call on each device looks up that device's copy of the
+ *     array (with the device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array.  Each call clears what must start at
+ *     zero, so calls ordered on one stream are independent; calls that can
+ *     run at the same time on the GPU (other streams, other host threads)
+ *     race on it and must be serialised by the caller.
+ *   - The device flag word of these calls is not exposed (per-sequence
+ *     errors still show as n_accepted = 0 and out_tokens = -1).
+ */
+sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_stride,
+                                 int64_t target_pos_stride, const void* draft_logits,
+                                 int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                 sv_dtype dtype, int B, int K, int V, const int32_t* draft_tokens,
+                                 const int32_t* k_per_row, const float* temperature, float top_p,
+                                 const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                                 int32_t* n_accepted, float* diag, void* stream);
+
+/*
  * sv_kv_commit - roll each sequence's KV write pointer back to its accepted
  * length [SSD §3.3, §4.3; SD §4.3].  seq_lens[b] holds the length at the start
  * of the round (the drafts were written at seq_lens[b] .. seq_lens[b]+k_b-1);

@@ -97,6 +97,62 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
   return SV_OK;
 }
 
+sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_stride,
+                                 int64_t target_pos_stride, const void* draft_logits,
+                                 int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                 sv_dtype dtype, int B, int K, int V, const int32_t* draft_tokens,
+                                 const int32_t* k_per_row, const float* temperature, float top_p,
+                                 const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                                 int32_t* n_accepted, float* diag, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
+  if (B < 1 || K < 0 || K > kMaxK || V < 1)
+    return fail(SV_ERR_SHAPE, "need B >= 1, 0 <= K <= 20, V >= 1");
+  if (!target_logits || !uniforms || !out_tokens || !n_accepted)
+    return fail(SV_ERR_ARG, "target_logits, uniforms, out_tokens and n_accepted are required");
+  if (K > 0 && !draft_tokens) return fail(SV_ERR_ARG, "draft_tokens is required when K > 0");
+  if (K > 0 && !draft_logits && !mode)
+    return fail(SV_ERR_ARG, "draft_logits may be NULL only when every row is greedy (mode given)");
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(SV_ERR_ARG, "top_p must be in (0, 1]");
+  const int es = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)))
+    return fail(SV_ERR_ARG, "logit pointers must be aligned to their element size");
+  const long long Vl = V;
+  long long ts = target_seq_stride ? target_seq_stride : (long long)(K + 1) * Vl;
+  long long tp = target_pos_stride ? target_pos_stride : Vl;
+  long long ds = draft_seq_stride ? draft_seq_stride : (long long)K * Vl;
+  long long dp = draft_pos_stride ? draft_pos_stride : Vl;
+  if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
+  if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
+  if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
+  if (top_p < 1.0f) return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is not implemented in this build");
+  sv::VerifyLaunch L;
+  L.target = target_logits;
+  L.t_seq = ts;
+  L.t_pos = tp;
+  L.draft = draft_logits;
+  L.d_seq = ds;
+  L.d_pos = dp;
+  L.dtype = dtype;
+  L.B = B;
+  L.K = K;
+  L.V = V;
+  L.tokens = draft_tokens;
+  L.kpr = k_per_row;
+  L.temp = temperature;
+  L.top_p = top_p;
+  L.unif = uniforms;
+  L.mode = mode;
+  L.out = out_tokens;
+  L.nacc = n_accepted;
+  L.diag = diag;
+  L.workspace = nullptr;
+  L.stream = stream;
+  std::string err;
+  int s = sv::verify_launch_noalloc(L, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream) {
   if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");

@@ -33,6 +33,12 @@ struct VerifyLaunch {
 int verify_launch(const VerifyLaunch& L, std::string* err);
 size_t verify_workspace_bytes(int B, int K);
 
+// Allocation-free verify: scratch in a fixed device array of this size
+// (L.workspace is ignored).
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
+constexpr int kMaxDevices = 64;
+int verify_launch_noalloc(const VerifyLaunch& L, std::string* err);
+
 int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
                   int K, uint32_t* flags, void* stream, std::string* err);
 

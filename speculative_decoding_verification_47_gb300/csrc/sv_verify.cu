@@ -31,6 +31,8 @@
 // for another one.
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
+#include <string>
 
 #include "sv_common.cuh"
 #include "sv_internal.h"
@@ -1168,6 +1170,56 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
 size_t verify_workspace_bytes(int B, int K) {
   size_t a, b;
   return ws_layout(B, K, &a, &b);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the verify step's scratch (flag word, per-sequence
+// words, per-position statistics) lives in this fixed device array instead of
+// a caller-provided workspace.  Every GPU that loads the library holds the
+// array until the process exits.  All calls share it: each call's first
+// kernel zeroes the flag word and the sequence words it will use (the
+// statistics are written before they are read), so consecutive calls on one
+// stream are independent, but calls whose kernels overlap on the GPU (other
+// streams, other host threads) race on it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mutex;
+static void* g_noalloc_addr[kMaxDevices];
+
+int verify_launch_noalloc(const VerifyLaunch& L, std::string* err) {
+  const size_t need = verify_workspace_bytes(L.B, L.K);
+  if (need > kNoAllocScratchBytes) {
+    *err = "sv_spec_verify_noalloc: B=" + std::to_string(L.B) + ", K=" + std::to_string(L.K) +
+           " needs " + std::to_string(need) + " bytes of scratch; the built-in buffer holds " +
+           std::to_string(kNoAllocScratchBytes) + " (use sv_spec_verify with a workspace)";
+    return SV_ERR_WORKSPACE;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = std::string("sv_spec_verify_noalloc: no usable current device: ") + cudaGetErrorString(e);
+    return SV_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+      // Host code cannot use the array's name as a device address: ask the
+      // runtime for the address of this device's copy (once per device).
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        *err = std::string("sv_spec_verify_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+        return SV_ERR_CUDA;
+      }
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  VerifyLaunch L2 = L;
+  L2.workspace = scratch;
+  return verify_launch(L2, err);
 }
 
 }  // namespace sv
