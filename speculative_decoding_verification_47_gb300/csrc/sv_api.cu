@@ -64,7 +64,6 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
   if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
   if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
   if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
-  if (top_p < 1.0f) return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is not implemented in this build");
   if (!workspace || !aligned(workspace, 256))
     return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < sv::verify_workspace_bytes(B, K))
@@ -124,7 +123,6 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
   if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
   if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
   if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
-  if (top_p < 1.0f) return fail(SV_ERR_UNSUPPORTED, "top_p < 1 is not implemented in this build");
   sv::VerifyLaunch L;
   L.target = target_logits;
   L.t_seq = ts;

@@ -51,6 +51,12 @@ struct ItemStats {
   float m_d, R_d, sd_hi, sd_lo;
   int argmax;
   uint32_t errbits;
+  // top-p (rows with top_p < 1): the cut key, how many tokens with that key
+  // are kept (the first nk in index order) out of cnt, and the kept mass in
+  // the row's 2^(z*c - R) units
+  uint32_t key_t, key_d;
+  int nk_t, cnt_t, nk_d, cnt_d;
+  float et_hi, et_lo, ed_hi, ed_lo;
 };
 
 struct VerifyParams {
@@ -110,6 +116,10 @@ struct RowSlice {
   __device__ __forceinline__ float elem(int e) const {  // from global memory
     return ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2))
                    : *reinterpret_cast<const float*>(row + (size_t)e * 4);
+  }
+  __device__ __forceinline__ uint32_t bits(int e) const {  // bit pattern, from global memory
+    return ES == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2)
+                   : *reinterpret_cast<const uint32_t*>(row + (size_t)e * 4);
   }
 };
 
@@ -184,6 +194,62 @@ __device__ __forceinline__ float earg(float z, const Expo& x, float R) {
 __device__ __forceinline__ float pow2i(float k) {
   if (!(k >= -126.f)) return 0.f;
   return __int_as_float((127 + (int)k) << 23);
+}
+
+// ---------------------------------------------------------------------------
+// Top-p order [FS §3.2]: tokens ranked by (probability desc, index asc) are
+// the tokens ranked by (logit desc, index asc), because the temperature
+// softmax is increasing in the logit.  A logit is identified by the
+// order-preserving unsigned key of its bit pattern (-0 taken as +0), so
+// "ranked before" is "larger key, or the same key at a smaller index".
+// ---------------------------------------------------------------------------
+template <int ES>
+__device__ __forceinline__ uint32_t okey(uint32_t b) {
+  if (ES == 2) {
+    b &= 0xffffu;
+    if (b == 0x8000u) b = 0u;
+    return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+  } else {
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+}
+
+// inverse of okey: the bit pattern of a key
+template <int ES>
+__device__ __forceinline__ uint32_t key_bits(uint32_t k) {
+  if (ES == 2) return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+  return (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+}
+
+template <int ES>
+__device__ __forceinline__ float bits_val(uint32_t b) {
+  return ES == 2 ? __uint_as_float(b << 16) : __uint_as_float(b);
+}
+
+// bit pattern of a value that is exactly representable in the row's type
+template <int ES>
+__device__ __forceinline__ uint32_t val_bits(float v) {
+  return ES == 2 ? (__float_as_uint(v) >> 16) : __float_as_uint(v);
+}
+
+// bit pattern of the largest representable value <= v
+template <int ES>
+__device__ __forceinline__ uint32_t floor_bits(float v) {
+  return ES == 2 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rd(v)) : __float_as_uint(v);
+}
+
+// element j of a 16-byte unit as its bit pattern
+template <int ES>
+__device__ __forceinline__ uint32_t unit_bits(const uint4& v, int j) {
+  if (ES == 4) return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+  const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
+  return (j & 1) ? (w >> 16) : (w & 0xffffu);
+}
+
+// kept by the cut (key kk, first dropped index kc among the tokens of key kk)
+__device__ __forceinline__ bool topp_kept(uint32_t key, int idx, uint32_t kk, int kc) {
+  return key > kk || (key == kk && idx < kc);
 }
 
 // ---------------------------------------------------------------------------
@@ -443,6 +509,17 @@ struct Weight {
   Expo x;
   float Rt, Rd, rho_hi, rho_lo;
   bool p_only;
+  // top-p cuts of the two rows (every token kept: key 0, index INT_MAX)
+  uint32_t kt, kd;
+  int ct, cd;
+  // weight of element e with logits (zt, zd) and keys (yt, yd), top-p masks applied
+  __device__ __forceinline__ float masked(float zt, float zd, uint32_t yt, uint32_t yd,
+                                          int e) const {
+    const float a = topp_kept(yt, e, kt, ct) ? e2(zt, x, -Rt) : 0.f;
+    if (p_only) return a;
+    const float b = topp_kept(yd, e, kd, cd) ? e2(zd, x, -Rd) : 0.f;
+    return fmaxf(0.f, __fmaf_rn(-rho_lo, b, __fmaf_rn(-rho_hi, b, a)));
+  }
   __device__ __forceinline__ float operator()(float zt, float zd) const {
     const float a = e2(zt, x, -Rt);
     if (p_only) return a;
@@ -511,26 +588,77 @@ struct PairRead {
       if (!W.p_only) vd = ldg_unit(sd, u);
     }
   }
+  template <bool TOPP>
   __device__ __forceinline__ float value(int u, const Weight& W, const uint4& vt,
                                          const uint4& vd) const {
     constexpr int EPU = 16 / ES;
     if (u >= st.n_units) return 0.f;
-    if (full(u)) return wsum_full<ES>(vt, W.p_only ? vt : vd, W);
-    float acc = 0.f;
     const int eb = st.ebase0 + u * EPU;
+    if (full(u)) {
+      if (!TOPP) return wsum_full<ES>(vt, W.p_only ? vt : vd, W);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < EPU; ++j) {
+        const uint32_t bt = unit_bits<ES>(vt, j), bd = W.p_only ? 0u : unit_bits<ES>(vd, j);
+        acc += W.masked(bits_val<ES>(bt), bits_val<ES>(bd), okey<ES>(bt), okey<ES>(bd), eb + j);
+      }
+      return acc;
+    }
+    float acc = 0.f;
     for (int j = 0; j < EPU; ++j) {
       const int e = eb + j;
       if (e < st.e0 || e >= st.e1) continue;
-      acc += W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+      acc += elem_w<TOPP>(e, W);
     }
     return acc;
   }
+  template <bool TOPP>
   __device__ __forceinline__ float elem_w(int e, const Weight& W) const {
-    return W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+    if (!TOPP) return W(st.elem(e), W.p_only ? 0.f : sd.elem(e));
+    const uint32_t bt = st.bits(e), bd = W.p_only ? 0u : sd.bits(e);
+    return W.masked(bits_val<ES>(bt), bits_val<ES>(bd), okey<ES>(bt), okey<ES>(bd), e);
   }
 };
 
+// ---------------------------------------------------------------------------
+// Top-p selection state of one row.  The cut lies in the key window
+// [lo, hi]; A is the mass of all keys above hi.  A "count" pass (window of
+// at most kNBc keys) histograms exact token counts per key, so a key's mass
+// is count * 2^(z*c - R) with no summation error; a wider window first takes
+// a "mass" pass over kNBm bins of 2^shift keys each, in 64-bit fixed point
+// (integer sums: the same bits whatever the order of the atomic adds).
+// ---------------------------------------------------------------------------
+constexpr int kNBc = 2048;
+constexpr int kNBm = 1024;
+constexpr int kHistRowBytes = 8448;  // >= (kNBc + 1) * 4 and kNBm * 8
+constexpr int kHistBytes = 2 * kHistRowBytes;
+
+struct TopSel {
+  uint32_t lo, hi;
+  int mode;      // 0 resolved, 1 count pass next, 2 mass pass next
+  int shift;     // mass pass: bin = (key - lo) >> shift
+  float scale;   // mass pass: element mass e * 2^a2 as an integer (exact scaling)
+  float descale; // 2^-a2
+  float R;       // the row's reference exponent
+  DF S, thr;     // row normaliser and top_p * S
+  DF A;          // mass of the keys above the window
+  uint32_t kx;   // key of the draft token's logit in this row
+  // result
+  uint32_t kstar;  // cut key
+  int cstar;       // tokens with the cut key
+  int nk;          // of which the first nk in index order are kept
+  int lt;          // tokens with key kx and an index below the draft token's
+  DF E;            // kept mass
+};
+
 struct Shared {
+  // top-p
+  TopSel ts[2];
+  int selbin[2], lowbin[2], sel_cnt[2];
+  DF sel_excl[2];
+  uint32_t rcnt[kMaxRounds];
+  uint32_t ccnt[kCmax];
+  int tcut, rrem, xtok;
   // all-gather slots, indexed by the writing CTA's rank
   RowAcc g_t[kCmax], g_d[kCmax];
   DF g_w[kCmax];
@@ -573,17 +701,443 @@ __device__ void write_outputs(const VerifyParams& P, int b, int n, int y, bool e
 }
 
 // ---------------------------------------------------------------------------
+// Cluster helpers (a cluster of one CTA synchronises and addresses locally)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void csync(cg::cluster_group& cluster, int C) {
+  if (C > 1) cluster.sync();
+  else __syncthreads();
+}
+
+template <typename T>
+__device__ __forceinline__ T* remote(cg::cluster_group& cluster, int C, T* p, int q) {
+  return C > 1 ? cluster.map_shared_rank(p, q) : p;
+}
+
+// ---------------------------------------------------------------------------
+// Top-p selection [FS §3.2]: keep a token iff the mass ranked strictly before
+// it is at most top_p * S.  The mass ranked before a token is the mass of all
+// larger keys plus that of the equal keys at smaller indices, so the kept set
+// is every key above a cut key k*, and the first nk tokens (index order) of
+// key k*.  The search narrows a key window by histogram passes over the row
+// (re-read from L2), every CTA of the cluster counting its own slice.
+//
+// Start window: [key(tau0 point), key(max)], where tau0 = (1 - top_p) S / (2V)
+// in e units.  A token whose e lies below tau0 has, ranked before it, every
+// token above tau0, of mass > S - V tau0 > top_p S: it is never kept.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void sel_set_mode(TopSel& t) {
+  const uint32_t span = t.hi - t.lo;
+  if (span < (uint32_t)kNBc) {
+    t.mode = 1;
+    t.shift = 0;
+  } else {
+    t.mode = 2;
+    t.shift = (32 - __clz(span)) - 10;  // (span >> shift) < kNBm
+  }
+}
+
+struct SelRow {
+  uint32_t lo, span, kx, lt;
+  int shift, mode, x;
+  float R, scale;
+  uint32_t* hc;             // count pass: kNBc counts, then the lt slot
+  unsigned long long* hm;   // mass pass: kNBm fixed-point sums
+};
+
+__device__ __forceinline__ SelRow sel_row(const TopSel& t, unsigned char* h, int x, bool active) {
+  SelRow r;
+  r.lo = t.lo;
+  r.span = t.hi - t.lo;
+  r.kx = t.kx;
+  r.lt = 0;
+  r.shift = t.shift;
+  r.mode = active ? t.mode : 0;
+  r.x = x;
+  r.R = t.R;
+  r.scale = t.scale;
+  r.hc = reinterpret_cast<uint32_t*>(h);
+  r.hm = reinterpret_cast<unsigned long long*>(h);
+  return r;
+}
+
+template <int ES>
+__device__ __forceinline__ void sel_elem(SelRow& s, uint32_t bits, int e, const Expo& X) {
+  const uint32_t key = okey<ES>(bits);
+  const uint32_t d = key - s.lo;
+  if (s.mode == 1) {
+    if (d <= s.span) atomicAdd(s.hc + d, 1u);
+    s.lt += (key == s.kx && e < s.x) ? 1u : 0u;
+  } else if (d <= s.span) {
+    atomicAdd(s.hm + (d >> s.shift), __float2ull_rn(e2(bits_val<ES>(bits), X, -s.R) * s.scale));
+  }
+}
+
+template <int ES>
+__device__ __forceinline__ void sel_unit(SelRow& s, const RowSlice<ES>& rs, int u, int ub0, int ub1,
+                                         const uint4& v, const Expo& X) {
+  constexpr int EPU = 16 / ES;
+  const int eb = rs.ebase0 + u * EPU;
+  if (u >= ub0 && u < ub1) {
+#pragma unroll
+    for (int j = 0; j < EPU; ++j) sel_elem<ES>(s, unit_bits<ES>(v, j), eb + j, X);
+  } else if (u < rs.n_units) {
+    for (int j = 0; j < EPU; ++j) {
+      const int e = eb + j;
+      if (e >= rs.e0 && e < rs.e1) sel_elem<ES>(s, rs.bits(e), e, X);
+    }
+  }
+}
+
+// Thread t gathers bins [8t, 8t+8) (count pass) or [4t, 4t+4) (mass pass)
+// of one row's histogram from every CTA of the cluster: integer sums, so
+// every CTA holds the same totals.
+__device__ __forceinline__ void sel_reduce(cg::cluster_group& cluster, int C, unsigned char* h,
+                                           bool counts, uint32_t (&w)[8], uint32_t* lt) {
+  const int tid = threadIdx.x;
+  if (counts) {
+    uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int q = 0; q < C; ++q) {
+      const uint4* p = remote(cluster, C, reinterpret_cast<uint4*>(h) + 2 * tid, q);
+      const uint4 x = p[0], y = p[1];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = a[k];
+    if (tid == 0) {
+      uint32_t l = 0;
+      for (int q = 0; q < C; ++q) l += *remote(cluster, C, reinterpret_cast<uint32_t*>(h) + kNBc, q);
+      *lt = l;
+    }
+  } else {
+    unsigned long long m[4] = {0ull, 0ull, 0ull, 0ull};
+    for (int q = 0; q < C; ++q) {
+      const ulonglong2* p = remote(cluster, C, reinterpret_cast<ulonglong2*>(h) + 2 * tid, q);
+      const ulonglong2 x = p[0], y = p[1];
+      m[0] += x.x; m[1] += x.y; m[2] += y.x; m[3] += y.y;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[2 * k] = (uint32_t)m[k];
+      w[2 * k + 1] = (uint32_t)(m[k] >> 32);
+    }
+  }
+}
+
+// Sum of v over the threads above this one (threadIdx greater), in
+// double-float; the same bits in every CTA that scans the same values.
+__device__ __forceinline__ DF block_suffix_excl(DF v, DF* wtot, int lane, int warp) {
+  DF s = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF n = DF{__shfl_down_sync(0xffffffffu, s.hi, o), __shfl_down_sync(0xffffffffu, s.lo, o)};
+    if (lane + o < 32) s = df_add(s, n);
+  }
+  DF ex = DF{__shfl_down_sync(0xffffffffu, s.hi, 1), __shfl_down_sync(0xffffffffu, s.lo, 1)};
+  if (lane == 31) ex = DF{0.f, 0.f};
+  if (lane == 0) wtot[warp] = s;
+  __syncthreads();
+  DF above = DF{0.f, 0.f};
+  for (int w = kWarps - 1; w > warp; --w) above = df_add(above, wtot[w]);
+  return df_add(above, ex);
+}
+
+// After a pass: find the bin holding the cut (mass above it <= top_p S <
+// mass above it plus its own) and narrow the window to it, or, after a count
+// pass, fix the cut key and how many of its tokens are kept.
+template <int ES>
+__device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t lt_tot,
+                            const Expo& X) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TopSel s = sh.ts[r];
+  const bool cm = s.mode == 1;
+  const int nb = cm ? 8 : 4;
+  DF m[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    m[q] = DF{0.f, 0.f};
+    if (cm) {
+      if (w[q]) {
+        const uint32_t key = s.lo + (uint32_t)(8 * tid + q);
+        const float e = e2(bits_val<ES>(key_bits<ES>(key)), X, -s.R);
+        m[q] = df_mul_f(DF{e, 0.f}, (float)w[q]);
+      }
+    } else if (q < 4) {
+      const unsigned long long v =
+          (unsigned long long)w[2 * q] | ((unsigned long long)w[2 * q + 1] << 32);
+      if (v) {
+        const float hi = __ull2float_rn(v);
+        const float lo = __ll2float_rn((long long)(v - __float2ull_rz(hi)));
+        m[q] = DF{hi * s.descale, lo * s.descale};
+      }
+    }
+  }
+  DF T = DF{0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) T = df_add(T, m[q]);
+  const DF above = df_add(s.A, block_suffix_excl(T, sh.scan, lane, warp));
+  DF run = above;
+  int cand = -1, low = 0x7fffffff;
+#pragma unroll
+  for (int q = 7; q >= 0; --q) {
+    if (q < nb && df_pos(m[q])) {
+      const DF inc = df_add(run, m[q]);
+      const int g = nb * tid + q;
+      if (cand < 0 && df_gt(inc, s.thr) && !df_gt(run, s.thr)) cand = g;
+      low = g;
+      run = inc;
+    }
+  }
+  if (cand >= 0) atomicMax(&sh.selbin[r], cand);
+  if (low != 0x7fffffff) atomicMin(&sh.lowbin[r], low);
+  __syncthreads();
+  int bs = sh.selbin[r];
+  if (bs < 0) bs = sh.lowbin[r];  // all of the window fits under top_p S (rounding): keep it all
+  if (bs != 0x7fffffff && bs / nb == tid) {
+    DF run2 = above;
+#pragma unroll
+    for (int q = 7; q >= 0; --q) {
+      if (q < nb && df_pos(m[q])) {
+        if (nb * tid + q == bs) {
+          sh.sel_excl[r] = run2;
+          sh.sel_cnt[r] = cm ? (int)w[q] : 0;
+        }
+        run2 = df_add(run2, m[q]);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    TopSel& t = sh.ts[r];
+    if (bs == 0x7fffffff) {  // no mass in the window (not reachable for a finite row): keep all
+      t.mode = 0;
+      t.kstar = 0u;
+      t.cstar = 0;
+      t.nk = 0x7fffffff;
+      t.lt = 0;
+      t.E = t.S;
+    } else if (cm) {
+      const uint32_t kk = t.lo + (uint32_t)bs;
+      const float es = e2(bits_val<ES>(key_bits<ES>(kk)), X, -t.R);
+      const DF excl = sh.sel_excl[r];
+      const int c = sh.sel_cnt[r];
+      // token n (0-based, index order) of key kk has mass excl + n*es ranked
+      // before it: kept iff n <= (thr - excl) / es
+      const DF q = df_div(df_sub(t.thr, excl), DF{es, 0.f});
+      float f = floorf(q.hi);
+      if (f == q.hi && q.lo < 0.f) f -= 1.f;
+      int nk = (f + 1.f >= (float)c) ? c : (f >= 0.f ? (int)f + 1 : 1);
+      t.kstar = kk;
+      t.cstar = c;
+      t.nk = nk;
+      t.E = df_add(excl, df_mul_f(DF{es, 0.f}, (float)nk));
+      t.lt = (int)lt_tot;
+      t.mode = 0;
+    } else {
+      const unsigned long long nlo = (unsigned long long)t.lo + ((unsigned long long)bs << t.shift);
+      unsigned long long nhi = nlo + ((1ull << t.shift) - 1ull);
+      if (nhi > (unsigned long long)t.hi) nhi = t.hi;
+      t.lo = (uint32_t)nlo;
+      t.hi = (uint32_t)nhi;
+      t.A = sh.sel_excl[r];
+      sel_set_mode(t);
+    }
+  }
+  __syncthreads();
+}
+
+// Top-p cut of the target row (and of the draft row when `two`) of one item.
+// Every CTA of the cluster ends with the same sh.ts[] results.
+template <int ES>
+__device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsigned char* hist,
+                                         cg::cluster_group& cluster, int C, int b, int i, int kb,
+                                         bool two, const Expo& X, const RowSlice<ES>& st,
+                                         const RowSlice<ES>& sd, const RowAcc& row_t,
+                                         const RowAcc& row_d) {
+  const int tid = threadIdx.x;
+  if (tid < 2 && (tid == 0 || two)) {
+    const int r = tid;
+    int x = -1;
+    if (i < kb) {
+      x = P.tokens[(size_t)b * P.K + i];
+      if (x < 0 || x >= P.V) x = -1;
+    }
+    if (r == 0) sh.xtok = x;
+    const RowAcc& row = r ? row_d : row_t;
+    const RowSlice<ES>& rs = r ? sd : st;
+    TopSel t;
+    t.R = row.R;
+    t.S = row.s;
+    t.thr = df_mul_f(row.s, P.top_p);
+    t.A = DF{0.f, 0.f};
+    t.hi = okey<ES>(val_bits<ES>(row.mx));
+    const float tau0 = 0.5f * (1.f - P.top_p) * (row.s.hi / (float)P.V);
+    const float z0 = __fdiv_rn(__log2f(tau0) + row.R, X.chi);
+    uint32_t lo;
+    if (!(z0 < row.mx)) lo = t.hi;
+    else if (!(z0 > -INFINITY)) lo = 0u;
+    else lo = okey<ES>(floor_bits<ES>(z0));
+    t.lo = min(lo, t.hi);
+    sel_set_mode(t);
+    // fixed point for mass passes: S * 2^a2 < 2^61
+    const int eS = ((__float_as_int(row.s.hi) >> 23) & 0xff) - 127;
+    const int a2 = 60 - eS;
+    t.scale = __int_as_float((127 + a2) << 23);
+    t.descale = __int_as_float((127 - a2) << 23);
+    t.kx = x >= 0 ? okey<ES>(rs.bits(x)) : 0u;
+    t.kstar = 0u;
+    t.cstar = 0;
+    t.nk = 0x7fffffff;
+    t.lt = 0;
+    t.E = row.s;
+    sh.ts[r] = t;
+  }
+  __syncthreads();
+  for (int pass = 0; pass < 5; ++pass) {
+    const bool a0 = sh.ts[0].mode != 0, a1 = two && sh.ts[1].mode != 0;
+    if (!a0 && !a1) break;
+    for (int k = tid; k < kHistBytes / 16; k += kThreads)
+      reinterpret_cast<uint4*>(hist)[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+      sh.selbin[0] = sh.selbin[1] = -1;
+      sh.lowbin[0] = sh.lowbin[1] = 0x7fffffff;
+    }
+    __syncthreads();
+    SelRow r0 = sel_row(sh.ts[0], hist, sh.xtok, a0);
+    SelRow r1 = sel_row(sh.ts[1], hist + kHistRowBytes, sh.xtok, a1);
+    {
+      const int NU = two ? max(st.n_units, sd.n_units) : st.n_units;
+      const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
+      for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight) {
+        uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
+#pragma unroll
+        for (int k = 0; k < kLoadsInFlight; ++k) {
+          const int u = u0 + k * kThreads;
+          vt[k] = (a0 && u >= tb0 && u < tb1) ? ldg_unit(st, u) : make_uint4(0, 0, 0, 0);
+          vd[k] = (a1 && u >= db0 && u < db1) ? ldg_unit(sd, u) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kLoadsInFlight; ++k) {
+          const int u = u0 + k * kThreads;
+          if (a0) sel_unit<ES>(r0, st, u, tb0, tb1, vt[k], X);
+          if (a1) sel_unit<ES>(r1, sd, u, db0, db1, vd[k], X);
+        }
+      }
+    }
+    if (r0.mode == 1 && r0.lt) atomicAdd(r0.hc + kNBc, r0.lt);
+    if (r1.mode == 1 && r1.lt) atomicAdd(r1.hc + kNBc, r1.lt);
+    csync(cluster, C);  // every CTA's histograms are complete
+    uint32_t w0[8], w1[8], lt0 = 0, lt1 = 0;
+    if (a0) sel_reduce(cluster, C, hist, r0.mode == 1, w0, &lt0);
+    if (a1) sel_reduce(cluster, C, hist + kHistRowBytes, r1.mode == 1, w1, &lt1);
+    csync(cluster, C);  // every CTA has read every histogram
+    if (a0) sel_resolve<ES>(sh, 0, w0, lt0, X);
+    if (a1) sel_resolve<ES>(sh, 1, w1, lt1, X);
+  }
+}
+
+// Index of token nk (0-based, index order) among the tokens of key kk in a
+// row: the first one the top-p cut drops.  Each CTA counts the key per unit
+// of its slice; the CTA holding token nk finds its round, unit and element
+// and writes the index into every CTA.  0x7fffffff if the row has <= nk.
+template <int ES>
+__device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group& cluster, int C,
+                                    int rank, const RowSlice<ES>& rs, uint32_t kk, int nk) {
+  constexpr int EPU = 16 / ES;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NU = rs.n_units, rounds = (NU + kThreads - 1) / kThreads;
+  const int ub0 = rs.ub0(), ub1 = rs.ub1();
+  for (int u = tid; u < rounds * kThreads; u += kThreads) {
+    uint32_t c = 0;
+    if (u >= ub0 && u < ub1) {
+      const uint4 v = ldg_unit(rs, u);
+#pragma unroll
+      for (int j = 0; j < EPU; ++j) c += okey<ES>(unit_bits<ES>(v, j)) == kk ? 1u : 0u;
+    } else if (u < NU) {
+      const int eb = rs.ebase0 + u * EPU;
+      for (int j = 0; j < EPU; ++j) {
+        const int e = eb + j;
+        if (e >= rs.e0 && e < rs.e1 && okey<ES>(rs.bits(e)) == kk) ++c;
+      }
+    }
+    iv[u] = c;
+  }
+  __syncthreads();
+  for (int r = warp; r < rounds; r += kWarps) {
+    uint32_t a = 0;
+    for (int t = lane; t < kThreads; t += 32) a += iv[r * kThreads + t];
+    a = __reduce_add_sync(0xffffffffu, a);
+    if (lane == 0) sh.rcnt[r] = a;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t a = 0;
+    for (int r = lane; r < rounds; r += 32) a += sh.rcnt[r];
+    a = __reduce_add_sync(0xffffffffu, a);
+    if (lane < C) *remote(cluster, C, &sh.ccnt[rank], lane) = a;
+  }
+  if (tid == 0) sh.tcut = 0x7fffffff;
+  csync(cluster, C);
+  uint32_t off = 0;
+  for (int q = 0; q < rank; ++q) off += sh.ccnt[q];
+  const uint32_t mine = sh.ccnt[rank];
+  if ((uint32_t)nk >= off && (uint32_t)nk - off < mine) {  // (uniform inside this CTA)
+    if (tid == 0) {
+      uint32_t rem = (uint32_t)nk - off;
+      int r = 0;
+      for (; r < rounds - 1; ++r) {
+        if (rem < sh.rcnt[r]) break;
+        rem -= sh.rcnt[r];
+      }
+      sh.rsel = r;
+      sh.rrem = (int)rem;
+    }
+    __syncthreads();
+    const int r = sh.rsel;
+    const uint32_t rem = (uint32_t)sh.rrem;
+    const uint32_t v = iv[r * kThreads + tid];
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    if (lane == 31) sh.r_i[warp] = (int)inc;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) inc += (uint32_t)sh.r_i[w];
+    if (v > 0 && inc > rem && inc - v <= rem) {
+      uint32_t left = rem - (inc - v);  // tokens of key kk to pass over inside this unit
+      const int eb = rs.ebase0 + (r * kThreads + tid) * EPU;
+      int idx = 0x7fffffff;
+      for (int j = 0; j < EPU; ++j) {
+        const int e = eb + j;
+        if (e < rs.e0 || e >= rs.e1 || okey<ES>(rs.bits(e)) != kk) continue;
+        if (left == 0) {
+          idx = e;
+          break;
+        }
+        --left;
+      }
+      for (int q = 0; q < C; ++q) *remote(cluster, C, &sh.tcut, q) = idx;
+    }
+  }
+  csync(cluster, C);
+  return sh.tcut;
+}
+
+// ---------------------------------------------------------------------------
 // Finisher: draw the resample (or bonus) token of sequence b at cut j with
 // the uniform uK.  Every CTA of the cluster takes part.  Pass over the rows:
 // each thread's unit sums go to shared memory in index order (round r holds
 // units r*kThreads .. r*kThreads + kThreads-1); then round totals, the
 // cluster-wide owner of u*total, the round, the unit and the element.
 // ---------------------------------------------------------------------------
-template <int ES>
+template <int ES, bool TOPP>
 __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals,
                                     cg::cluster_group& cluster, int C, int rank, int b, int kb,
                                     float T, int j, float uK, int e0, int e1, float Rt, float Rd,
-                                    DF S_t, DF S_d) {
+                                    DF S_t, DF S_d, uint32_t kt, int nkt, int cntt, uint32_t kd,
+                                    int nkd, int cntd) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool bonus = (j == kb);
   const Expo X = make_expo(T);
@@ -604,6 +1158,17 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
     W.rho_hi = rho.hi;
     W.rho_lo = rho.lo;
   }
+  W.kt = W.kd = 0u;
+  W.ct = W.cd = 0x7fffffff;
+  if (TOPP) {  // (S_t, S_d are the kept masses here)
+    uint32_t* iv = reinterpret_cast<uint32_t*>(vals);
+    W.kt = kt;
+    if (nkt < cntt) W.ct = tie_cut<ES>(sh, iv, cluster, C, rank, pr.st, kt, nkt);
+    if (!bonus) {
+      W.kd = kd;
+      if (nkd < cntd) W.cd = tie_cut<ES>(sh, iv, cluster, C, rank, pr.sd, kd, nkd);
+    }
+  }
   const int NU = pr.st.n_units;
   const int rounds = (NU + kThreads - 1) / kThreads;
   DF slice_w{0.f, 0.f};
@@ -620,7 +1185,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
 #pragma unroll
       for (int k = 0; k < kLoadsInFlight; ++k) {
         const int u = u0 + k * kThreads;
-        if (u < rounds * kThreads) vals[u] = pr.value(u, W, vt[k], vd[k]);
+        if (u < rounds * kThreads) vals[u] = pr.template value<TOPP>(u, W, vt[k], vd[k]);
       }
     }
     __syncthreads();
@@ -725,7 +1290,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   for (int q = 0; q < EPU; ++q) {
     const int e = eb + q;
     if (e < pr.st.e0 || e >= pr.st.e1) continue;
-    const float wv = pr.elem_w(e, W);
+    const float wv = pr.template elem_w<TOPP>(e, W);
     if (wv > 0.f) ylast = e;
     cum = df_add(cum, DF{wv, 0.f});
     if (!past_end && wv > 0.f && df_gt(cum, rem)) {
@@ -740,7 +1305,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
 // Decision of one item and its publication in the sequence word (rank 0,
 // thread 0).  Returns 1 if this item completes the sequence's prefix, with
 // the cut position and whether it is an error in *j_out / *err_out.
-template <int ES>
+template <int ES, bool TOPP>
 __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int b, int kb,
                                    bool greedy, bool has_draft, const Expo& X, const RowAcc& row_t,
                                    const RowAcc& row_d, bool bad_t, bool bad_d, int* j_out,
@@ -760,17 +1325,28 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
       // p(x)/q(x) = 2^((z_t - z_d)*c + R_d - R_t) * S_d / S_t, formed in the
       // exponent domain so that neither factor underflows on its own;
       // zero where the exact probability underflows double precision.
+      // Under top-p, S is the kept mass and a dropped token has probability 0.
+      DF Et = row_t.s, Ed = row_d.s;
+      bool keep_t = true, keep_d = true;
+      if (TOPP) {
+        const TopSel& a = sh.ts[0];
+        const TopSel& d = sh.ts[1];
+        Et = a.E;
+        Ed = d.E;
+        keep_t = a.kx > a.kstar || (a.kx == a.kstar && a.lt < a.nk);
+        keep_d = d.kx > d.kstar || (d.kx == d.kstar && d.lt < d.nk);
+      }
       const float lt = (zt_x - row_t.mx) * X.chi, ld = (zd_x - row_d.mx) * X.chi;
       float r;
-      if (!(ld > -1074.f) || !(lt > -1074.f)) {
+      if (!keep_t || !keep_d || !(ld > -1074.f) || !(lt > -1074.f)) {
         r = 0.f;
       } else {
         const float a = zt_x - zd_x;
         const float ex = __fmaf_rn(a, X.chi, a * X.clo) + (row_d.R - row_t.R);
-        r = ex2(ex) * df_to_float(df_div(row_d.s, row_t.s));
+        r = ex2(ex) * df_to_float(df_div(Ed, Et));
       }
-      diag_px = ex2(earg(zt_x, X, row_t.R)) / row_t.s.hi;
-      diag_qx = ex2(earg(zd_x, X, row_d.R)) / row_d.s.hi;
+      diag_px = keep_t ? ex2(earg(zt_x, X, row_t.R)) / Et.hi : 0.f;
+      diag_qx = keep_d ? ex2(earg(zd_x, X, row_d.R)) / Ed.hi : 0.f;
       diag_r = r;
       reject = !(u_i < r);
     }
@@ -786,6 +1362,23 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
   s.sd_lo = row_d.s.lo;
   s.argmax = row_t.amax;
   s.errbits = errbits;
+  const bool sel = TOPP && !greedy && !bad_t && !bad_d;
+  if (sel) {
+    const TopSel& a = sh.ts[0];
+    s.key_t = a.kstar;
+    s.nk_t = a.nk;
+    s.cnt_t = a.cstar;
+    s.et_hi = a.E.hi;
+    s.et_lo = a.E.lo;
+    if (has_draft) {
+      const TopSel& d = sh.ts[1];
+      s.key_d = d.kstar;
+      s.nk_d = d.nk;
+      s.cnt_d = d.cstar;
+      s.ed_hi = d.E.hi;
+      s.ed_lo = d.E.lo;
+    }
+  }
   P.stats[(size_t)b * (P.K + 1) + i] = s;
   if (P.diag) {
     float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
@@ -795,11 +1388,11 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
     } else if (!bad_t) {
       // normaliser relative to the row max: S_R * 2^(R - m*c)
       dg[SV_DIAG_S_T] = df_to_float(row_t.s) * ex2(-earg(row_t.mx, X, row_t.R));
-      dg[SV_DIAG_MASS_T] = 1.f;
+      dg[SV_DIAG_MASS_T] = sel ? df_to_float(df_div(sh.ts[0].E, row_t.s)) : 1.f;
       if (has_draft && !bad_d) {
         dg[SV_DIAG_M_D] = row_d.mx;
         dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
-        dg[SV_DIAG_MASS_D] = 1.f;
+        dg[SV_DIAG_MASS_D] = sel ? df_to_float(df_div(sh.ts[1].E, row_d.s)) : 1.f;
         dg[SV_DIAG_P_X] = diag_px;
         dg[SV_DIAG_Q_X] = diag_qx;
         dg[SV_DIAG_RATIO] = diag_r;
@@ -821,7 +1414,7 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
   return (!was && now) ? 1 : 0;
 }
 
-template <int ES>
+template <int ES, bool TOPP>
 __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -830,7 +1423,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   const int item = blockIdx.x / C;
   const int i = item / P.B, b = item % P.B;
 
-  extern __shared__ __align__(16) float vals[];  // finisher's unit sums
+  extern __shared__ __align__(16) float vals[];  // finisher's unit sums; top-p histograms
   __shared__ Shared sh;
 
   // ---- per-row parameters (identical in every CTA of the cluster) ----
@@ -965,11 +1558,14 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
                      (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
   const bool bad_d = has_draft && (!(row_d.mx > -INFINITY && row_d.mx < INFINITY) ||
                                    !(row_d.R > kRnone && row_d.R < INFINITY));
+  if (TOPP && !greedy && !bad_t && !bad_d)
+    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb, has_draft,
+                    X, st, sd, row_t, row_d);
 
   // ---- decision and publication (rank 0, one thread) ----
   if (rank == 0 && tid == 0) {
     int j1, e1_;
-    const int fin = decide<ES>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
+    const int fin = decide<ES, TOPP>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
                                &j1, &e1_);
     if (C > 1) {
       for (int r = 0; r < C; ++r) {
@@ -1015,14 +1611,40 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   }
   float Rt = row_t.R, Rd = row_d.R;
   DF S_t = row_t.s, S_d = row_d.s;
+  uint32_t kt = 0u, kd = 0u;
+  int nkt = 0x7fffffff, cntt = 0, nkd = 0x7fffffff, cntd = 0;
   if (j != i) {
     const ItemStats* sj = P.stats + (size_t)b * (P.K + 1) + j;
     Rt = __ldcg(&sj->R_t);
     Rd = __ldcg(&sj->R_d);
     S_t = DF{__ldcg(&sj->st_hi), __ldcg(&sj->st_lo)};
     S_d = DF{__ldcg(&sj->sd_hi), __ldcg(&sj->sd_lo)};
+    if (TOPP) {  // kept masses and cuts
+      S_t = DF{__ldcg(&sj->et_hi), __ldcg(&sj->et_lo)};
+      kt = __ldcg(&sj->key_t);
+      nkt = __ldcg(&sj->nk_t);
+      cntt = __ldcg(&sj->cnt_t);
+      if (j < kb) {
+        S_d = DF{__ldcg(&sj->ed_hi), __ldcg(&sj->ed_lo)};
+        kd = __ldcg(&sj->key_d);
+        nkd = __ldcg(&sj->nk_d);
+        cntd = __ldcg(&sj->cnt_d);
+      }
+    }
+  } else if (TOPP) {
+    S_t = sh.ts[0].E;
+    kt = sh.ts[0].kstar;
+    nkt = sh.ts[0].nk;
+    cntt = sh.ts[0].cstar;
+    if (j < kb) {
+      S_d = sh.ts[1].E;
+      kd = sh.ts[1].kstar;
+      nkd = sh.ts[1].nk;
+      cntd = sh.ts[1].cstar;
+    }
   }
-  finish<ES>(P, sh, vals, cluster, C, rank, b, kb, T, j, uK, e0, e1, Rt, Rd, S_t, S_d);
+  finish<ES, TOPP>(P, sh, vals, cluster, C, rank, b, kb, T, j, uK, e0, e1, Rt, Rd, S_t, S_d, kt, nkt,
+                   cntt, kd, nkd, cntd);
 }
 
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, int B) {
@@ -1044,17 +1666,19 @@ size_t ws_layout(int B, int K, size_t* words_off, size_t* stats_off) {
   return (off + 255) / 256 * 256;
 }
 
-static int g_configured[2] = {0, 0};
+static int g_configured[4] = {0, 0, 0, 0};
 
-template <int ES>
+template <int ES, bool TOPP>
 static cudaError_t configure() {
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxRounds * kThreads * (int)sizeof(float));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(verify_kernel<ES>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int ES>
+template <int ES, bool TOPP>
 static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem, cudaStream_t stream) {
   VerifyParams P = P0;
   cudaLaunchConfig_t cfg = {};
@@ -1069,7 +1693,7 @@ static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<ES>, P);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<ES, TOPP>, P);
 }
 
 static int sm_count() {
@@ -1112,11 +1736,14 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     *err = "vocabulary too large for the cluster slice layout";
     return SV_ERR_SHAPE;
   }
-  const size_t smem = (size_t)rounds * kThreads * sizeof(float);
+  const bool topp = L.top_p < 1.0f;
+  size_t smem = (size_t)rounds * kThreads * sizeof(float);
+  if (topp && smem < (size_t)kHistBytes) smem = kHistBytes;
   cudaError_t e;
-  const int gi = ES == 2 ? 0 : 1;
+  const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   if (!g_configured[gi]) {
-    e = ES == 2 ? configure<2>() : configure<4>();
+    e = ES == 2 ? (topp ? configure<2, true>() : configure<2, false>())
+                : (topp ? configure<4, true>() : configure<4, false>());
     if (e != cudaSuccess) {
       *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return SV_ERR_CUDA;
@@ -1159,7 +1786,10 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     return SV_ERR_CUDA;
   }
   const int items = (L.K + 1) * L.B;
-  e = ES == 2 ? launch<2>(P, C, items, smem, stream) : launch<4>(P, C, items, smem, stream);
+  if (ES == 2)
+    e = topp ? launch<2, true>(P, C, items, smem, stream) : launch<2, false>(P, C, items, smem, stream);
+  else
+    e = topp ? launch<4, true>(P, C, items, smem, stream) : launch<4, false>(P, C, items, smem, stream);
   if (e != cudaSuccess) {
     *err = std::string("verify launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;

@@ -185,7 +185,9 @@ def synth_verify(
     threads: int | None = None,
 ) -> VerifyInputs:
     """Draw a verify batch.  ``k_per_row``, ``temperature``, ``sigma`` and
-    ``mode`` are per-row arrays (or scalars broadcast over B)."""
+    ``mode`` are per-row arrays (or scalars broadcast over B).  ``top_p`` is
+    kept as the float32 value the verify call receives, so that the oracle
+    and the library cut at the same threshold."""
     k_per_row = np.broadcast_to(np.asarray(k_per_row, dtype=np.int32), (B,)).copy()
     temperature = np.broadcast_to(np.asarray(temperature, dtype=np.float32), (B,)).copy()
     sigma = np.broadcast_to(np.asarray(sigma, dtype=np.float64), (B,)).copy()
@@ -213,7 +215,7 @@ def synth_verify(
 
     return VerifyInputs(name=name, dtype=dtype, B=B, K=K, V=V, target=target,
                         draft=draft, draft_tokens=tokens, k_per_row=k_per_row,
-                        temperature=temperature, top_p=float(top_p),
+                        temperature=temperature, top_p=float(np.float32(top_p)),
                         uniforms=uniforms, mode=mode, sigma=sigma)
 
 
