@@ -6,7 +6,8 @@ workload (B=256 sequences, K=8 with ragged k_b in 2..8, V=128256 bf16 logits,
 per-row temperature in {0.1, 0.7, 1.0} and draft noise in {0.3, 1, 2};
 sampled mode).  Inputs are resident in HBM when timing starts and are
 rotated over three identical copies (3.3 GB > the 129 MB L2) so no step
-reuses data cached by the previous one.
+reuses data cached by the previous one.  ``--workload c1|c3`` times the
+other batch workloads the same way (c3: half greedy, top_p = 0.9).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle on bounded samples of the same workload instead.  Under torchrun each
@@ -31,8 +32,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "verified positions/s and spec_verify HBM GB/s (% of GB300 peak) at 1 GPU"
-WORKLOAD = ("headline verify batch: B=256, K=8, ragged k_b~U{2..8}, V=128256 bf16 logits, "
-            "T_b in {0.1,0.7,1.0}, draft noise in {0.3,1,2}, sampled; + kv_commit")
+WORKLOADS = {
+    "c2": ("headline verify batch: B=256, K=8, ragged k_b~U{2..8}, V=128256 bf16 logits, "
+           "T_b in {0.1,0.7,1.0}, draft noise in {0.3,1,2}, sampled; + kv_commit"),
+    "c1": ("verify batch: B=64, k=5, V=32000 bf16 logits, T=0.8, draft noise 1.0, sampled; "
+           "+ kv_commit"),
+    "c3": ("mixed verify batch: B=128, k=6, V=151936 bf16 logits, T=0.7, top_p=0.9 on both "
+           "sides, rows 0..63 greedy and 64..127 sampled, draft noise 0.5; + kv_commit"),
+}
 COPIES = 3
 
 
@@ -104,35 +111,35 @@ class ClockSampler:
 # CPU oracle leg (bounded sample, spawn pool, sequences regenerated per worker)
 # --------------------------------------------------------------------------
 def _oracle_worker(args):
-    seqs, B = args
+    name, B, seqs = args
     sys.path.insert(0, ROOT)
     import numpy as np
     from oracle import verify as ov
     from speculative_decoding_verification_47_gb300 import workloads as wl
-    k, T, s = wl.c2_row_params(B)
-    V, K = 128256, 8
-    rows = []
-    for b in seqs:
-        t, d, x, u = wl._gen_sequence(b, B, K, V, wl.BF16, int(k[b]), float(T[b]), float(s[b]),
-                                      wl.SAMPLED, (1002, 2002, 2))
-        rows.append((b, t, d, x, u))
+    spec = wl.row_spec(name, B)
+    rows = [(b,) + tuple(spec.sequence(b)) for b in seqs]
     t0 = time.perf_counter()
     pos = 0
     for b, t, d, x, u in rows:
-        ov.verify_sequence(ov._LazyRows(t, "bf16"), ov._LazyRows(d, "bf16"), x, int(k[b]), K, V,
-                           float(T[b]), 1.0, u.astype(np.float64), 0)
-        pos += int(k[b])
+        kb = int(spec.k_per_row[b])
+        ov.verify_sequence(ov._LazyRows(t, spec.dtype), ov._LazyRows(d, spec.dtype), x, kb,
+                           spec.K, spec.V, float(spec.temperature[b]), spec.top_p,
+                           u.astype(np.float64), int(spec.mode[b]))
+        pos += kb
     return pos, time.perf_counter() - t0
 
 
-def cpu_oracle(sample_seqs: int, workers: int):
+def cpu_oracle(name: str, B: int, sample_seqs: int, workers: int):
+    """The oracle on the first ``sample_seqs`` sequences (spread over the
+    batch when it mixes row modes: every (B // sample)-th sequence)."""
     import multiprocessing as mp
-    B = 256
-    seqs = list(range(sample_seqs))
+    sample_seqs = max(1, min(sample_seqs, B))
+    stride = max(1, B // sample_seqs)
+    seqs = list(range(0, B, stride))[:sample_seqs]
     chunks = [seqs[i::workers] for i in range(workers)]
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers) as pool:
-        res = pool.map(_oracle_worker, [(c, B) for c in chunks if c])
+        res = pool.map(_oracle_worker, [(name, B, c) for c in chunks if c])
     pos = sum(r[0] for r in res)
     wall = max(r[1] for r in res)
     return pos, wall, len([c for c in chunks if c])
@@ -171,17 +178,21 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         workers = min(16, len(os.sched_getaffinity(0)))
-        pos, wall, used = cpu_oracle(args.cpu_sample, workers)
+        Bw = args.B or wl.row_spec(args.workload).B
+        pos, wall, used = cpu_oracle(args.workload, Bw, args.cpu_sample, workers)
         cpu = {"value": pos / wall, "unit": "positions/s", "cores": used, "kind": "oracle",
-               "sample": f"first {args.cpu_sample} of the 256 sequences of the same workload, "
-                         f"float64 oracle, {used} spawn workers, wall {wall:.2f} s"}
+               "sample": f"{min(args.cpu_sample, Bw)} of the {Bw} sequences of the same workload "
+                         f"(evenly spaced), float64 oracle, {used} spawn workers, "
+                         f"wall {wall:.2f} s"}
 
-    w = wl.config_c2(B=args.B)
+    w = wl.config_by_name(args.workload, args.B)
     B, K, V = w.B, w.K, w.V
-    es = 2
+    es = 2 if w.dtype == wl.BF16 else 4
+    svdt = sb.SV_BF16 if w.dtype == wl.BF16 else sb.SV_F32
+    top_p = w.top_p
     dev = torch.device("cuda", local)
-    tg = torch.from_numpy(w.target.view(np.int16))
-    dr = torch.from_numpy(w.draft.view(np.int16))
+    tg = torch.from_numpy(w.target.view(np.int16) if es == 2 else w.target)
+    dr = torch.from_numpy(w.draft.view(np.int16) if es == 2 else w.draft)
     tgts = [tg.to(dev) for _ in range(COPIES)]
     drfs = [dr.to(dev) for _ in range(COPIES)]
     tok = torch.from_numpy(w.draft_tokens).to(dev)
@@ -194,12 +205,12 @@ def run_gpu(args):
     cap = torch.full((B,), 2**30, dtype=torch.int32, device=dev)
     out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
     nacc = torch.empty((B,), dtype=torch.int32, device=dev)
-    wsb = sb.sv_workspace_size(B, K, V, sb.SV_BF16)
+    wsb = sb.sv_workspace_size(B, K, V, svdt)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(c):
-        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
+        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
         sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
 
@@ -210,8 +221,12 @@ def run_gpu(args):
     n_host = nacc.cpu().numpy()
     kb = w.k_per_row.astype(np.int64)
     positions = int(kb.sum())
-    rows_needed = int(np.where(n_host < kb, 2 * (n_host + 1), 2 * kb + 1).sum())
-    rows_all = int((2 * kb + 1).sum())
+    greedy = w.mode == wl.GREEDY
+    # rows the rule reads: up to the cut (target + draft on sampled rows,
+    # target only on greedy rows), every row when all drafts are accepted
+    rows_needed = int(np.where(greedy, np.minimum(n_host, kb) + 1,
+                               np.where(n_host < kb, 2 * (n_host + 1), 2 * kb + 1)).sum())
+    rows_all = int(np.where(greedy, kb + 1, 2 * kb + 1).sum())
     small_bytes = B * 4 * (K + 1) * 2 + B * 16  # tokens, uniforms, outputs, per-row knobs
     bytes_needed = rows_needed * V * es + small_bytes
     bytes_all = rows_all * V * es + small_bytes
@@ -230,7 +245,7 @@ def run_gpu(args):
     for it in range(args.steps):
         c = it % COPIES
         ev[it][0].record(stream)
-        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
+        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
         ev[it][1].record(stream)
         sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
@@ -251,8 +266,8 @@ def run_gpu(args):
     # end to end: pinned host inputs -> device, verify + commit, outputs -> host
     e2e = None
     if not args.no_e2e:
-        h_t = torch.from_numpy(w.target.view(np.int16)).pin_memory()
-        h_d = torch.from_numpy(w.draft.view(np.int16)).pin_memory()
+        h_t = tg.pin_memory()
+        h_d = dr.pin_memory()
         h_small = [torch.from_numpy(a).pin_memory() for a in
                    (w.draft_tokens, w.k_per_row, w.temperature, w.uniforms, w.mode, w.seq_lens)]
         d_small = [tok, kpr, tmp, uni, mode, seq]
@@ -266,8 +281,8 @@ def run_gpu(args):
             drfs[0].copy_(h_d, non_blocking=True)
             for d_, h_ in zip(d_small, h_small):
                 d_.copy_(h_, non_blocking=True)
-            sb.sv_spec_verify(tgts[0], 0, 0, drfs[0], 0, 0, sb.SV_BF16, B, K, V, tok, kpr, tmp,
-                              1.0, uni, mode, out, nacc, None, ws, wsb, stream)
+            sb.sv_spec_verify(tgts[0], 0, 0, drfs[0], 0, 0, svdt, B, K, V, tok, kpr, tmp,
+                              top_p, uni, mode, out, nacc, None, ws, wsb, stream)
             sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
             o_out.copy_(out, non_blocking=True)
             o_n.copy_(nacc, non_blocking=True)
@@ -288,7 +303,7 @@ def run_gpu(args):
             t = torch.tensor([ems], device=dev, dtype=torch.float64)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             ems = float(t.item())
-        h2d = (h_t.numel() + h_d.numel()) * 2 + sum(x.numel() * x.element_size() for x in h_small)
+        h2d = (h_t.numel() + h_d.numel()) * es + sum(x.numel() * x.element_size() for x in h_small)
         d2h = (o_out.numel() + o_n.numel() + o_seq.numel()) * 4
         e2e = {"value": positions * world / (ems / steps_e2e * 1e-3), "unit": "positions/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -308,9 +323,10 @@ def run_gpu(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "input_dtype": "bf16",
+        "input_dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "K": K, "V": V,
+        "config": {"workload": WORKLOADS[args.workload], "name": args.workload,
+                   "B": B, "K": K, "V": V, "top_p": top_p,
                    "positions_per_step": positions, "target_rows": int((kb + 1).sum()),
                    "l2": f"{COPIES} rotating input copies ({COPIES * (w.target.nbytes + w.draft.nbytes) / 1e9:.1f} GB) > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
@@ -322,7 +338,7 @@ def run_gpu(args):
                 "frac_of_peak": achieved / peak, "peak_gbs": peak, "peak_source": peak_src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": args.traffic,
-                     "kernel": "verify_kernel<2> (+ its init kernel)",
+                     "kernel": f"verify_kernel<{es},{'true' if top_p < 1 else 'false'}>",
                      "launch_ms": verify_ms, "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -340,12 +356,15 @@ def run_reference(args):
     world, rank, local = dist_setup(args)
     if rank != 0:
         return
+    sys.path.insert(0, ROOT)
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    spec = wl.row_spec(args.workload, args.B)
     workers = min(16, len(os.sched_getaffinity(0)))
     for _ in range(args.warmup):
-        cpu_oracle(workers, workers)  # one sequence per worker
+        cpu_oracle(args.workload, spec.B, workers, workers)  # one sequence per worker
     tot_pos, tot_wall = 0, 0.0
     for _ in range(args.steps):
-        pos, wall, used = cpu_oracle(args.ref_sample, workers)
+        pos, wall, used = cpu_oracle(args.workload, spec.B, args.ref_sample, workers)
         tot_pos += pos
         tot_wall += wall
     value = tot_pos / tot_wall
@@ -363,11 +382,11 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": 256, "K": 8, "V": 128256,
-                   "parallelism": "host cores"},
+        "config": {"workload": WORKLOADS[args.workload], "name": args.workload, "B": spec.B,
+                   "K": spec.K, "V": spec.V, "top_p": spec.top_p, "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": used, "kind": "oracle",
-                         "sample": f"each step: first {args.ref_sample} of the 256 sequences, "
-                                   f"float64 oracle over {used} spawn workers"},
+                         "sample": f"each step: {args.ref_sample} of the {spec.B} sequences "
+                                   f"(evenly spaced), float64 oracle over {used} spawn workers"},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -380,8 +399,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
-    ap.add_argument("--B", type=int, default=256,
-                    help="sequences (256 for the headline batch; smaller only for profiling)")
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS),
+                    help="c2 is the headline batch; c1 and c3 are the other batch workloads")
+    ap.add_argument("--B", type=int, default=None,
+                    help="sequences (the workload's own B by default; smaller only for profiling)")
     ap.add_argument("--cpu-sample", type=int, default=256)
     ap.add_argument("--ref-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -239,6 +239,12 @@ __device__ __forceinline__ uint32_t floor_bits(float v) {
   return ES == 2 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rd(v)) : __float_as_uint(v);
 }
 
+// bit pattern of the smallest representable value >= v
+template <int ES>
+__device__ __forceinline__ uint32_t ceil_bits(float v) {
+  return ES == 2 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_ru(v)) : __float_as_uint(v);
+}
+
 // element j of a 16-byte unit as its bit pattern
 template <int ES>
 __device__ __forceinline__ uint32_t unit_bits(const uint4& v, int j) {
@@ -509,9 +515,11 @@ struct Weight {
   Expo x;
   float Rt, Rd, rho_hi, rho_lo;
   bool p_only;
-  // top-p cuts of the two rows (every token kept: key 0, index INT_MAX)
+  // top-p cuts of the two rows (every token kept: key 0, index INT_MAX);
+  // vkt = value of key kt (-inf without a cut): below it no target token is kept
   uint32_t kt, kd;
   int ct, cd;
+  float vkt;
   // weight of element e with logits (zt, zd) and keys (yt, yd), top-p masks applied
   __device__ __forceinline__ float masked(float zt, float zd, uint32_t yt, uint32_t yd,
                                           int e) const {
@@ -573,6 +581,20 @@ __device__ __forceinline__ float wsum_full(const uint4& vt, const uint4& vd, con
   return e + f;
 }
 
+// Masked weight sum of one full unit (out of line: reached only by the units
+// that hold a kept target token).
+template <int ES>
+__device__ __noinline__ float masked_unit(const Weight& W, uint4 vt, uint4 vd, int eb) {
+  constexpr int EPU = 16 / ES;
+  float acc = 0.f;
+#pragma unroll 1
+  for (int j = 0; j < EPU; ++j) {
+    const uint32_t bt = unit_bits<ES>(vt, j), bd = W.p_only ? 0u : unit_bits<ES>(vd, j);
+    acc += W.masked(bits_val<ES>(bt), bits_val<ES>(bd), okey<ES>(bt), okey<ES>(bd), eb + j);
+  }
+  return acc;
+}
+
 // Rows of the cut position as the finisher reads them (usually from L2: they
 // were streamed moments earlier).  Full units of both rows are read as 16-byte
 // vectors when the rows share their 16-byte phase, else element by element.
@@ -596,13 +618,9 @@ struct PairRead {
     const int eb = st.ebase0 + u * EPU;
     if (full(u)) {
       if (!TOPP) return wsum_full<ES>(vt, W.p_only ? vt : vd, W);
-      float acc = 0.f;
-#pragma unroll
-      for (int j = 0; j < EPU; ++j) {
-        const uint32_t bt = unit_bits<ES>(vt, j), bd = W.p_only ? 0u : unit_bits<ES>(vd, j);
-        acc += W.masked(bits_val<ES>(bt), bits_val<ES>(bd), okey<ES>(bt), okey<ES>(bd), eb + j);
-      }
-      return acc;
+      // no kept target token: max(0, 0 - rho q') = 0 for every element
+      if (unit_max<ES>(vt) < W.vkt) return 0.f;
+      return masked_unit<ES>(W, vt, vd, eb);
     }
     float acc = 0.f;
     for (int j = 0; j < EPU; ++j) {
@@ -621,28 +639,43 @@ struct PairRead {
 };
 
 // ---------------------------------------------------------------------------
-// Top-p selection state of one row.  The cut lies in the key window
-// [lo, hi]; A is the mass of all keys above hi.  A "count" pass (window of
-// at most kNBc keys) histograms exact token counts per key, so a key's mass
-// is count * 2^(z*c - R) with no summation error; a wider window first takes
-// a "mass" pass over kNBm bins of 2^shift keys each, in 64-bit fixed point
-// (integer sums: the same bits whatever the order of the atomic adds).
+// Top-p selection state of one row.  The cut is searched in the key window
+// [lo, hi].  Every pass sums the mass of the tokens above the window exactly
+// (in registers).  A "count" pass (window of at most kNB keys) histograms
+// exact token counts per key, so a key's mass is count * 2^(z*c - R) with no
+// summation error; it settles the cut when the cut lies in the window.  A
+// wider window first
+// takes a "locator" pass: float masses over kNB bins, which only choose the
+// bin that most likely holds the cut (their order of accumulation does not
+// change the result, which comes from exact counts).  Locator bins are
+// uniform in log-probability (z*c - R), so the many tokens of a long tail
+// spread over many bins; when that cannot narrow a window (keys too close in
+// value), bins of 2^shift consecutive keys are used instead.
+// If a pass finds the cut outside its window (a locator misled by rounding),
+// the feasible key range [flo, fhi] shrinks to the side that holds it and
+// the search continues there.
 // ---------------------------------------------------------------------------
-constexpr int kNBc = 2048;
-constexpr int kNBm = 1024;
-constexpr int kHistRowBytes = 8448;  // >= (kNBc + 1) * 4 and kNBm * 8
+constexpr int kNB = 2048;
+constexpr int kSlotLt = kNB;         // count pass: tokens of key kx before the draft token
+constexpr int kSlotAbove = kNB + 2;  // count pass: double-float mass above the window
+constexpr int kHistRowBytes = 8448;  // >= (kNB + 4) * 4
 constexpr int kHistBytes = 2 * kHistRowBytes;
+constexpr int kStageBytes = kThreads * kLoadsInFlight * 16;  // each thread's units in flight
+constexpr int kSelSmemBytes = kHistBytes + kStageBytes;
+constexpr int kMaxSelPasses = 12;
 
 struct TopSel {
-  uint32_t lo, hi;
-  int mode;      // 0 resolved, 1 count pass next, 2 mass pass next
-  int shift;     // mass pass: bin = (key - lo) >> shift
-  float scale;   // mass pass: element mass e * 2^a2 as an integer (exact scaling)
-  float descale; // 2^-a2
-  float R;       // the row's reference exponent
-  DF S, thr;     // row normaliser and top_p * S
-  DF A;          // mass of the keys above the window
-  uint32_t kx;   // key of the draft token's logit in this row
+  uint32_t lo, hi;    // window of the next pass
+  uint32_t flo, fhi;  // keys that may still hold the cut
+  int mode;           // 0 resolved, 1 count pass next, 2 locator pass next
+  int shift;          // locator over key bins: bin = (key - lo) >> shift
+  int vbins;          // locator over value bins: bin = kNB-1 - (int)((tmax - t(z)) * inv)
+  float tmax, inv;    //   with t(z) = z*chi - R
+  float chi;          // log2(e) / T (leading part)
+  float R;            // the row's reference exponent
+  DF S, thr;          // row normaliser and top_p * S
+  DF A;               // mass above hi (exact, summed by the last pass)
+  uint32_t kx;        // key of the draft token's logit in this row
   // result
   uint32_t kstar;  // cut key
   int cstar;       // tokens with the cut key
@@ -656,6 +689,7 @@ struct Shared {
   TopSel ts[2];
   int selbin[2], lowbin[2], sel_cnt[2];
   DF sel_excl[2];
+  DF wab[2][kWarps];
   uint32_t rcnt[kMaxRounds];
   uint32_t ccnt[kCmax];
   int tcut, rrem, xtok;
@@ -718,81 +752,246 @@ __device__ __forceinline__ T* remote(cg::cluster_group& cluster, int C, T* p, in
 // it is at most top_p * S.  The mass ranked before a token is the mass of all
 // larger keys plus that of the equal keys at smaller indices, so the kept set
 // is every key above a cut key k*, and the first nk tokens (index order) of
-// key k*.  The search narrows a key window by histogram passes over the row
-// (re-read from L2), every CTA of the cluster counting its own slice.
+// key k*.  The search narrows a key window by passes over the row (re-read
+// from L2), every CTA of the cluster counting its own slice.
 //
-// Start window: [key(tau0 point), key(max)], where tau0 = (1 - top_p) S / (2V)
+// First window: [key(tau0 point), key(max)], where tau0 = (1 - top_p) S / (2V)
 // in e units.  A token whose e lies below tau0 has, ranked before it, every
 // token above tau0, of mass > S - V tau0 > top_p S: it is never kept.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void sel_set_mode(TopSel& t) {
+template <int ES>
+__device__ __forceinline__ void sel_set_mode(TopSel& t, bool value_bins) {
   const uint32_t span = t.hi - t.lo;
-  if (span < (uint32_t)kNBc) {
+  t.vbins = 0;
+  if (span < (uint32_t)kNB) {
     t.mode = 1;
     t.shift = 0;
   } else {
     t.mode = 2;
-    t.shift = (32 - __clz(span)) - 10;  // (span >> shift) < kNBm
-  }
-}
-
-struct SelRow {
-  uint32_t lo, span, kx, lt;
-  int shift, mode, x;
-  float R, scale;
-  uint32_t* hc;             // count pass: kNBc counts, then the lt slot
-  unsigned long long* hm;   // mass pass: kNBm fixed-point sums
-};
-
-__device__ __forceinline__ SelRow sel_row(const TopSel& t, unsigned char* h, int x, bool active) {
-  SelRow r;
-  r.lo = t.lo;
-  r.span = t.hi - t.lo;
-  r.kx = t.kx;
-  r.lt = 0;
-  r.shift = t.shift;
-  r.mode = active ? t.mode : 0;
-  r.x = x;
-  r.R = t.R;
-  r.scale = t.scale;
-  r.hc = reinterpret_cast<uint32_t*>(h);
-  r.hm = reinterpret_cast<unsigned long long*>(h);
-  return r;
-}
-
-template <int ES>
-__device__ __forceinline__ void sel_elem(SelRow& s, uint32_t bits, int e, const Expo& X) {
-  const uint32_t key = okey<ES>(bits);
-  const uint32_t d = key - s.lo;
-  if (s.mode == 1) {
-    if (d <= s.span) atomicAdd(s.hc + d, 1u);
-    s.lt += (key == s.kx && e < s.x) ? 1u : 0u;
-  } else if (d <= s.span) {
-    atomicAdd(s.hm + (d >> s.shift), __float2ull_rn(e2(bits_val<ES>(bits), X, -s.R) * s.scale));
-  }
-}
-
-template <int ES>
-__device__ __forceinline__ void sel_unit(SelRow& s, const RowSlice<ES>& rs, int u, int ub0, int ub1,
-                                         const uint4& v, const Expo& X) {
-  constexpr int EPU = 16 / ES;
-  const int eb = rs.ebase0 + u * EPU;
-  if (u >= ub0 && u < ub1) {
-#pragma unroll
-    for (int j = 0; j < EPU; ++j) sel_elem<ES>(s, unit_bits<ES>(v, j), eb + j, X);
-  } else if (u < rs.n_units) {
-    for (int j = 0; j < EPU; ++j) {
-      const int e = eb + j;
-      if (e >= rs.e0 && e < rs.e1) sel_elem<ES>(s, rs.bits(e), e, X);
+    t.shift = (32 - __clz(span)) - 11;  // (span >> shift) < kNB
+    if (value_bins) {
+      const float tmax = __fmaf_rn(bits_val<ES>(key_bits<ES>(t.hi)), t.chi, -t.R);
+      const float tmin = __fmaf_rn(bits_val<ES>(key_bits<ES>(t.lo)), t.chi, -t.R);
+      const float inv = __fdiv_rn((float)(kNB - 1), tmax - tmin);
+      if (tmax > tmin && inv > 0.f && inv < INFINITY) {
+        t.vbins = 1;
+        t.tmax = tmax;
+        t.inv = inv;
+      }
     }
   }
 }
 
-// Thread t gathers bins [8t, 8t+8) (count pass) or [4t, 4t+4) (mass pass)
-// of one row's histogram from every CTA of the cluster: integer sums, so
-// every CTA holds the same totals.
+// Pass parameters of one row, in registers.
+struct SelP {
+  uint32_t lo, span, kx;
+  int shift;
+  bool counts, vbins;
+  float R, chi, tmax, inv;
+  float vfloor;  // value of key lo
+  uint32_t floor2;  // bf16: vfloor in both halves
+};
+
+__device__ __forceinline__ SelP sel_params(const TopSel& t, int ES) {
+  SelP p;
+  p.lo = t.lo;
+  p.span = t.hi - t.lo;
+  p.kx = t.kx;
+  p.shift = t.shift;
+  p.counts = t.mode == 1;
+  p.vbins = t.vbins != 0;
+  p.R = t.R;
+  p.chi = t.chi;
+  p.tmax = t.tmax;
+  p.inv = t.inv;
+  p.vfloor = ES == 2 ? bits_val<2>(key_bits<2>(t.lo)) : bits_val<4>(key_bits<4>(t.lo));
+  const uint32_t fb = ES == 2 ? key_bits<2>(t.lo) : 0u;
+  p.floor2 = fb | (fb << 16);
+  return p;
+}
+
+// Mask of the unit's elements whose value is at least the window's floor
+// (bit j = slot j): they are in the window or above it.
+template <int ES>
+__device__ __forceinline__ uint32_t window_mask(const uint4& v, const SelP& p) {
+  if (ES == 2) {
+    const __nv_bfloat162 f = *reinterpret_cast<const __nv_bfloat162*>(&p.floor2);
+    const uint32_t m0 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.x), f);
+    const uint32_t m1 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.y), f);
+    const uint32_t m2 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.z), f);
+    const uint32_t m3 = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.w), f);
+    const uint32_t m = (m0 & 0x10001u) | ((m1 & 0x10001u) << 2) | ((m2 & 0x10001u) << 4) |
+                       ((m3 & 0x10001u) << 6);
+    return (m | (m >> 15)) & 0xffu;
+  } else {
+    return (__uint_as_float(v.x) >= p.vfloor ? 1u : 0u) | (__uint_as_float(v.y) >= p.vfloor ? 2u : 0u) |
+           (__uint_as_float(v.z) >= p.vfloor ? 4u : 0u) | (__uint_as_float(v.w) >= p.vfloor ? 8u : 0u);
+  }
+}
+
+// The unit's elements in `mask` (slot 0 = element eb): add the mass of the
+// ones above the window to *above.  Count pass: count their keys in the
+// window, return how many have the draft token's key at a smaller index.
+// Locator pass: add their masses to the bins.
+template <int ES>
+__device__ __forceinline__ uint32_t sel_bits(const SelP& p, unsigned char* h, const uint4& v, int eb,
+                                             uint32_t mask, int x, const Expo& X, DF* above) {
+  uint32_t* hc = reinterpret_cast<uint32_t*>(h);
+  float* hm = reinterpret_cast<float*>(h);
+  uint32_t lt = 0;
+  while (mask) {
+    const int j = __ffs(mask) - 1;
+    mask &= mask - 1u;
+    const uint32_t bits = unit_bits<ES>(v, j);
+    const uint32_t key = okey<ES>(bits);
+    const uint32_t d = key - p.lo;
+    const float z = bits_val<ES>(bits);
+    if (d > p.span) {
+      if (key > p.lo) df_acc(*above, e2(z, X, -p.R));
+    } else if (p.counts) {
+      atomicAdd(hc + d, 1u);
+    } else {
+      int bin = (int)(d >> p.shift);
+      if (p.vbins)  // bins numbered upward in value, like key bins
+        bin = max(0, kNB - 1 - (int)((p.tmax - __fmaf_rn(z, p.chi, -p.R)) * p.inv));
+      atomicAdd(hm + bin, e2(z, X, -p.R));
+    }
+    if (p.counts) lt += (key == p.kx && eb + j < x) ? 1u : 0u;
+  }
+  return lt;
+}
+
+// A partial unit at a slice end, as a 16-byte unit: the slots of elements in
+// [e0, e1) are set in *valid, the others are zero.
+template <int ES>
+__device__ __forceinline__ uint4 edge_unit(const RowSlice<ES>& rs, int eb, uint32_t* valid) {
+  constexpr int EPU = 16 / ES;
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < EPU; ++j) {
+    const int e = eb + j;
+    if (e < rs.e0 || e >= rs.e1) continue;
+    m |= 1u << j;
+    const uint32_t b = rs.bits(e);
+    if (ES == 4) w[j] = b;
+    else w[j >> 1] |= (j & 1) ? (b << 16) : b;
+  }
+  *valid = m;
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One unit of a selection pass.
+template <int ES>
+__device__ __forceinline__ uint32_t sel_unit(const SelP& p, unsigned char* h, const RowSlice<ES>& rs,
+                                             int u, int ub0, int ub1, const uint4& v, int x,
+                                             const Expo& X, DF* above) {
+  constexpr int EPU = 16 / ES;
+  const int eb = rs.ebase0 + u * EPU;
+  if (u >= ub0 && u < ub1) {
+    const uint32_t mask = window_mask<ES>(v, p);
+    if (mask) return sel_bits<ES>(p, h, v, eb, mask, x, X, above);
+  } else if (u < rs.n_units) {
+    uint32_t valid;
+    const uint4 ve = edge_unit<ES>(rs, eb, &valid);
+    return sel_bits<ES>(p, h, ve, eb, valid, x, X, above);
+  }
+  return 0u;
+}
+
+// One selection pass of this thread's warp over one row slice (out of line:
+// one copy of the code, with registers of its own).  Each thread marks the
+// elements of its units in flight that reach the window; the warp then
+// takes the marked elements of all its lanes 32 at a time (the units are
+// staged in shared memory), so sparse windows keep every lane busy.
+// Returns this thread's lt count and adds its mass above the window to
+// *above.
+template <int ES>
+__device__ __noinline__ uint32_t sel_stream(const TopSel* tp, unsigned char* h, uint4* stage,
+                                            const RowSlice<ES> rs, int x, float chi, float clo,
+                                            DF* above) {
+  constexpr int EPU = 16 / ES;
+  static_assert(kLoadsInFlight * EPU <= 32, "one 32-bit mask for the units in flight");
+  const SelP p = sel_params(*tp, ES);
+  const Expo X{chi, clo};
+  const int lane = threadIdx.x & 31;
+  uint4* mine = stage + threadIdx.x * kLoadsInFlight;
+  const unsigned char* wstage = reinterpret_cast<const unsigned char*>(stage + (threadIdx.x - lane) * kLoadsInFlight);
+  const int NU = rs.n_units, b0 = rs.ub0(), b1 = rs.ub1();
+  uint32_t lt = 0;
+  DF ab = *above;
+  // (every lane runs the same number of steps: the shuffles below need all 32)
+  const int steps = (NU + kThreads * kLoadsInFlight - 1) / (kThreads * kLoadsInFlight);
+  for (int it = 0; it < steps; ++it) {
+    const int u0 = threadIdx.x + it * kThreads * kLoadsInFlight;
+    uint4 v[kLoadsInFlight];
+    uint32_t mall = 0;
+#pragma unroll
+    for (int k = 0; k < kLoadsInFlight; ++k) {
+      const int u = u0 + k * kThreads;
+      if (u >= b0 && u < b1) {
+        v[k] = ldg_unit(rs, u);
+      } else if (u < NU) {  // a partial unit at a slice end
+        uint32_t valid;
+        v[k] = edge_unit<ES>(rs, rs.ebase0 + u * EPU, &valid);
+        mall |= valid << (k * EPU);
+      } else {
+        v[k] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kLoadsInFlight; ++k) {
+      const int u = u0 + k * kThreads;
+      if (u >= b0 && u < b1) mall |= window_mask<ES>(v[k], p) << (k * EPU);
+    }
+    // exclusive prefix of the marked counts over the warp
+    const int c = __popc(mall);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    const int total = __shfl_sync(0xffffffffu, inc, 31);
+    if (total == 0) continue;  // (warp-uniform)
+    const int ex = inc - c;
+    if (mall) {
+#pragma unroll
+      for (int k = 0; k < kLoadsInFlight; ++k) mine[k] = v[k];
+    }
+    __syncwarp();
+    for (int base = 0; base < total; base += 32) {
+      const int q = base + lane;
+      // source lane: the last lane whose prefix is <= q
+      int L = 0;
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1) {
+        const int e_ = __shfl_sync(0xffffffffu, ex, L + step);
+        if (e_ <= q) L += step;
+      }
+      const uint32_t mL = __shfl_sync(0xffffffffu, mall, L);
+      const int exL = __shfl_sync(0xffffffffu, ex, L);
+      if (q < total) {
+        const int bit = (int)__fns(mL, 0u, q - exL + 1);
+        const int k = bit / EPU, j = bit % EPU;
+        const unsigned char* src = wstage + (size_t)L * kLoadsInFlight * 16 + bit * ES;
+        const uint32_t bits = ES == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(src)
+                                      : *reinterpret_cast<const uint32_t*>(src);
+        const int eb = rs.ebase0 + (u0 - lane + L + k * kThreads) * EPU;
+        lt += sel_bits<ES>(p, h, make_uint4(bits, 0u, 0u, 0u), eb + j, 1u, x, X, &ab);
+      }
+    }
+    __syncwarp();  // staged units are read before the next step overwrites them
+  }
+  *above = ab;
+  return lt;
+}
+
+// Thread t gathers bins [8t, 8t+8) of one row's histogram from every CTA of
+// the cluster, in rank order (so every CTA holds the same totals); thread 0
+// also gathers the mass above the window and the count pass's lt count.
 __device__ __forceinline__ void sel_reduce(cg::cluster_group& cluster, int C, unsigned char* h,
-                                           bool counts, uint32_t (&w)[8], uint32_t* lt) {
+                                           bool counts, uint32_t (&w)[8], uint32_t* lt, DF* above) {
   const int tid = threadIdx.x;
   if (counts) {
     uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -804,23 +1003,27 @@ __device__ __forceinline__ void sel_reduce(cg::cluster_group& cluster, int C, un
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) w[k] = a[k];
-    if (tid == 0) {
-      uint32_t l = 0;
-      for (int q = 0; q < C; ++q) l += *remote(cluster, C, reinterpret_cast<uint32_t*>(h) + kNBc, q);
-      *lt = l;
-    }
   } else {
-    unsigned long long m[4] = {0ull, 0ull, 0ull, 0ull};
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int q = 0; q < C; ++q) {
-      const ulonglong2* p = remote(cluster, C, reinterpret_cast<ulonglong2*>(h) + 2 * tid, q);
-      const ulonglong2 x = p[0], y = p[1];
-      m[0] += x.x; m[1] += x.y; m[2] += y.x; m[3] += y.y;
+      const float4* p = remote(cluster, C, reinterpret_cast<float4*>(h) + 2 * tid, q);
+      const float4 x = p[0], y = p[1];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      w[2 * k] = (uint32_t)m[k];
-      w[2 * k + 1] = (uint32_t)(m[k] >> 32);
+    for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(a[k]);
+  }
+  if (tid == 0) {
+    uint32_t l = 0;
+    DF ab{0.f, 0.f};
+    for (int q = 0; q < C; ++q) {
+      uint32_t* r = remote(cluster, C, reinterpret_cast<uint32_t*>(h), q);
+      l += r[kSlotLt];
+      ab = df_add(ab, DF{__uint_as_float(r[kSlotAbove]), __uint_as_float(r[kSlotAbove + 1])});
     }
+    *lt = l;
+    *above = ab;
   }
 }
 
@@ -842,16 +1045,34 @@ __device__ __forceinline__ DF block_suffix_excl(DF v, DF* wtot, int lane, int wa
   return df_add(above, ex);
 }
 
-// After a pass: find the bin holding the cut (mass above it <= top_p S <
-// mass above it plus its own) and narrow the window to it, or, after a count
-// pass, fix the cut key and how many of its tokens are kept.
+// The cut lies under the window (or above it): search the rest of the
+// feasible range on that side.
+template <int ES>
+__device__ __forceinline__ void sel_go_below(TopSel& t) {
+  t.fhi = t.lo - 1u;
+  t.lo = t.flo;
+  t.hi = t.fhi;
+  sel_set_mode<ES>(t, true);
+}
+
+template <int ES>
+__device__ __forceinline__ void sel_go_above(TopSel& t) {
+  t.flo = t.hi + 1u;
+  t.lo = t.flo;
+  t.hi = t.fhi;
+  sel_set_mode<ES>(t, true);
+}
+
+// After a count pass: fix the cut key and how many of its tokens are kept, or
+// move to the side of the window that holds the cut.  After a locator pass:
+// narrow the window to the bin whose (approximate) mass interval holds
+// top_p S; if none does, to the end of the window nearest to it.
 template <int ES>
 __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t lt_tot,
                             const Expo& X) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const TopSel s = sh.ts[r];
   const bool cm = s.mode == 1;
-  const int nb = cm ? 8 : 4;
   DF m[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -862,14 +1083,8 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
         const float e = e2(bits_val<ES>(key_bits<ES>(key)), X, -s.R);
         m[q] = df_mul_f(DF{e, 0.f}, (float)w[q]);
       }
-    } else if (q < 4) {
-      const unsigned long long v =
-          (unsigned long long)w[2 * q] | ((unsigned long long)w[2 * q + 1] << 32);
-      if (v) {
-        const float hi = __ull2float_rn(v);
-        const float lo = __ll2float_rn((long long)(v - __float2ull_rz(hi)));
-        m[q] = DF{hi * s.descale, lo * s.descale};
-      }
+    } else {
+      m[q] = DF{__uint_as_float(w[q]), 0.f};
     }
   }
   DF T = DF{0.f, 0.f};
@@ -880,9 +1095,9 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
   int cand = -1, low = 0x7fffffff;
 #pragma unroll
   for (int q = 7; q >= 0; --q) {
-    if (q < nb && df_pos(m[q])) {
+    if (df_pos(m[q])) {
       const DF inc = df_add(run, m[q]);
-      const int g = nb * tid + q;
+      const int g = 8 * tid + q;
       if (cand < 0 && df_gt(inc, s.thr) && !df_gt(run, s.thr)) cand = g;
       low = g;
       run = inc;
@@ -892,13 +1107,16 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
   if (low != 0x7fffffff) atomicMin(&sh.lowbin[r], low);
   __syncthreads();
   int bs = sh.selbin[r];
-  if (bs < 0) bs = sh.lowbin[r];  // all of the window fits under top_p S (rounding): keep it all
-  if (bs != 0x7fffffff && bs / nb == tid) {
+  const bool above_w = df_gt(s.A, s.thr) && s.hi < s.fhi;  // cut above the window
+  const bool below = cm && bs < 0 && s.lo > s.flo;          // cut under the window
+  if (bs < 0 && !below)  // count pass: nothing below, keep the whole window;
+    bs = sh.lowbin[r];   // locator: its lowest bin (the cut is there or lower)
+  if (bs >= 0 && bs != 0x7fffffff && bs / 8 == tid) {
     DF run2 = above;
 #pragma unroll
     for (int q = 7; q >= 0; --q) {
-      if (q < nb && df_pos(m[q])) {
-        if (nb * tid + q == bs) {
+      if (df_pos(m[q])) {
+        if (8 * tid + q == bs) {
           sh.sel_excl[r] = run2;
           sh.sel_cnt[r] = cm ? (int)w[q] : 0;
         }
@@ -909,7 +1127,13 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
   __syncthreads();
   if (tid == 0) {
     TopSel& t = sh.ts[r];
-    if (bs == 0x7fffffff) {  // no mass in the window (not reachable for a finite row): keep all
+    if (above_w) {
+      // the cut lies above the window (its keys all rank after mass > top_p S)
+      sel_go_above<ES>(t);
+    } else if (below) {
+      sel_go_below<ES>(t);
+    } else if (bs < 0 || bs == 0x7fffffff) {
+      // no mass where the cut should be (not reachable for a finite row)
       t.mode = 0;
       t.kstar = 0u;
       t.cstar = 0;
@@ -926,21 +1150,37 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
       const DF q = df_div(df_sub(t.thr, excl), DF{es, 0.f});
       float f = floorf(q.hi);
       if (f == q.hi && q.lo < 0.f) f -= 1.f;
-      int nk = (f + 1.f >= (float)c) ? c : (f >= 0.f ? (int)f + 1 : 1);
+      const int nk = (f + 1.f >= (float)c) ? c : (f >= 0.f ? (int)f + 1 : 1);
       t.kstar = kk;
       t.cstar = c;
       t.nk = nk;
       t.E = df_add(excl, df_mul_f(DF{es, 0.f}, (float)nk));
       t.lt = (int)lt_tot;
       t.mode = 0;
+    } else if (t.vbins) {
+      // keys of bin bs with half a bin of margin on each side (the bin edges
+      // are recomputed, not stored), one key wider still
+      const float rk = (float)(kNB - 1 - bs);  // bin rank from the top of the window
+      const float z_top = __fdiv_rn(t.tmax - (rk - 0.5f) / t.inv + t.R, t.chi);
+      const float z_bot = __fdiv_rn(t.tmax - (rk + 1.5f) / t.inv + t.R, t.chi);
+      uint32_t nhi = t.hi, nlo = t.lo;
+      if (z_top < bits_val<ES>(key_bits<ES>(t.hi))) nhi = min(t.hi, okey<ES>(ceil_bits<ES>(z_top)) + 1u);
+      if (z_bot > bits_val<ES>(key_bits<ES>(t.lo))) nlo = max(t.lo, okey<ES>(floor_bits<ES>(z_bot)) - 1u);
+      if (nlo > nhi) {
+        nlo = t.lo;
+        nhi = t.hi;
+      }
+      const bool narrowed = (nhi - nlo) < (t.hi - t.lo) / 2u;
+      t.lo = nlo;
+      t.hi = nhi;
+      sel_set_mode<ES>(t, narrowed);
     } else {
       const unsigned long long nlo = (unsigned long long)t.lo + ((unsigned long long)bs << t.shift);
-      unsigned long long nhi = nlo + ((1ull << t.shift) - 1ull);
+      unsigned long long nhi = nlo + (1ull << t.shift) - 1ull;
       if (nhi > (unsigned long long)t.hi) nhi = t.hi;
       t.lo = (uint32_t)nlo;
       t.hi = (uint32_t)nhi;
-      t.A = sh.sel_excl[r];
-      sel_set_mode(t);
+      sel_set_mode<ES>(t, true);
     }
   }
   __syncthreads();
@@ -954,7 +1194,7 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
                                          bool two, const Expo& X, const RowSlice<ES>& st,
                                          const RowSlice<ES>& sd, const RowAcc& row_t,
                                          const RowAcc& row_d) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 2 && (tid == 0 || two)) {
     const int r = tid;
     int x = -1;
@@ -978,12 +1218,10 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     else if (!(z0 > -INFINITY)) lo = 0u;
     else lo = okey<ES>(floor_bits<ES>(z0));
     t.lo = min(lo, t.hi);
-    sel_set_mode(t);
-    // fixed point for mass passes: S * 2^a2 < 2^61
-    const int eS = ((__float_as_int(row.s.hi) >> 23) & 0xff) - 127;
-    const int a2 = 60 - eS;
-    t.scale = __int_as_float((127 + a2) << 23);
-    t.descale = __int_as_float((127 - a2) << 23);
+    t.flo = t.lo;
+    t.fhi = t.hi;
+    t.chi = X.chi;
+    sel_set_mode<ES>(t, true);
     t.kx = x >= 0 ? okey<ES>(rs.bits(x)) : 0u;
     t.kstar = 0u;
     t.cstar = 0;
@@ -993,7 +1231,7 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     sh.ts[r] = t;
   }
   __syncthreads();
-  for (int pass = 0; pass < 5; ++pass) {
+  for (int pass = 0; pass < kMaxSelPasses; ++pass) {
     const bool a0 = sh.ts[0].mode != 0, a1 = two && sh.ts[1].mode != 0;
     if (!a0 && !a1) break;
     for (int k = tid; k < kHistBytes / 16; k += kThreads)
@@ -1003,33 +1241,40 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
       sh.lowbin[0] = sh.lowbin[1] = 0x7fffffff;
     }
     __syncthreads();
-    SelRow r0 = sel_row(sh.ts[0], hist, sh.xtok, a0);
-    SelRow r1 = sel_row(sh.ts[1], hist + kHistRowBytes, sh.xtok, a1);
-    {
-      const int NU = two ? max(st.n_units, sd.n_units) : st.n_units;
-      const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-      for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight) {
-        uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
-#pragma unroll
-        for (int k = 0; k < kLoadsInFlight; ++k) {
-          const int u = u0 + k * kThreads;
-          vt[k] = (a0 && u >= tb0 && u < tb1) ? ldg_unit(st, u) : make_uint4(0, 0, 0, 0);
-          vd[k] = (a1 && u >= db0 && u < db1) ? ldg_unit(sd, u) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < kLoadsInFlight; ++k) {
-          const int u = u0 + k * kThreads;
-          if (a0) sel_unit<ES>(r0, st, u, tb0, tb1, vt[k], X);
-          if (a1) sel_unit<ES>(r1, sd, u, db0, db1, vd[k], X);
-        }
-      }
+    const int x = sh.xtok;
+    const bool c0 = a0 && sh.ts[0].mode == 1, c1 = a1 && sh.ts[1].mode == 1;
+    uint32_t l0 = 0, l1 = 0;
+    DF ab0{0.f, 0.f}, ab1{0.f, 0.f};
+    unsigned char* h1 = hist + kHistRowBytes;
+    uint4* stage = reinterpret_cast<uint4*>(hist + kHistBytes);
+    if (a0) l0 = sel_stream<ES>(&sh.ts[0], hist, stage, st, x, X.chi, X.clo, &ab0);
+    if (a1) l1 = sel_stream<ES>(&sh.ts[1], h1, stage, sd, x, X.chi, X.clo, &ab1);
+    // the CTA's lt count (count passes) and mass above the window (fixed order)
+    if (c0 && l0) atomicAdd(reinterpret_cast<uint32_t*>(hist) + kSlotLt, l0);
+    if (c1 && l1) atomicAdd(reinterpret_cast<uint32_t*>(h1) + kSlotLt, l1);
+    ab0 = df_warp_sum(ab0);
+    ab1 = df_warp_sum(ab1);
+    if (lane == 0) {
+      sh.wab[0][warp] = ab0;
+      sh.wab[1][warp] = ab1;
     }
-    if (r0.mode == 1 && r0.lt) atomicAdd(r0.hc + kNBc, r0.lt);
-    if (r1.mode == 1 && r1.lt) atomicAdd(r1.hc + kNBc, r1.lt);
+    __syncthreads();
+    if (tid < 2 && (tid == 0 ? a0 : a1)) {
+      DF a{0.f, 0.f};
+      for (int q = 0; q < kWarps; ++q) a = df_add(a, sh.wab[tid][q]);
+      uint32_t* hc = reinterpret_cast<uint32_t*>(tid ? h1 : hist);
+      hc[kSlotAbove] = __float_as_uint(a.hi);
+      hc[kSlotAbove + 1] = __float_as_uint(a.lo);
+    }
     csync(cluster, C);  // every CTA's histograms are complete
     uint32_t w0[8], w1[8], lt0 = 0, lt1 = 0;
-    if (a0) sel_reduce(cluster, C, hist, r0.mode == 1, w0, &lt0);
-    if (a1) sel_reduce(cluster, C, hist + kHistRowBytes, r1.mode == 1, w1, &lt1);
+    DF A0{0.f, 0.f}, A1{0.f, 0.f};
+    if (a0) sel_reduce(cluster, C, hist, c0, w0, &lt0, &A0);
+    if (a1) sel_reduce(cluster, C, h1, c1, w1, &lt1, &A1);
+    if (tid == 0) {  // exact mass above each window
+      if (a0) sh.ts[0].A = A0;
+      if (a1) sh.ts[1].A = A1;
+    }
     csync(cluster, C);  // every CTA has read every histogram
     if (a0) sel_resolve<ES>(sh, 0, w0, lt0, X);
     if (a1) sel_resolve<ES>(sh, 1, w1, lt1, X);
@@ -1047,12 +1292,15 @@ __device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group&
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NU = rs.n_units, rounds = (NU + kThreads - 1) / kThreads;
   const int ub0 = rs.ub0(), ub1 = rs.ub1();
+  const float vk = bits_val<ES>(key_bits<ES>(kk));  // units entirely below it hold no token of key kk
   for (int u = tid; u < rounds * kThreads; u += kThreads) {
     uint32_t c = 0;
     if (u >= ub0 && u < ub1) {
       const uint4 v = ldg_unit(rs, u);
+      if (unit_max<ES>(v) >= vk) {
 #pragma unroll
-      for (int j = 0; j < EPU; ++j) c += okey<ES>(unit_bits<ES>(v, j)) == kk ? 1u : 0u;
+        for (int j = 0; j < EPU; ++j) c += okey<ES>(unit_bits<ES>(v, j)) == kk ? 1u : 0u;
+      }
     } else if (u < NU) {
       const int eb = rs.ebase0 + u * EPU;
       for (int j = 0; j < EPU; ++j) {
@@ -1160,9 +1408,11 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   }
   W.kt = W.kd = 0u;
   W.ct = W.cd = 0x7fffffff;
+  W.vkt = -INFINITY;
   if (TOPP) {  // (S_t, S_d are the kept masses here)
     uint32_t* iv = reinterpret_cast<uint32_t*>(vals);
     W.kt = kt;
+    if (kt != 0u) W.vkt = bits_val<ES>(key_bits<ES>(kt));
     if (nkt < cntt) W.ct = tie_cut<ES>(sh, iv, cluster, C, rank, pr.st, kt, nkt);
     if (!bonus) {
       W.kd = kd;
@@ -1738,7 +1988,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   }
   const bool topp = L.top_p < 1.0f;
   size_t smem = (size_t)rounds * kThreads * sizeof(float);
-  if (topp && smem < (size_t)kHistBytes) smem = kHistBytes;
+  if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   if (!g_configured[gi]) {

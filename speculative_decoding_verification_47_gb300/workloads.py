@@ -249,6 +249,56 @@ def config_c0_batched(rounds: int = 64, V: int = 32000) -> VerifyInputs:
                         seeds=(1000, 2000, 0))
 
 
+@dataclass
+class RowSpec:
+    """Everything needed to regenerate any single sequence of a named batch
+    workload with ``_gen_sequence`` (per-sequence random streams)."""
+
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    k_per_row: np.ndarray
+    temperature: np.ndarray
+    sigma: np.ndarray
+    mode: np.ndarray
+    top_p: float
+    seeds: tuple
+
+    def sequence(self, b: int):
+        return _gen_sequence(b, self.B, self.K, self.V, self.dtype, int(self.k_per_row[b]),
+                             float(self.temperature[b]), float(self.sigma[b]),
+                             int(self.mode[b]), self.seeds)
+
+
+def row_spec(name: str, B: int | None = None) -> RowSpec:
+    """Row parameters of the batch workloads c1, c2, c3."""
+    def full(v, n, dt):
+        return np.broadcast_to(np.asarray(v, dtype=dt), (n,)).copy()
+
+    if name == "c1":
+        B = B or 64
+        return RowSpec("c1", B, 5, 32000, BF16, full(5, B, np.int32), full(0.8, B, np.float32),
+                       full(1.0, B, np.float64), full(SAMPLED, B, np.uint8), 1.0,
+                       (1001, 2001, 1))
+    if name == "c2":
+        B = B or 256
+        k, T, sg = c2_row_params(B)
+        return RowSpec("c2", B, 8, 128256, BF16, k, T, sg, full(SAMPLED, B, np.uint8), 1.0,
+                       (1002, 2002, 2))
+    if name == "c3":
+        B = B or 128
+        mode = np.where(np.arange(B) < B // 2, GREEDY, SAMPLED).astype(np.uint8)
+        return RowSpec("c3", B, 6, 151936, BF16, full(6, B, np.int32), full(0.7, B, np.float32),
+                       full(0.5, B, np.float64), mode, float(np.float32(0.9)), (1003, 2003, 3))
+    raise ValueError(f"no row spec for workload {name!r}")
+
+
+def config_by_name(name: str, B: int | None = None) -> VerifyInputs:
+    return {"c1": config_c1, "c2": config_c2, "c3": config_c3}[name](**({"B": B} if B else {}))
+
+
 def config_c1(B: int = 64, V: int = 32000) -> VerifyInputs:
     """B=64, k=5, V=32000, bf16, draft noise 1.0, T=0.8, sampled; seq_lens
     ~U[128, 4096] for the KV write-pointer commit."""

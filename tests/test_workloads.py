@@ -59,3 +59,20 @@ def test_c2_row_params():
     assert k.min() >= 2 and k.max() <= 8
     assert set(np.unique(T).tolist()) <= {np.float32(0.1), np.float32(0.7), np.float32(1.0)}
     assert set(np.unique(s).tolist()) <= {0.3, 1.0, 2.0}
+
+
+def test_row_spec_regenerates_the_batch_sequences():
+    """bench.py's CPU legs regenerate single sequences from the row spec; they
+    must be the sequences of the batch workload."""
+    for name, B in (("c1", 5), ("c2", 6), ("c3", 4)):
+        spec = wl.row_spec(name, B)
+        w = wl.config_by_name(name, B)
+        assert (spec.B, spec.K, spec.V, spec.dtype, spec.top_p) == (w.B, w.K, w.V, w.dtype, w.top_p)
+        np.testing.assert_array_equal(spec.mode, w.mode)
+        np.testing.assert_array_equal(spec.k_per_row, w.k_per_row)
+        for b in (0, B - 1):
+            t, d, x, u = spec.sequence(b)
+            np.testing.assert_array_equal(t, w.target[b])
+            np.testing.assert_array_equal(d, w.draft[b])
+            np.testing.assert_array_equal(x, w.draft_tokens[b])
+            np.testing.assert_array_equal(u, w.uniforms[b])
