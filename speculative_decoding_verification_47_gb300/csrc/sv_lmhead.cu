@@ -9,16 +9,17 @@
 // Two kernels on the caller's stream:
 //  1. rmsnorm_kernel: one CTA per row writes the normalised, weighted bf16
 //     row y into the workspace (4 MB at M=512, H=4096: L2-resident for 2.).
-//  2. lmhead_gemm_kernel: one CTA per 128 x 256 output tile on the 5th-
-//     generation tensor cores.  A 4-stage ring in shared memory is filled by
-//     the TMA engine (cp.async.bulk.tensor, 128-byte swizzle): y tiles
-//     K-major (128 rows x 64 k), W tiles N-major (64 k x 64 n, four per
-//     stage).  One thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
-//     fp32 accumulator in tensor memory) and tcgen05.commit frees each stage
-//     once its MMAs are done; the four warps then read the accumulator back
-//     with tcgen05.ld and store bf16 (or fp32) logits.  Tiles are numbered
-//     M-fastest, so the four row tiles that share a W column block run side
-//     by side and W streams from HBM about once.
+//  2. lmhead_gemm_kernel: persistent, one CTA per SM, 128 x BN output tiles
+//     on the 5th-generation tensor cores (BN in 128..256, chosen per shape for
+//     the fewest waves).  A 4-stage ring in shared memory is filled by the TMA
+//     engine (cp.async.bulk.tensor, 128-byte swizzle): y tiles K-major (128
+//     rows x 64 k), W tiles N-major (64 k x 64 n, up to four per stage).  One
+//     thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32 accumulator
+//     in tensor memory) and tcgen05.commit frees each stage once its MMAs are
+//     done; two accumulators let four epilogue warps read one tile back
+//     (tcgen05.ld) and store bf16 (or fp32) logits while the next tile
+//     accumulates.  Tiles are numbered M-fastest, so the row tiles that share
+//     a W column block run side by side and W streams from HBM about once.
 #include <cuda.h>  // CUtensorMap and the encoder's signature (resolved at run time)
 
 #include <cstdint>
@@ -34,13 +35,12 @@ namespace lmh {
 
 constexpr int BM = 128, BN = 256, BK = 64;        // BK: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
+constexpr int kPrefetch = 8;  // k blocks of W pulled into L2 ahead of the ring
 constexpr int kABytes = BM * BK * 2;                // 16 KB
 constexpr int kBAtomBytes = BK * 64 * 2;            // 8 KB: BK rows x 64 columns of W
 constexpr int kBBytes = (BN / 64) * kBAtomBytes;    // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;      // 48 KB
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + slack to align to 1 KB
-constexpr int kThreads = 128;                       // one warpgroup: the 128 TMEM lanes
-constexpr uint32_t kTmemCols = BN;                  // fp32 accumulator columns
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5
 // = 1), A and B bf16 (bits 7-9 and 10-12 = 1), A K-major (bit 15 = 0), B
@@ -66,6 +66,26 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same box delivered to every CTA of the cluster in `mask` (same smem
+// offset, same mbarrier offset in each)
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+// Pull a box into L2 ahead of its shared-memory load (hides HBM latency that
+// the shared-memory ring alone is too short to cover).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -86,6 +106,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_addr(bar))
                : "memory");
+}
+
+// ... arriving at the barrier of the same offset in every CTA of `mask`
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes
@@ -154,19 +183,40 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint16_t* _
 }
 
 // ---------------------------------------------------------------------------
-// 2. The tcgen05 GEMM.
+// 2. The tcgen05 GEMM: persistent CTAs (one per SM) in clusters of CM along
+//    M.  The CTAs of a cluster compute the CM row tiles of one column block
+//    together: each loads its own y tile and 1/CM of the W tiles, which the
+//    TMA engine multicasts to every CTA of the cluster, so W crosses the L2
+//    interface once per cluster instead of once per CTA.  A stage may be
+//    refilled once every CTA's MMAs have released it (tcgen05.commit
+//    multicast to the stage's barrier in each CTA).  Warp 0 streams operand
+//    tiles, warp 1 issues the MMAs into one of two TMEM accumulators (512
+//    columns: tile i uses half i & 1), warps 2-5 drain the other accumulator
+//    to global memory while the next tile accumulates.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1)
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemAlloc = 512;
+
+template <int BNT, int CM>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        void* __restrict__ out, int out_f32, int M, int N, int K, uint32_t* flags) {
+  static_assert(BNT % 16 == 0 && BNT >= 64 && BNT <= 256, "MMA N");
+  static_assert(CM == 1 || CM == 2 || CM == 4, "cluster size");
+  constexpr int kAtoms = (BNT + 63) / 64;  // W tiles of 64 columns per stage
+  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
+  constexpr uint32_t kTx = (uint32_t)(kABytes + kAtoms * kBAtomBytes);
+  constexpr uint32_t kIdescT = (kIdesc & ~(0x3Fu << 17)) | ((uint32_t)(BNT >> 3) << 17);
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], accf[2], acce[2];
   __shared__ uint32_t tmem_base;
   __shared__ int issued, consumed, failed;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = (M + BM - 1) / BM;
-  const int m0 = (blockIdx.x % mt) * BM, n0 = (blockIdx.x / mt) * BN;
+  const int mt = (M + BM - 1) / BM, nt = (N + BNT - 1) / BNT;
+  const int mg = (mt + CM - 1) / CM;      // row groups of CM tiles
+  const int tiles = mg * nt;              // cluster tiles
+  const int rank = (int)(blockIdx.x % CM), cid = (int)(blockIdx.x / CM), ncl = (int)(gridDim.x / CM);
   const int KB = K / BK;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -174,120 +224,185 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CM);  // released by the MMAs of every CTA of the cluster
     }
-    mbar_init(&done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+    }
     issued = consumed = failed = 0;
     fence_mbar_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
-  if (warp == 0) {  // the whole warp allocates the accumulator's TMEM columns
+  if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_base)),
-                 "r"(kTmemCols)
+                 "r"(kTmemAlloc)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  if (CM > 1) cg::this_cluster().sync();  // every CTA's barriers exist before any multicast
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 0 && lane == 0) {
-    // ---- TMA producer ----
-    int kb = 0;
-    for (; kb < KB; ++kb) {
-      const int s = kb % kStages, use = kb / kStages;
-      if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) {
-        atomicOr(flags, SV_FLAG_TIMEOUT);
-        failed = 1;
-        break;
-      }
-      uint8_t* a = smem + s * kStageBytes;
-      uint8_t* b = a + kABytes;
-      mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
-      tma_load_2d(a, &tmA, kb * BK, m0, &full[s]);
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer: one stage counter across all tiles ----
+      int g = 0;
+      bool ok = true;
+      for (int t = cid; t < tiles && ok; t += ncl) {
+        const int m0 = ((t % mg) * CM + rank) * BM, n0 = (t / mg) * BNT;
+        // this CTA's share of the W boxes of the first k blocks, into L2
+        for (int kb = 0; kb < kPrefetch && kb < KB; ++kb)
 #pragma unroll
-      for (int j = 0; j < BN / 64; ++j) tma_load_2d(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s]);
-    }
-    issued = kb;
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ----
-    int kb = 0;
-    for (; kb < KB; ++kb) {
-      const int s = kb % kStages, use = kb / kStages;
-      if (!mbar_wait_bounded(&full[s], (uint32_t)(use & 1))) {
+          for (int j = 0; j < kAtoms; ++j)
+            if (j % CM == rank) tma_prefetch_2d(&tmB, n0 + 64 * j, kb * BK);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          if (kb + kPrefetch < KB) {
+#pragma unroll
+            for (int j = 0; j < kAtoms; ++j)
+              if (j % CM == rank) tma_prefetch_2d(&tmB, n0 + 64 * j, (kb + kPrefetch) * BK);
+          }
+          const int s = g % kStages, use = g / kStages;
+          if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + s * kStageBytes;
+          uint8_t* b = a + kABytes;
+          mbar_arrive_expect_tx(&full[s], kTx);
+          tma_load_2d(a, &tmA, kb * BK, m0, &full[s]);
+#pragma unroll
+          for (int j = 0; j < kAtoms; ++j) {
+            if (CM == 1) tma_load_2d(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s]);
+            else if (j % CM == rank)
+              tma_load_2d_mc(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s], kMask);
+          }
+        }
+      }
+      issued = g;
+      // wait until every stage has been released by all the cluster's MMAs:
+      // no arrival from another CTA is then still on its way to this one
+      for (int i = 0; i < kStages && ok; ++i) {
+        const int gg = g + i, s = gg % kStages, use = gg / kStages;
+        if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) ok = false;
+      }
+      if (!ok) {
         atomicOr(flags, SV_FLAG_TIMEOUT);
         failed = 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer ----
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = cid; t < tiles && ok; t += ncl, ++i) {
+        const int b = i & 1, ub = i >> 1;
+        if (ub > 0 && !mbar_wait_bounded(&acce[b], (uint32_t)((ub - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * 256);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % kStages, use = g / kStages;
+          if (!mbar_wait_bounded(&full[s], (uint32_t)(use & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_addr(smem + s * kStageBytes);
+          const uint32_t bb = a + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = desc_sw128(a + 32u * kk, 16u, 1024u);
+            const uint64_t bd = desc_sw128(bb + 2048u * kk, (uint32_t)kBAtomBytes, 1024u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+                "l"(ad), "l"(bd), "r"(kIdescT), "r"(acc)
+                : "memory");
+          }
+          if (CM == 1) tc_commit(&empty[s]);
+          else tc_commit_mc(&empty[s], kMask);
+        }
+        if (!ok) break;
+        tc_commit(&accf[b]);  // accumulator b complete
+      }
+      consumed = g;
+      if (!ok) {
+        atomicOr(flags, SV_FLAG_TIMEOUT);
+        failed = 1;
+      }
+    }
+  } else {
+    // ---- epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31 ----
+    const int lg = warp & 3;
+    int i = 0;
+    for (int t = cid; t < tiles; t += ncl, ++i) {
+      const int b = i & 1, ub = i >> 1;
+      const bool ok = mbar_wait_bounded(&accf[b], (uint32_t)(ub & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) atomicOr(flags, SV_FLAG_TIMEOUT);
         break;
       }
       tc_fence_after();
-      const uint32_t a = smem_addr(smem + s * kStageBytes);
-      const uint32_t b = a + kABytes;
+      const int m0 = ((t % mg) * CM + rank) * BM, n0 = (t / mg) * BNT;
+      const int row = m0 + lg * 32 + lane;
+      const uint32_t tbase = tmem + (uint32_t)(b * 256) + ((uint32_t)(lg * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BNT; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)c, v);
+        const int n = n0 + c;
+        if (row >= M || n >= N) continue;
+        if (out_f32) {
+          float* o = static_cast<float*>(out) + (size_t)row * N + n;
+          if (n + 32 <= N) {
 #pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        // A: next 16 k = 32 bytes along the swizzled row; B: next 16 k rows
-        // = two 8-row groups of 1 KB; B's 64-column atoms are kBAtomBytes apart
-        tc_mma(tmem, desc_sw128(a + 32u * kk, 16u, 1024u),
-               desc_sw128(b + 2048u * kk, (uint32_t)kBAtomBytes, 1024u), (kb | kk) != 0 ? 1u : 0u);
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<uint4*>(o)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (q < N - n) o[q] = __uint_as_float(v[q]);
+          }
+        } else {
+          uint16_t* o = static_cast<uint16_t*>(out) + (size_t)row * N + n;
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+          if (n + 32 <= N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4*>(o)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (q < N - n) o[q] = (uint16_t)((q & 1) ? (pk[q >> 1] >> 16) : (pk[q >> 1] & 0xffffu));
+          }
+        }
       }
-      tc_commit(&empty[s]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);  // accumulator b may be overwritten
     }
-    consumed = kb;
-    tc_commit(&done);  // arrives when every MMA issued above has completed
   }
   __syncwarp();
-
-  // ---- epilogue: TMEM -> registers -> global ----
-  const bool ok = mbar_wait_bounded(&done, 0u);
-  if (!ok && lane == 0) atomicOr(flags, SV_FLAG_TIMEOUT);
-  tc_fence_after();
-  const int row = m0 + warp * 32 + lane;
-  if (__all_sync(0xffffffffu, ok)) {
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-      const int n = n0 + c;
-      if (row >= M || n >= N) continue;
-      if (out_f32) {
-        float* o = static_cast<float*>(out) + (size_t)row * N + n;
-        if (n + 32 <= N) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4*>(o)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (q < N - n) o[q] = __uint_as_float(v[q]);
-        }
-      } else {
-        uint16_t* o = static_cast<uint16_t*>(out) + (size_t)row * N + n;
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-        if (n + 32 <= N) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<uint4*>(o)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (q < N - n) o[q] = (uint16_t)((q & 1) ? (pk[q >> 1] >> 16) : (pk[q >> 1] & 0xffffu));
-        }
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && failed) {
     // a wait ran out: let the copies already issued land before the CTA exits
-    for (int kb = consumed; kb < issued; ++kb)
-      (void)mbar_wait_bounded(&full[kb % kStages], (uint32_t)((kb / kStages) & 1), 64);
+    for (int g = consumed; g < issued; ++g)
+      (void)mbar_wait_bounded(&full[g % kStages], (uint32_t)((g / kStages) & 1), 64);
   }
-  __syncthreads();
+  if (CM > 1) cg::this_cluster().sync();  // no CTA leaves while another may still write to it
+  else __syncthreads();
   if (warp == 0) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemAlloc)
                  : "memory");
   }
 }
@@ -302,7 +417,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 static std::mutex g_mutex;
 static EncodeTiledFn g_encode = nullptr;
-static int g_configured = 0;
+
+static int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  }
+  return n;
+}
 
 static EncodeTiledFn encoder(std::string* err) {
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -339,6 +464,90 @@ static bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, uint
   return true;
 }
 
+struct GemmArgs {
+  CUtensorMap a, b;
+  void* out;
+  int out_f32, M, N, K;
+  uint32_t* flags;
+};
+
+static void cluster_cfg(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int cm,
+                        cudaStream_t st) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3((unsigned)grid, 1, 1);
+  cfg->blockDim = dim3(kGemmThreads, 1, 1);
+  cfg->dynamicSmemBytes = kSmemBytes;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cm;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+// Clusters of CM that can be resident at once (the grid of the persistent
+// kernel); 0 if the query fails.
+template <int BNT, int CM>
+static int active_clusters() {
+  static int n = -1;
+  if (n < 0) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    cluster_cfg(&cfg, attr, CM * 64, CM, nullptr);
+    int c = 0;
+    if (cudaFuncSetAttribute(lmhead_gemm_kernel<BNT, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, lmhead_gemm_kernel<BNT, CM>, &cfg) != cudaSuccess)
+      c = 0;
+    n = c;
+  }
+  return n;
+}
+
+template <int BNT, int CM>
+static cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int* grid_out) {
+  const int mt = (g.M + BM - 1) / BM;
+  const int tiles = ((mt + CM - 1) / CM) * ((g.N + BNT - 1) / BNT);
+  int act = active_clusters<BNT, CM>();
+  if (act <= 0) act = num_sms() / CM;
+  const int clusters = tiles < act ? tiles : act;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cluster_cfg(&cfg, attr, clusters * CM, CM, st);
+  *grid_out = clusters * CM;
+  return cudaLaunchKernelEx(&cfg, lmhead_gemm_kernel<BNT, CM>, g.a, g.b, g.out, g.out_f32, g.M, g.N, g.K,
+                            g.flags);
+}
+
+template <int CM>
+static cudaError_t launch_cm(const GemmArgs& g, cudaStream_t st, int* grid_out) {
+  // tile width: the fewest rounds of cluster tiles over the resident
+  // clusters, weighted by the width (columns one CTA computes), then the widest
+  const int mt = (g.M + BM - 1) / BM, mg = (mt + CM - 1) / CM;
+  const int widths[5] = {256, 224, 192, 160, 128};
+  const int acts[5] = {active_clusters<256, CM>(), active_clusters<224, CM>(), active_clusters<192, CM>(),
+                       active_clusters<160, CM>(), active_clusters<128, CM>()};
+  int best = 0;
+  long long best_cost = -1;
+  for (int i = 0; i < 5; ++i) {
+    const long long act = acts[i] > 0 ? acts[i] : num_sms() / CM;
+    const long long tiles = (long long)mg * ((g.N + widths[i] - 1) / widths[i]);
+    const long long cost = ((tiles + act - 1) / act) * widths[i];
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = i;
+    }
+  }
+  switch (widths[best]) {
+    case 224: return launch_gemm<224, CM>(g, st, grid_out);
+    case 192: return launch_gemm<192, CM>(g, st, grid_out);
+    case 160: return launch_gemm<160, CM>(g, st, grid_out);
+    case 128: return launch_gemm<128, CM>(g, st, grid_out);
+    default: return launch_gemm<256, CM>(g, st, grid_out);
+  }
+}
+
 }  // namespace lmh
 
 size_t lmhead_workspace_bytes(int M, int H) { return 256 + (size_t)M * H * 2 + 256; }
@@ -352,22 +561,16 @@ int lmhead_launch(const void* hidden, const void* norm_w, float eps, const void*
   if (!enc) return SV_ERR_CUDA;
   uint32_t* flags = static_cast<uint32_t*>(workspace);
   uint16_t* y = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 256);
-  CUtensorMap tmA, tmB;
-  if (!make_map(enc, &tmA, y, (uint64_t)H, (uint64_t)M, (uint64_t)H * 2, BK, BM, err)) return SV_ERR_CUDA;
-  if (!make_map(enc, &tmB, W, (uint64_t)V, (uint64_t)H, (uint64_t)V * 2, 64, BK, err)) return SV_ERR_CUDA;
+  GemmArgs g;
+  if (!make_map(enc, &g.a, y, (uint64_t)H, (uint64_t)M, (uint64_t)H * 2, BK, BM, err)) return SV_ERR_CUDA;
+  if (!make_map(enc, &g.b, W, (uint64_t)V, (uint64_t)H, (uint64_t)V * 2, 64, BK, err)) return SV_ERR_CUDA;
+  g.out = logits;
+  g.out_f32 = out_dtype == SV_F32 ? 1 : 0;
+  g.M = M;
+  g.N = V;
+  g.K = H;
+  g.flags = flags;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_configured) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-      if (e != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
-        return SV_ERR_CUDA;
-      }
-      g_configured = 1;
-    }
-  }
   rmsnorm_kernel<<<M, kNormThreads, 0, st>>>(static_cast<const uint16_t*>(hidden),
                                              static_cast<const uint16_t*>(norm_w), eps, y, H, flags);
   cudaError_t e = cudaGetLastError();
@@ -375,10 +578,15 @@ int lmhead_launch(const void* hidden, const void* norm_w, float eps, const void*
     *err = std::string("rmsnorm launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((V + BN - 1) / BN);
-  lmhead_gemm_kernel<<<tiles, kThreads, kSmemBytes, st>>>(tmA, tmB, logits, out_dtype == SV_F32 ? 1 : 0,
-                                                          M, V, H, flags);
-  e = cudaGetLastError();
+  // cluster of CM row tiles sharing the W tiles (CM divides the row tiles)
+  const int mt = (M + BM - 1) / BM;
+  int grid = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);  // one-time attribute setup inside
+    if (mt % 4 == 0) e = launch_cm<4>(g, st, &grid);
+    else if (mt % 2 == 0) e = launch_cm<2>(g, st, &grid);
+    else e = launch_cm<1>(g, st, &grid);
+  }
   if (e != cudaSuccess) {
     *err = std::string("lmhead launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
