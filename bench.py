@@ -7,7 +7,9 @@ per-row temperature in {0.1, 0.7, 1.0} and draft noise in {0.3, 1, 2};
 sampled mode).  Inputs are resident in HBM when timing starts and are
 rotated over three identical copies (3.3 GB > the 129 MB L2) so no step
 reuses data cached by the previous one.  ``--workload c1|c3`` times the
-other batch workloads the same way (c3: half greedy, top_p = 0.9).
+other batch workloads the same way (c3: half greedy, top_p = 0.9);
+``--workload c4`` times the layer-skip step: draft and target logits from
+hidden states through sv_lmhead_rmsnorm (tcgen05 GEMM), then verify + commit.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle on bounded samples of the same workload instead.  Under torchrun each
@@ -39,6 +41,9 @@ WORKLOADS = {
            "+ kv_commit"),
     "c3": ("mixed verify batch: B=128, k=6, V=151936 bf16 logits, T=0.7, top_p=0.9 on both "
            "sides, rows 0..63 greedy and 64..127 sampled, draft noise 0.5; + kv_commit"),
+    "c4": ("layer-skip step: hidden [512,4096] bf16 -> final RMSNorm (eps 1e-5) -> LM head "
+           "W[4096,32000] bf16 for the draft and the target logits, then verify B=64, k=7, "
+           "T=1, sampled; + kv_commit"),
 }
 COPIES = 3
 
@@ -148,6 +153,20 @@ def cpu_oracle(name: str, B: int, sample_seqs: int, workers: int):
 # --------------------------------------------------------------------------
 # GPU arm
 # --------------------------------------------------------------------------
+def reduce_timing(ms: float, positions: int, pg=None, device=None):
+    """Whole-job timing over the ranks of a replica run: the slowest rank's
+    elapsed time and the positions all ranks verified (each rank runs its own
+    batch; there is no collective on the data path)."""
+    if pg is None:
+        return ms, positions
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    n = torch.tensor([positions], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    pg.all_reduce(n, op=pg.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -254,14 +273,10 @@ def run_gpu(args):
     if pg is not None:
         pg.barrier()
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    if pg is not None:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, total_positions = reduce_timing(t_start.elapsed_time(t_end), positions, pg, dev)
     verify_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms_step = ms / args.steps
-    value = positions * world / (ms_step * 1e-3)
+    value = total_positions / (ms_step * 1e-3)
 
     # end to end: pinned host inputs -> device, verify + commit, outputs -> host
     e2e = None
@@ -310,7 +325,10 @@ def run_gpu(args):
                "steps": steps_e2e}
 
     peak, peak_src = peaks()
-    achieved = bytes_needed / (verify_ms * 1e-3) / 1e9
+    # algorithmic bytes: every target and draft row of the call read once
+    # (s*V*sum_b(2k_b+1) sampled, s*V*(k_b+1) greedy); the kernel skips the
+    # rows after each sequence's first rejection, so it moves fewer
+    achieved = bytes_all / (verify_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -330,11 +348,11 @@ def run_gpu(args):
                    "positions_per_step": positions, "target_rows": int((kb + 1).sum()),
                    "l2": f"{COPIES} rotating input copies ({COPIES * (w.target.nbytes + w.draft.nbytes) / 1e9:.1f} GB) > 129 MB L2",
                    "parallelism": f"replicas x{world}"},
-        "hbm": {"bytes_needed_per_call": bytes_needed,
-                "bytes_all_rows_per_call": bytes_all,
-                "rows_needed": rows_needed, "rows_all": rows_all,
-                "gbs_needed": achieved,
-                "gbs_all_rows_equivalent": bytes_all / (verify_ms * 1e-3) / 1e9,
+        "hbm": {"bytes_algorithmic_per_call": bytes_all,
+                "bytes_rows_read_per_call": bytes_needed,
+                "rows_all": rows_all, "rows_read": rows_needed,
+                "gbs_algorithmic": achieved,
+                "gbs_rows_read": bytes_needed / (verify_ms * 1e-3) / 1e9,
                 "frac_of_peak": achieved / peak, "peak_gbs": peak, "peak_source": peak_src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": args.traffic,
@@ -352,12 +370,217 @@ def run_gpu(args):
         pg.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# c4: layer-skip draft/target logits on the tensor cores, then verify
+# --------------------------------------------------------------------------
+def _c4_oracle_step(x, tokens, knobs, B, K):
+    """One step of the float64 oracle: both LM heads, then the verify rule."""
+    import numpy as np
+    from oracle import lmhead as ol
+    from oracle import verify as ov
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    V = x.V
+    dl = wl.f64_to_bf16_bits(ol.lmhead_rmsnorm(x.hidden, x.norm_w, x.eps, x.W)).reshape(B, K + 1, V)
+    tl = wl.f64_to_bf16_bits(ol.lmhead_rmsnorm(x.hidden_t, x.norm_w, x.eps, x.W)).reshape(B, K + 1, V)
+    ov.spec_verify(tl, np.ascontiguousarray(dl[:, :K]), wl.BF16, B, K, V, tokens,
+                   knobs["k_per_row"], knobs["temperature"], 1.0, knobs["uniforms"], knobs["mode"])
+    return int(knobs["k_per_row"].sum())
+
+
+def run_gpu_c4(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from speculative_decoding_verification_47_gb300 import binding as sb
+    from speculative_decoding_verification_47_gb300 import build as bld
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    if pg is not None:
+        pg.barrier()
+    B, K = 64, 7
+    x = wl.lmhead_inputs()
+    M, H, V = x.M, x.H, x.V
+    knobs = wl.c4_verify_knobs(B, K)
+    dev = torch.device("cuda", local)
+    d_h = torch.from_numpy(x.hidden.view(np.int16)).to(dev)
+    d_ht = torch.from_numpy(x.hidden_t.view(np.int16)).to(dev)
+    d_w = torch.from_numpy(x.norm_w.view(np.int16)).to(dev)
+    d_W = torch.from_numpy(x.W.view(np.int16)).to(dev)  # 262 MB model weight (> L2)
+    dl = torch.empty((M, V), dtype=torch.int16, device=dev)
+    tl = torch.empty((M, V), dtype=torch.int16, device=dev)
+    wsl = sb.sv_lmhead_workspace_size(M, H)
+    ws1 = torch.zeros(wsl, dtype=torch.uint8, device=dev)
+    ws2 = torch.zeros(wsl, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # draft tokens from the first draft logits (the draft sampler precedes the path)
+    sb.sv_lmhead_rmsnorm(d_h, d_w, x.eps, d_W, dl, sb.SV_BF16, M, H, V, ws1, wsl, stream)
+    torch.cuda.synchronize()
+    d_bits = dl.cpu().numpy().view(np.uint16).reshape(B, K + 1, V)
+    tokens = wl.draw_draft_tokens(d_bits[:, :K], wl.BF16, knobs["k_per_row"], knobs["temperature"],
+                                  knobs["mode"], seed=4004)
+    tok = torch.from_numpy(tokens).to(dev)
+    kpr = torch.from_numpy(knobs["k_per_row"]).to(dev)
+    tmp = torch.from_numpy(knobs["temperature"]).to(dev)
+    uni = torch.from_numpy(knobs["uniforms"]).to(dev)
+    mode = torch.from_numpy(knobs["mode"]).to(dev)
+    seq = torch.from_numpy(np.random.default_rng(3004).integers(128, 4097, size=B).astype(np.int32)).to(dev)
+    cap = torch.full((B,), 2**30, dtype=torch.int32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    wsb = sb.sv_workspace_size(B, K, V, sb.SV_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        pos = _c4_oracle_step(x, tokens, knobs, B, K)
+        wall = time.perf_counter() - t0
+        cpu = {"value": pos / wall, "unit": "positions/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle",
+               "sample": f"one full step (two float64 LM heads 512x4096x32000 with NumPy BLAS, "
+                         f"then the verify rule on 64 sequences), wall {wall:.2f} s"}
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(max(args.steps, 1))]
+
+    def step(i=None):
+        if i is not None:
+            ev[i][0].record(stream)
+        sb.sv_lmhead_rmsnorm(d_h, d_w, x.eps, d_W, dl, sb.SV_BF16, M, H, V, ws1, wsl, stream)
+        if i is not None:
+            ev[i][1].record(stream)
+        sb.sv_lmhead_rmsnorm(d_ht, d_w, x.eps, d_W, tl, sb.SV_BF16, M, H, V, ws2, wsl, stream)
+        sb.sv_spec_verify(tl, 0, 0, dl, (K + 1) * V, V, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
+                          uni, mode, out, nacc, None, ws, wsb, stream)
+        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = (sb.sv_read_device_flags(ws), sb.sv_read_device_flags(ws1))
+    positions = int(knobs["k_per_row"].sum())
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for it in range(args.steps):
+        step(it)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clk = clocks.stop()
+    ms, total_positions = reduce_timing(t_start.elapsed_time(t_end), positions, pg, dev)
+    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[:args.steps])
+    ms_step = ms / args.steps
+    value = total_positions / (ms_step * 1e-3)
+    flops = 2.0 * M * H * V
+    achieved = flops / (lm_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        h_h = torch.from_numpy(x.hidden.view(np.int16)).pin_memory()
+        h_ht = torch.from_numpy(x.hidden_t.view(np.int16)).pin_memory()
+        h_small = [torch.from_numpy(a).pin_memory() for a in
+                   (tokens, knobs["k_per_row"], knobs["temperature"], knobs["uniforms"], knobs["mode"])]
+        d_small = [tok, kpr, tmp, uni, mode]
+        o_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        o_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+        o_seq = torch.empty((B,), dtype=torch.int32).pin_memory()
+        steps_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            d_h.copy_(h_h, non_blocking=True)
+            d_ht.copy_(h_ht, non_blocking=True)
+            for d_, h_ in zip(d_small, h_small):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            o_out.copy_(out, non_blocking=True)
+            o_n.copy_(nacc, non_blocking=True)
+            o_seq.copy_(seq, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b)
+        if pg is not None:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = (h_h.numel() + h_ht.numel()) * 2 + sum(t_.numel() * t_.element_size() for t_ in h_small)
+        d2h = (o_out.numel() + o_n.numel() + o_seq.numel()) * 4
+        e2e = {"value": positions * world / (ems / steps_e2e * 1e-3), "unit": "positions/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps_e2e}
+
+    tpeak, tsrc = tensor_peak()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS["c4"], "name": "c4", "B": B, "K": K, "V": V, "M": M, "H": H,
+                   "l2": "W (262 MB) > 129 MB L2, streamed from HBM by every LM-head call",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": achieved / tpeak, "traffic": args.traffic,
+                     "kernel": "sv_lmhead_rmsnorm (rmsnorm_kernel + lmhead_gemm_kernel), draft call",
+                     "flops_per_call": flops, "launch_ms": lm_ms, "peak_source": tsrc},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk,
+        "device_flags": list(flags),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def run_reference(args):
     world, rank, local = dist_setup(args)
     if rank != 0:
         return
     sys.path.insert(0, ROOT)
     from speculative_decoding_verification_47_gb300 import workloads as wl
+    if args.workload == "c4":
+        return run_reference_c4(args)
     spec = wl.row_spec(args.workload, args.B)
     workers = min(16, len(os.sched_getaffinity(0)))
     for _ in range(args.warmup):
@@ -393,6 +616,42 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_c4(args):
+    """The oracle on the layer-skip step; draft tokens from the oracle's own
+    draft logits."""
+    import numpy as np
+    from oracle import lmhead as ol
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    B, K = 64, 7
+    x = wl.lmhead_inputs()
+    knobs = wl.c4_verify_knobs(B, K)
+    dl = wl.f64_to_bf16_bits(ol.lmhead_rmsnorm(x.hidden, x.norm_w, x.eps, x.W)).reshape(B, K + 1, x.V)
+    tokens = wl.draw_draft_tokens(dl[:, :K], wl.BF16, knobs["k_per_row"], knobs["temperature"],
+                                  knobs["mode"], seed=4004)
+    for _ in range(min(args.warmup, 1)):
+        _c4_oracle_step(x, tokens, knobs, B, K)
+    tot_pos, tot_wall = 0, 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        tot_pos += _c4_oracle_step(x, tokens, knobs, B, K)
+        tot_wall += time.perf_counter() - t0
+    value = tot_pos / tot_wall
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS["c4"], "name": "c4", "B": B, "K": K, "V": x.V,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: both float64 LM heads and the verify rule, in full"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -414,6 +673,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "c4":
+        run_gpu_c4(args)
     else:
         run_gpu(args)
 
