@@ -704,12 +704,20 @@ struct Shared {
   // item scalars, written by one thread and read by the whole CTA
   RowAcc row_t, row_d;
   DF S_w, rem;
-  int skip, skip_seen;
+  int skip, skip_seen, moot;
   int fin, fin_j, fin_err;
   int owner, rsel;
   int x;
   float u_i, zt_x, zd_x;
 };
+
+// An earlier position of the sequence has been rejected (or failed): this
+// item cannot change the result.
+__device__ __forceinline__ bool item_moot(const unsigned long long* words, int b, int i) {
+  const unsigned long long w = __ldcg(words + b);
+  const unsigned long long R = ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
+  return (R & ((1ull << i) - 1)) != 0;
+}
 
 __device__ __forceinline__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
   const unsigned long long mask = (1ull << kWordBits) - 1;
@@ -1750,7 +1758,14 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   {
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-    for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight) {
+    int step = 0;
+    for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight, ++step) {
+      // every other step each thread looks again whether an earlier
+      // position has been rejected meanwhile; if so it stops reading (the
+      // item is then moot, and rank 0 drops it after the combine).  A plain
+      // per-thread load: the lanes of a warp may leave this loop at
+      // different steps, so no warp-synchronous operation may sit in it.
+      if (i > 0 && (step & 1) && item_moot(P.words, b, i)) break;
       uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
 #pragma unroll
       for (int k = 0; k < kLoadsInFlight; ++k) {
@@ -1790,6 +1805,11 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
       sh.row_d = cd;
     }
   }
+  // rank 0 decides once, for the whole cluster, whether the item became moot
+  if (rank == 0 && tid == 32) {
+    const int m = (i > 0 && item_moot(P.words, b, i)) ? 1 : 0;
+    for (int r = 0; r < C; ++r) *remote(cluster, C, &sh.moot, r) = m;
+  }
   if (C > 1) {
     cluster.sync();
     if (warp == 0) {
@@ -1802,6 +1822,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     }
   }
   __syncthreads();
+  if (sh.moot) return;  // (uniform in the cluster; no distributed access follows)
   const RowAcc row_t = sh.row_t, row_d = sh.row_d;
   // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
   const bool bad_t = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
