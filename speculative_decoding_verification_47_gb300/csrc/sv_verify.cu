@@ -1657,12 +1657,16 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
       }
     }
   }
-  __threadfence();
   unsigned long long bits = 1ull << i;
   if (errbits) bits |= 1ull << (2 * kWordBits + i);
   else if (reject) bits |= 1ull << (kWordBits + i);
-  const unsigned long long old = atomicOr(P.words + b, bits);
-  __threadfence();
+  // release: this item's statistics are visible before its bits; acquire:
+  // the finisher then sees the statistics every earlier item released
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(P.words + b), "l"(bits)
+               : "memory");
   int j0, j1;
   bool e0_, e1_;
   const bool was = resolvable(old, kb, &j0, &e0_);
