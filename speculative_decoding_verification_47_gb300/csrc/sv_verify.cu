@@ -42,7 +42,9 @@ namespace sv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCmax = 16;
-constexpr int kLoadsInFlight = 4;                  // 16-byte loads per row per thread per step
+constexpr int kLoadsInFlight = 4;                  // 16-byte units per row per thread per step
+constexpr int kRingStages = 2;                     // steps of units in flight ahead of the one reduced
+constexpr int kRingBytes = kRingStages * 2 * kLoadsInFlight * kThreads * 16;  // 64 KB
 constexpr int kMaxRounds = 64;                     // slice <= 64 * 256 units = 256 KB of a row
 constexpr int kWordBits = 21;                      // positions per field of the sequence word
 
@@ -397,9 +399,22 @@ __device__ __forceinline__ void greedy_elem(RowAcc& a, float z, int e) {
 }
 
 // ---------------------------------------------------------------------------
-// Loads: 16-byte units straight into registers (read-only path).  Units
-// outside the aligned body [ub0, ub1) are read element by element.
+// Loads: 16-byte units, read-only path, straight into registers or (the row
+// pass) copied asynchronously into the thread's own shared-memory slots
+// (cp.async: the bytes in flight hold no registers).  Units outside the
+// aligned body [ub0, ub1) are read element by element.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int ES>
 __device__ __forceinline__ uint4 ldg_unit(const RowSlice<ES>& rs, int u) {
   return __ldg(reinterpret_cast<const uint4*>(rs.base16 + 16 * (uintptr_t)u));
@@ -697,7 +712,6 @@ struct Shared {
   RowAcc g_t[kCmax], g_d[kCmax];
   DF g_w[kCmax];
   // per-warp partials
-  RowAcc l_t[kThreads], l_d[kThreads];
   DF rtot[kMaxRounds];
   DF scan[kWarps];
   int r_i[kWarps];
@@ -1760,43 +1774,73 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   }
   RowAcc at = acc_init(), ad = acc_init();
   {
+    // Each thread keeps kRingStages steps of its units in flight in its own
+    // shared-memory slots (slot k of stage s: ring[(s*2L + k)*kThreads + tid],
+    // k < L target, k >= L draft) and reduces the oldest step from there.
+    constexpr int L = kLoadsInFlight;
+    constexpr int kStep = kThreads * L;
+    uint4* ring = reinterpret_cast<uint4*>(vals);
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-    int step = 0;
-    for (int u0 = tid; u0 < NU; u0 += kThreads * kLoadsInFlight, ++step) {
+    const int nsteps = (NU > tid) ? (NU - tid + kStep - 1) / kStep : 0;
+    auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
+      const int u0 = tid + n * kStep;
+      uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        const int u = u0 + k * kThreads;
+        if (u >= tb0 && u < tb1)
+          cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
+        if (has_draft && u >= db0 && u < db1)
+          cp_async16(slot + (L + k) * kThreads, reinterpret_cast<const void*>(sd.base16 + 16 * (uintptr_t)u));
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int n = 0; n < kRingStages; ++n) issue(n);
+    for (int n = 0; n < nsteps; ++n) {
       // every other step each thread looks again whether an earlier
       // position has been rejected meanwhile; if so it stops reading (the
       // item is then moot, and rank 0 drops it after the combine).  A plain
       // per-thread load: the lanes of a warp may leave this loop at
       // different steps, so no warp-synchronous operation may sit in it.
-      if (i > 0 && (step & 1) && item_moot(P.words, b, i)) break;
-      uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
+      if (i > 0 && (n & 1) && item_moot(P.words, b, i)) break;
+      cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
+      const int u0 = tid + n * kStep;
+      const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      uint4 vt[L], vd[L];
 #pragma unroll
-      for (int k = 0; k < kLoadsInFlight; ++k) {
+      for (int k = 0; k < L; ++k) {
         const int u = u0 + k * kThreads;
-        vt[k] = (u >= tb0 && u < tb1) ? ldg_unit(st, u) : make_uint4(0, 0, 0, 0);
-        vd[k] = (has_draft && u >= db0 && u < db1) ? ldg_unit(sd, u) : make_uint4(0, 0, 0, 0);
+        vt[k] = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
+        vd[k] = (has_draft && u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int k = 0; k < kLoadsInFlight; ++k) {
+      for (int k = 0; k < L; ++k) {
         const int u = u0 + k * kThreads;
         row_unit_v<ES>(at, st, u, tb0, tb1, vt[k], greedy, X);
         if (has_draft) row_unit_v<ES>(ad, sd, u, db0, db1, vd[k], false, X);
       }
       if (!greedy) acc_flush(at);
       if (has_draft) acc_flush(ad);
+      issue(n + kRingStages);  // (the slots were consumed above)
     }
+    cp_async_wait_all();
   }
   if (!greedy) acc_finish_max<ES>(at);
   if (has_draft) acc_finish_max<ES>(ad);
 
   // ---- combine: threads -> CTA (warp 0, through shared memory) -> cluster ----
-  sh.l_t[tid] = at;
-  if (has_draft) sh.l_d[tid] = ad;
+  // (the per-thread partials reuse the ring: every thread's copies have landed)
+  RowAcc* l_t = reinterpret_cast<RowAcc*>(vals);
+  RowAcc* l_d = l_t + kThreads;
+  __syncthreads();
+  l_t[tid] = at;
+  if (has_draft) l_d[tid] = ad;
   __syncthreads();
   if (warp == 0) {
-    RowAcc ct = acc_merge_lanes(sh.l_t, lane, greedy);
-    RowAcc cd = has_draft ? acc_merge_lanes(sh.l_d, lane, false) : acc_init();
+    RowAcc ct = acc_merge_lanes(l_t, lane, greedy);
+    RowAcc cd = has_draft ? acc_merge_lanes(l_d, lane, false) : acc_init();
     ct = lanes_combine(ct, true, greedy);
     cd = lanes_combine(cd, true, false);
     if (C > 1) {
@@ -1983,12 +2027,15 @@ static int sm_count() {
 }
 
 // Cluster width: enough CTAs per position level (B items each) to give every
-// SM about three, as wide as small batches need for latency, and at least wide
-// enough that a slice fits kMaxRounds rounds; at most 16 CTAs.
+// SM about three, but no slice under 32 KB of a row (narrower slices spend
+// more time in the per-item combine and decision than in streaming), and at
+// least wide enough that a slice fits kMaxRounds rounds; at most 16 CTAs.
 static void choose_geometry(int V, int ES, int B, int* C_out, int* slice_out) {
   const long long row_bytes = (long long)V * ES;
   const long long max_slice = (long long)kMaxRounds * kThreads * 16 - 64;
   int C = (3 * sm_count() + B - 1) / (B > 0 ? B : 1);
+  const int cwide = (int)((row_bytes + 32767) / 32768);
+  if (C > cwide) C = cwide;
   const int cmin = (int)((row_bytes + max_slice - 1) / max_slice);
   if (C < cmin) C = cmin;
   if (C < 1) C = 1;
@@ -2013,6 +2060,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   }
   const bool topp = L.top_p < 1.0f;
   size_t smem = (size_t)rounds * kThreads * sizeof(float);
+  if (smem < (size_t)kRingBytes) smem = kRingBytes;  // the row pass's ring
   if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
