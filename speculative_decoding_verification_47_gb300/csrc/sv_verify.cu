@@ -481,32 +481,6 @@ __device__ __forceinline__ RowAcc lanes_combine(RowAcc v, bool valid, bool greed
   return RowAcc{m, Rw, s, 0x7fffffff};
 }
 
-// Lane l of warp 0 folds the accumulators of threads l, l + 32, ... into one
-// (exact power-of-two rescaling to the largest reference, compensated sums).
-__device__ __forceinline__ RowAcc acc_merge_lanes(const RowAcc* acc, int lane, bool greedy) {
-  RowAcc a = acc[lane];
-  for (int t = lane + 32; t < kThreads; t += 32) {
-    const RowAcc b = acc[t];
-    if (greedy) {
-      if (b.mx != b.mx) a.mx = b.mx;
-      else if (b.mx > a.mx || (b.mx == a.mx && b.amax < a.amax)) {
-        a.mx = b.mx;
-        a.amax = b.amax;
-      }
-      continue;
-    }
-    a.mx = nanmax(a.mx, b.mx);
-    if (b.R > a.R) {
-      acc_raise(a, b.R);
-      a.s = df_add(a.s, b.s);
-    } else if (b.R > kRnone) {
-      const float p = pow2i(b.R - a.R);
-      a.s = df_add(a.s, DF{b.s.hi * p, b.s.lo * p});
-    }
-  }
-  return a;
-}
-
 __device__ __forceinline__ DF df_shfl(DF v, int src) {
   return DF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
@@ -705,6 +679,7 @@ struct Shared {
   int selbin[2], lowbin[2], sel_cnt[2];
   DF sel_excl[2];
   DF wab[2][kWarps];
+  RowAcc w_t[kWarps], w_d[kWarps];  // per-warp partials of the row pass
   uint32_t rcnt[kMaxRounds];
   uint32_t ccnt[kCmax];
   int tcut, rrem, xtok;
@@ -1830,19 +1805,19 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   if (!greedy) acc_finish_max<ES>(at);
   if (has_draft) acc_finish_max<ES>(ad);
 
-  // ---- combine: threads -> CTA (warp 0, through shared memory) -> cluster ----
-  // (the per-thread partials reuse the ring: every thread's copies have landed)
-  RowAcc* l_t = reinterpret_cast<RowAcc*>(vals);
-  RowAcc* l_d = l_t + kThreads;
-  __syncthreads();
-  l_t[tid] = at;
-  if (has_draft) l_d[tid] = ad;
+  // ---- combine: lanes -> warps (butterflies) -> CTA (warp 0) -> cluster ----
+  {
+    const RowAcc wt = lanes_combine(at, true, greedy);
+    const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
+    if (lane == 0) {
+      sh.w_t[warp] = wt;
+      sh.w_d[warp] = wd;
+    }
+  }
   __syncthreads();
   if (warp == 0) {
-    RowAcc ct = acc_merge_lanes(l_t, lane, greedy);
-    RowAcc cd = has_draft ? acc_merge_lanes(l_d, lane, false) : acc_init();
-    ct = lanes_combine(ct, true, greedy);
-    cd = lanes_combine(cd, true, false);
+    const RowAcc ct = lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy);
+    const RowAcc cd = lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false);
     if (C > 1) {
       if (lane < C) {
         *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
@@ -1991,7 +1966,9 @@ template <int ES, bool TOPP>
 static cudaError_t configure() {
   cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxRounds * kThreads * (int)sizeof(float));
+                                       kMaxRounds * kThreads * (int)sizeof(float) > kRingBytes
+                                           ? kMaxRounds * kThreads * (int)sizeof(float)
+                                           : kRingBytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
