@@ -700,12 +700,15 @@ struct Shared {
   float u_i, zt_x, zd_x;
 };
 
-// An earlier position of the sequence has been rejected (or failed): this
-// item cannot change the result.
-__device__ __forceinline__ bool item_moot(const unsigned long long* words, int b, int i) {
-  const unsigned long long w = __ldcg(words + b);
+// An earlier position of the sequence has been rejected (or failed) in the
+// sequence word w: item i cannot change the result.
+__device__ __forceinline__ bool word_moot(unsigned long long w, int i) {
   const unsigned long long R = ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
   return (R & ((1ull << i) - 1)) != 0;
+}
+
+__device__ __forceinline__ bool item_moot(const unsigned long long* words, int b, int i) {
+  return word_moot(__ldcg(words + b), i);
 }
 
 __device__ __forceinline__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
@@ -1773,13 +1776,18 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     };
 #pragma unroll
     for (int n = 0; n < kRingStages; ++n) issue(n);
+    // the sequence word, read two steps before it is looked at (no stall)
+    unsigned long long wseen = (i > 0) ? __ldcg(P.words + b) : 0ull;
     for (int n = 0; n < nsteps; ++n) {
       // every other step each thread looks again whether an earlier
       // position has been rejected meanwhile; if so it stops reading (the
       // item is then moot, and rank 0 drops it after the combine).  A plain
       // per-thread load: the lanes of a warp may leave this loop at
       // different steps, so no warp-synchronous operation may sit in it.
-      if (i > 0 && (n & 1) && item_moot(P.words, b, i)) break;
+      if (i > 0 && (n & 1)) {
+        if (word_moot(wseen, i)) break;
+        wseen = __ldcg(P.words + b);
+      }
       cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
       const int u0 = tid + n * kStep;
       const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
