@@ -161,8 +161,9 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
  * on every GPU that loads it until the process exits.  The call allocates
  * nothing and frees nothing.
  *   - Limit: sv_workspace_size(B, K, V, dtype) must be <= 2 MiB (for example
- *     B = 256 with K <= 20, or B = 4096 with K <= 11); larger batches return
- *     SV_ERR_WORKSPACE without launching anything.
+ *     B <= 4096 with any K <= 20, B = 8192 with K <= 14, or B = 16384 with
+ *     K <= 6); larger batches return SV_ERR_WORKSPACE without launching
+ *     anything.
  *   - The first call on each device looks up that device's copy of the
  *     array (with the device current); make that first call before any
  *     stream capture.

@@ -11,24 +11,27 @@
 // Work decomposition.  One "item" is a (sequence b, position i) pair: the
 // target row i and, for i < k_b on a sampled row, the draft row i.  An item
 // runs on a thread-block cluster of C CTAs; CTA r owns the vocabulary slice
-// [r*L, (r+1)*L) of both rows and streams it through a 3-stage ring in shared
-// memory fed by the bulk-copy engine (one mbarrier per stage).  Each row is
-// reduced in ONE pass: the running max, and the sum of 2^(z*c - R) where the
-// reference exponent R is an integer that only grows; when it grows the
-// partial sum is rescaled by an exact power of two, so the online pass adds
-// no rounding beyond the exponentials themselves.  The cluster combines the
-// per-slice results through distributed shared memory.
+// [r*L, (r+1)*L) of both rows.  Each thread keeps two steps of 16-byte units
+// of both rows in flight in its own shared-memory slots (cp.async) and
+// reduces the oldest step.  Each row is reduced in ONE pass: the running max,
+// and the sum of 2^(z*c - R) where the reference exponent R is an integer
+// that only grows; when it grows the partial sum is rescaled by an exact
+// power of two, so the online pass adds no rounding beyond the exponentials
+// themselves.  The cluster combines the per-slice results through
+// distributed shared memory.
 //
 // Items are launched position-major (all sequences' position 0 first).  Each
 // item publishes {done, rejected, error} bits for its position in one 64-bit
-// word per sequence.  An item that starts after an earlier position of its
-// sequence has been rejected exits without reading its rows: those rows
-// cannot change the result.  The item whose publication completes the
-// prefix 0..j (j = first rejection, or k_b when all were accepted) is the
-// sequence's finisher: it streams row(s) j again (usually still in L2) to
-// sum the residual max(0, p - q) (or p for the bonus) per chunk, then reads
-// back the one chunk that holds the inverse-CDF point.  No item ever waits
-// for another one.
+// word per sequence.  An item whose sequence already has an earlier rejection
+// (seen at its start, or while it streams) drops out: those rows cannot
+// change the result.  Every CTA of the cluster computes the item's verdict;
+// rank 0 publishes it.  A sampled item that rejects x_i, or the bonus item
+// i = k_b, then draws its token at once from norm(max(0, p - q)) (or p):
+// one more pass over its rows sums the residual per warp and round, and one
+// warp re-reads the 32 units around the inverse-CDF point.  The sequence's
+// outputs are written by whichever comes last of the item that completes the
+// prefix 0..j (j = first rejection, or k_b) and the draw at j, met through a
+// second per-sequence word.  No item ever waits for another one.
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -42,23 +45,18 @@ namespace sv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCmax = 16;
-constexpr int kLoadsInFlight = 4;                  // 16-byte units per row per thread per step
+constexpr int kLoadsInFlight = 2;                  // 16-byte units per row per thread per step
 constexpr int kRingStages = 2;                     // steps of units in flight ahead of the one reduced
-constexpr int kRingBytes = kRingStages * 2 * kLoadsInFlight * kThreads * 16;  // 64 KB
+constexpr int kRingBytes = kRingStages * 2 * kLoadsInFlight * kThreads * 16;  // 32 KB
 constexpr int kMaxRounds = 64;                     // slice <= 64 * 256 units = 256 KB of a row
 constexpr int kWordBits = 21;                      // positions per field of the sequence word
 
+// What an item leaves for the one that writes its sequence's outputs.
 struct ItemStats {
-  float m_t, R_t, st_hi, st_lo;
-  float m_d, R_d, sd_hi, sd_lo;
-  int argmax;
-  uint32_t errbits;
-  // top-p (rows with top_p < 1): the cut key, how many tokens with that key
-  // are kept (the first nk in index order) out of cnt, and the kept mass in
-  // the row's 2^(z*c - R) units
-  uint32_t key_t, key_d;
-  int nk_t, cnt_t, nk_d, cnt_d;
-  float et_hi, et_lo, ed_hi, ed_lo;
+  int argmax;        // first maximum of the target row (greedy rows)
+  uint32_t errbits;  // SV_FLAG_* bits of this position's error, 0 if none
+  int y;             // this position's draw (resample or bonus), kYBad if its uniform was bad
+  int pad;
 };
 
 struct VerifyParams {
@@ -78,6 +76,7 @@ struct VerifyParams {
   float* diag;
   uint32_t* flags;
   unsigned long long* words;
+  uint32_t* words2;  // per sequence: bit 0 prefix resolved, bit 1+i draw of position i stored
   ItemStats* stats;
   int slice_len;  // elements per CTA slice
 };
@@ -686,6 +685,7 @@ struct Shared {
   // all-gather slots, indexed by the writing CTA's rank
   RowAcc g_t[kCmax], g_d[kCmax];
   DF g_w[kCmax];
+  int g_m[kCmax];
   // per-warp partials
   DF rtot[kMaxRounds];
   DF scan[kWarps];
@@ -693,11 +693,13 @@ struct Shared {
   // item scalars, written by one thread and read by the whole CTA
   RowAcc row_t, row_d;
   DF S_w, rem;
-  int skip, skip_seen, moot;
-  int fin, fin_j, fin_err;
+  int skip, moot;
+  int fin;
   int owner, rsel;
   int x;
-  float u_i, zt_x, zd_x;
+  float u_i, zt_x, zd_x, uK;
+  uint32_t eb;  // the item's verdict: error bits, rejection
+  int rej;
 };
 
 // An earlier position of the sequence has been rejected (or failed) in the
@@ -711,7 +713,7 @@ __device__ __forceinline__ bool item_moot(const unsigned long long* words, int b
   return word_moot(__ldcg(words + b), i);
 }
 
-__device__ __forceinline__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
+__device__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
   const unsigned long long mask = (1ull << kWordBits) - 1;
   const unsigned long long D = w & mask;
   const unsigned long long Rj = (w >> kWordBits) & mask;
@@ -722,6 +724,58 @@ __device__ __forceinline__ bool resolvable(unsigned long long w, int kb, int* j_
   *j_out = j;
   *err = (E >> j) & 1;
   return (D & need) == need;
+}
+
+constexpr int kYBad = -2;  // a draw whose uniform was outside [0, 1)
+
+__device__ void write_outputs(const VerifyParams& P, int b, int n, int y, bool err);
+
+// Outputs of sampled sequence b with the draw y at its cut j (error outputs
+// if the draw's uniform was bad).
+__device__ void emit_sampled(const VerifyParams& P, int b, int j, int y);
+
+__device__ __forceinline__ uint32_t or_acqrel32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.or.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long or_acqrel64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
+__device__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err);
+
+// A sampled sequence's outputs need its prefix resolved (bit 0 of its second
+// word, set by the item whose publication completed the prefix) and the draw
+// at its cut j stored (bit 1 + j, set by item j after its draw).  Each side
+// sets its bit with one atomic; the one that finds the other bit already set
+// writes the outputs, so exactly one does.
+__device__ void prefix_resolved(const VerifyParams& P, int b, int j) {
+  const uint32_t old = or_acqrel32(P.words2 + b, 1u);
+  if (old & (1u << (1 + j))) emit_sampled(P, b, j, __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].y));
+}
+
+__device__ void draw_ready(const VerifyParams& P, int b, int i, int kb, int y) {
+  P.stats[(size_t)b * (P.K + 1) + i].y = y;
+  const uint32_t old = or_acqrel32(P.words2 + b, 1u << (1 + i));
+  if (old & 1u) {  // prefix already resolved: emit if this position is the cut
+    int j;
+    bool err;
+    const unsigned long long w = or_acqrel64(P.words + b, 0ull);
+    if (resolvable(w, kb, &j, &err) && !err && j == i) emit_sampled(P, b, i, y);
+  }
+}
+
+__device__ void emit_sampled(const VerifyParams& P, int b, int j, int y) {
+  if (y == kYBad) {
+    write_outputs(P, b, 0, -1, true);
+    atomicOr(P.flags, SV_FLAG_BAD_UNIFORM);
+  } else {
+    write_outputs(P, b, j, y, false);
+  }
 }
 
 __device__ void write_outputs(const VerifyParams& P, int b, int n, int y, bool err) {
@@ -1374,11 +1428,13 @@ __device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group&
 }
 
 // ---------------------------------------------------------------------------
-// Finisher: draw the resample (or bonus) token of sequence b at cut j with
-// the uniform uK.  Every CTA of the cluster takes part.  Pass over the rows:
-// each thread's unit sums go to shared memory in index order (round r holds
-// units r*kThreads .. r*kThreads + kThreads-1); then round totals, the
-// cluster-wide owner of u*total, the round, the unit and the element.
+// Draw of the resample (or bonus) token of sequence b at position j with the
+// uniform uK, made by item j itself right after its verdict.  Every CTA of
+// the cluster takes part.  One pass over both rows puts each thread's unit
+// sums in shared memory in index order (round r holds units
+// r*kThreads .. r*kThreads + kThreads-1); then round totals, the cluster-wide
+// owner of u*total, the round, the unit and the element.  The token is
+// stored for the sequence's outputs.
 // ---------------------------------------------------------------------------
 template <int ES, bool TOPP>
 __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals,
@@ -1549,17 +1605,17 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
     }
   }
   if (y < 0) y = ylast;
-  write_outputs(P, b, j, y, false);
+  draw_ready(P, b, j, kb, y);
 }
 
-// Decision of one item and its publication in the sequence word (rank 0,
-// thread 0).  Returns 1 if this item completes the sequence's prefix, with
-// the cut position and whether it is an error in *j_out / *err_out.
+// Verdict of one item: its error bits and whether x_i is rejected.  Every
+// CTA of the cluster computes it (thread 0) from values that are identical in
+// all of them, and gets the same answer; *dq receives p'(x), q'(x) and the
+// ratio for the diagnostics.
 template <int ES, bool TOPP>
-__device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int b, int kb,
-                                   bool greedy, bool has_draft, const Expo& X, const RowAcc& row_t,
-                                   const RowAcc& row_d, bool bad_t, bool bad_d, int* j_out,
-                                   int* err_out) {
+__device__ __noinline__ void judge(const VerifyParams& P, Shared& sh, int i, int kb, bool greedy,
+                                   bool has_draft, const Expo& X, const RowAcc& row_t,
+                                   const RowAcc& row_d, bool bad_t, bool bad_d, float* dq) {
   const int x = sh.x;
   const float u_i = sh.u_i, zt_x = sh.zt_x, zd_x = sh.zd_x;
   uint32_t errbits = 0;
@@ -1601,35 +1657,30 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
       reject = !(u_i < r);
     }
   }
+  sh.eb = errbits;
+  sh.rej = reject ? 1 : 0;
+  dq[0] = diag_px;
+  dq[1] = diag_qx;
+  dq[2] = diag_r;
+}
+
+// Publication of an item's verdict in the sequence word (rank 0, thread 0).
+// Returns 1 if it completes the sequence's prefix, with the cut position and
+// whether it is an error in *j_out / *err_out; *moot_out tells whether an
+// earlier position had already been rejected or failed.
+template <bool TOPP>
+__device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, int b, int kb,
+                                    bool greedy, bool has_draft, const Expo& X,
+                                    const RowAcc& row_t, const RowAcc& row_d, bool bad_t,
+                                    bool bad_d, uint32_t errbits, bool reject, const float* dq,
+                                    int* j_out, int* err_out, bool* moot_out) {
   ItemStats s;
-  s.m_t = row_t.mx;
-  s.R_t = row_t.R;
-  s.st_hi = row_t.s.hi;
-  s.st_lo = row_t.s.lo;
-  s.m_d = row_d.mx;
-  s.R_d = row_d.R;
-  s.sd_hi = row_d.s.hi;
-  s.sd_lo = row_d.s.lo;
   s.argmax = row_t.amax;
   s.errbits = errbits;
-  const bool sel = TOPP && !greedy && !bad_t && !bad_d;
-  if (sel) {
-    const TopSel& a = sh.ts[0];
-    s.key_t = a.kstar;
-    s.nk_t = a.nk;
-    s.cnt_t = a.cstar;
-    s.et_hi = a.E.hi;
-    s.et_lo = a.E.lo;
-    if (has_draft) {
-      const TopSel& d = sh.ts[1];
-      s.key_d = d.kstar;
-      s.nk_d = d.nk;
-      s.cnt_d = d.cstar;
-      s.ed_hi = d.E.hi;
-      s.ed_lo = d.E.lo;
-    }
-  }
+  s.y = -1;
+  s.pad = 0;
   P.stats[(size_t)b * (P.K + 1) + i] = s;
+  const bool sel = TOPP && !greedy && !bad_t && !bad_d;
   if (P.diag) {
     float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
     dg[SV_DIAG_M_T] = row_t.mx;
@@ -1643,9 +1694,9 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
         dg[SV_DIAG_M_D] = row_d.mx;
         dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
         dg[SV_DIAG_MASS_D] = sel ? df_to_float(df_div(sh.ts[1].E, row_d.s)) : 1.f;
-        dg[SV_DIAG_P_X] = diag_px;
-        dg[SV_DIAG_Q_X] = diag_qx;
-        dg[SV_DIAG_RATIO] = diag_r;
+        dg[SV_DIAG_P_X] = dq[0];
+        dg[SV_DIAG_Q_X] = dq[1];
+        dg[SV_DIAG_RATIO] = dq[2];
       }
     }
   }
@@ -1653,12 +1704,9 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
   if (errbits) bits |= 1ull << (2 * kWordBits + i);
   else if (reject) bits |= 1ull << (kWordBits + i);
   // release: this item's statistics are visible before its bits; acquire:
-  // the finisher then sees the statistics every earlier item released
-  unsigned long long old;
-  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;"
-               : "=l"(old)
-               : "l"(P.words + b), "l"(bits)
-               : "memory");
+  // the outputs then see the statistics every earlier item released
+  const unsigned long long old = or_acqrel64(P.words + b, bits);
+  *moot_out = word_moot(old, i);
   int j0, j1;
   bool e0_, e1_;
   const bool was = resolvable(old, kb, &j0, &e0_);
@@ -1669,7 +1717,7 @@ __device__ __noinline__ int decide(const VerifyParams& P, Shared& sh, int i, int
 }
 
 template <int ES, bool TOPP>
-__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -1677,8 +1725,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   const int item = blockIdx.x / C;
   const int i = item / P.B, b = item % P.B;
 
-  extern __shared__ __align__(16) float vals[];  // finisher's unit sums; top-p histograms
+  extern __shared__ __align__(16) float vals[];  // cp.async ring; draw's unit sums; top-p histograms
   __shared__ Shared sh;
+
+  // the sequence word, read first so that its latency overlaps the
+  // parameter loads (thread 0 of every CTA)
+  const unsigned long long w0 = (tid == 0 && i > 0) ? __ldcg(P.words + b) : 0ull;
 
   // ---- per-row parameters (identical in every CTA of the cluster) ----
   const int kb = P.kpr ? P.kpr[b] : P.K;
@@ -1701,31 +1753,16 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   const bool has_draft = !greedy && i < kb;
   const Expo X = greedy ? Expo{1.f, 1e-30f} : make_expo(T);
 
-  // ---- rank 0 decides whether an earlier rejection makes this item moot ----
-  if (C > 1) {
-    if (rank == 0 && tid == 0) {
-      const unsigned long long w = __ldcg(P.words + b);
-      const unsigned long long R =
-          ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
-      sh.skip = (R & ((1ull << i) - 1)) != 0;
-    }
-    cluster.sync();  // every CTA runs (distributed shared memory is safe)
-    if (tid == 0) sh.skip_seen = *cluster.map_shared_rank(&sh.skip, 0);
-    __syncthreads();
-    if (sh.skip_seen) {
-      cluster.sync();  // rank 0 stays until every CTA has read its flag
-      return;
-    }
-  } else {
-    if (tid == 0) {
-      const unsigned long long w = __ldcg(P.words + b);
-      const unsigned long long R =
-          ((w >> kWordBits) | (w >> (2 * kWordBits))) & ((1ull << kWordBits) - 1);
-      sh.skip_seen = (R & ((1ull << i) - 1)) != 0;
-    }
-    __syncthreads();
-    if (sh.skip_seen) return;
+  // ---- an earlier rejection already makes this item moot: no streaming ----
+  // Each CTA looks for itself.  The CTAs of a cluster may see different words,
+  // so the flag only decides whether this CTA streams; the cluster-wide
+  // verdict is the OR of every CTA's flag, formed in the combine below.
+  if (tid == 0) {
+    sh.skip = word_moot(w0, i) ? 1 : 0;
+    sh.moot = 0;
   }
+  __syncthreads();
+  const bool skip = sh.skip != 0;
 
   // ---- stream the slices: one pass per row, loads straight to registers ----
   const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
@@ -1733,10 +1770,11 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
   if (has_draft) sd.init(P.drf + (long long)b * P.d_seq + (long long)i * P.d_pos, e0, e1);
   else sd = st;
-  // rank 0, warp 1: the decision's inputs, fetched while the rows stream
-  if (rank == 0 && tid == 32) {
+  // warp 1 of every CTA: the decision's inputs, fetched while the rows stream
+  if (tid == 32 && !skip) {
     int x = -1;
     float u = 0.f, zt = 0.f, zd = 0.f;
+    sh.uK = greedy ? 0.f : P.unif[(size_t)b * (P.K + 1) + P.K];
     if (i < kb) {
       x = P.tokens[(size_t)b * P.K + i];
       if (!greedy) u = P.unif[(size_t)b * (P.K + 1) + i];
@@ -1760,49 +1798,87 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     uint4* ring = reinterpret_cast<uint4*>(vals);
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-    const int nsteps = (NU > tid) ? (NU - tid + kStep - 1) / kStep : 0;
+    const int nsteps = (!skip && NU > tid) ? (NU - tid + kStep - 1) / kStep : 0;
+    // Interior steps (every unit of the step inside the aligned bodies of
+    // both rows) take a path without per-unit bounds checks.
+    const int in0 = has_draft ? max(tb0, db0) : tb0, in1 = has_draft ? min(tb1, db1) : tb1;
+    const char* gt = reinterpret_cast<const char*>(st.base16) + 16 * (size_t)tid;
+    const char* gd = reinterpret_cast<const char*>(sd.base16) + 16 * (size_t)tid;
+    auto interior = [&](int u0) { return u0 >= in0 && u0 + (L - 1) * kThreads < in1; };
     auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
       const int u0 = tid + n * kStep;
       uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      if (interior(u0)) {
+        const char* pt = gt + (size_t)n * kStep * 16;
 #pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const int u = u0 + k * kThreads;
-        if (u >= tb0 && u < tb1)
-          cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
-        if (has_draft && u >= db0 && u < db1)
-          cp_async16(slot + (L + k) * kThreads, reinterpret_cast<const void*>(sd.base16 + 16 * (uintptr_t)u));
+        for (int k = 0; k < L; ++k) cp_async16(slot + k * kThreads, pt + (size_t)k * kThreads * 16);
+        if (has_draft) {
+          const char* pd = gd + (size_t)n * kStep * 16;
+#pragma unroll
+          for (int k = 0; k < L; ++k)
+            cp_async16(slot + (L + k) * kThreads, pd + (size_t)k * kThreads * 16);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+          const int u = u0 + k * kThreads;
+          if (u >= tb0 && u < tb1)
+            cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
+          if (has_draft && u >= db0 && u < db1)
+            cp_async16(slot + (L + k) * kThreads, reinterpret_cast<const void*>(sd.base16 + 16 * (uintptr_t)u));
+        }
       }
       cp_async_commit();
     };
+    if (!skip) {
 #pragma unroll
-    for (int n = 0; n < kRingStages; ++n) issue(n);
+      for (int n = 0; n < kRingStages; ++n) issue(n);
+    }
     // the sequence word, read two steps before it is looked at (no stall)
-    unsigned long long wseen = (i > 0) ? __ldcg(P.words + b) : 0ull;
+    unsigned long long wseen = (i > 0 && !skip) ? __ldcg(P.words + b) : 0ull;
     for (int n = 0; n < nsteps; ++n) {
       // every other step each thread looks again whether an earlier
       // position has been rejected meanwhile; if so it stops reading (the
-      // item is then moot, and rank 0 drops it after the combine).  A plain
-      // per-thread load: the lanes of a warp may leave this loop at
+      // item is then moot, and the cluster drops it after the combine).  A
+      // plain per-thread load: the lanes of a warp may leave this loop at
       // different steps, so no warp-synchronous operation may sit in it.
       if (i > 0 && (n & 1)) {
-        if (word_moot(wseen, i)) break;
+        if (word_moot(wseen, i)) {
+          sh.moot = 1;  // (a plain store: read after the barriers below)
+          break;
+        }
         wseen = __ldcg(P.words + b);
       }
       cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
       const int u0 = tid + n * kStep;
       const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
-      uint4 vt[L], vd[L];
+      // units are read from the slots one at a time (the ring, not registers,
+      // holds the step)
+      if (interior(u0)) {
+        constexpr int EPU = 16 / ES;
 #pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const int u = u0 + k * kThreads;
-        vt[k] = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
-        vd[k] = (has_draft && u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
-      }
+        for (int k = 0; k < L; ++k) {
+          const uint4 vt = slot[k * kThreads];
+          if (greedy)
+            greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
+          else
+            sampled_unit<ES>(at, vt, X);
+        }
+        if (has_draft) {
 #pragma unroll
-      for (int k = 0; k < L; ++k) {
-        const int u = u0 + k * kThreads;
-        row_unit_v<ES>(at, st, u, tb0, tb1, vt[k], greedy, X);
-        if (has_draft) row_unit_v<ES>(ad, sd, u, db0, db1, vd[k], false, X);
+          for (int k = 0; k < L; ++k) sampled_unit<ES>(ad, slot[(L + k) * kThreads], X);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+          const int u = u0 + k * kThreads;
+          const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
+          row_unit_v<ES>(at, st, u, tb0, tb1, vt, greedy, X);
+          if (has_draft) {
+            const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
+            row_unit_v<ES>(ad, sd, u, db0, db1, vd, false, X);
+          }
+        }
       }
       if (!greedy) acc_flush(at);
       if (has_draft) acc_flush(ad);
@@ -1826,20 +1902,20 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
   if (warp == 0) {
     const RowAcc ct = lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy);
     const RowAcc cd = lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false);
+    // this CTA's moot flag: the word it saw at the start, or at the last
+    // step it looked (any thread)
+    const int m = (sh.skip | sh.moot) ? 1 : 0;
     if (C > 1) {
       if (lane < C) {
         *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
         *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
+        *cluster.map_shared_rank(&sh.g_m[rank], lane) = m;
       }
     } else if (lane == 0) {
       sh.row_t = ct;
       sh.row_d = cd;
+      sh.g_m[0] = m;
     }
-  }
-  // rank 0 decides once, for the whole cluster, whether the item became moot
-  if (rank == 0 && tid == 32) {
-    const int m = (i > 0 && item_moot(P.words, b, i)) ? 1 : 0;
-    for (int r = 0; r < C; ++r) *remote(cluster, C, &sh.moot, r) = m;
   }
   if (C > 1) {
     cluster.sync();
@@ -1853,7 +1929,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     }
   }
   __syncthreads();
-  if (sh.moot) return;  // (uniform in the cluster; no distributed access follows)
+  {
+    // moot if any CTA saw an earlier rejection (the same OR in every CTA)
+    int m = 0;
+    for (int r = 0; r < C; ++r) m |= sh.g_m[r];
+    if (m) return;  // (uniform in the cluster; no distributed access follows)
+  }
   const RowAcc row_t = sh.row_t, row_d = sh.row_d;
   // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
   const bool bad_t = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
@@ -1864,105 +1945,88 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const VerifyParams 
     topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb, has_draft,
                     X, st, sd, row_t, row_d);
 
-  // ---- decision and publication (rank 0, one thread) ----
+  // ---- verdict (every CTA), publication (rank 0, one thread) ----
+  float dq[3];
+  if (tid == 0) judge<ES, TOPP>(P, sh, i, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d, dq);
+  __syncthreads();
+  const uint32_t eb_i = sh.eb;
+  const bool rej = sh.rej != 0;
+  // The draw this item owes on a sampled row: the resample at its own
+  // rejection, or the bonus at k_b.  It is made now, while the item's rows
+  // may still be in L2; it goes unused if an earlier position turns out
+  // rejected, and is skipped if one already was when this item published.
+  const bool cand = !greedy && eb_i == 0u && (rej || i == kb);
   if (rank == 0 && tid == 0) {
     int j1, e1_;
-    const int fin = decide<ES, TOPP>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
-                               &j1, &e1_);
-    if (C > 1) {
-      for (int r = 0; r < C; ++r) {
-        Shared* rs = cluster.map_shared_rank(&sh, r);
-        rs->fin = fin;
-        rs->fin_j = j1;
-        rs->fin_err = e1_;
+    bool moot_pub;
+    const int fin = publish<TOPP>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
+                                  eb_i, rej, dq, &j1, &e1_, &moot_pub);
+    if (fin) {  // this publication resolved the sequence's prefix, cut at j1
+      if (e1_) {
+        const uint32_t ebj = __ldcg(&P.stats[(size_t)b * (P.K + 1) + j1].errbits);
+        write_outputs(P, b, 0, -1, true);
+        atomicOr(P.flags, ebj);
+      } else if (greedy) {
+        const int a = j1 == i ? row_t.amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j1].argmax);
+        write_outputs(P, b, j1, a, false);
+      } else {
+        prefix_resolved(P, b, j1);
       }
-    } else {
-      sh.fin = fin;
-      sh.fin_j = j1;
-      sh.fin_err = e1_;
+    }
+    if (cand) {
+      int draw = moot_pub ? 0 : 1;
+      if (draw && !(sh.uK >= 0.f && sh.uK < 1.f)) {
+        draw_ready(P, b, i, kb, kYBad);
+        draw = 0;
+      }
+      for (int r = 0; r < C; ++r) *remote(cluster, C, &sh.fin, r) = draw;
     }
   }
-  if (C > 1) cluster.sync();
-  else __syncthreads();
+  if (!cand) return;  // (uniform in the cluster: no distributed access follows)
+  csync(cluster, C);
   if (!sh.fin) return;
 
-  // ======================= finisher =======================
-  const int j = sh.fin_j;
-  if (sh.fin_err) {
-    if (rank == 0 && tid == 0) {
-      const uint32_t eb = __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].errbits);
-      write_outputs(P, b, 0, -1, true);
-      atomicOr(P.flags, eb);
-    }
-    return;
-  }
-  if (greedy) {
-    if (rank == 0 && tid == 0) {
-      const int a = j == i ? row_t.amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j].argmax);
-      write_outputs(P, b, j, a, false);
-    }
-    return;
-  }
-  const float uK = P.unif[(size_t)b * (P.K + 1) + P.K];
-  if (!(uK >= 0.f && uK < 1.f)) {
-    if (rank == 0 && tid == 0) {
-      write_outputs(P, b, 0, -1, true);
-      atomicOr(P.flags, SV_FLAG_BAD_UNIFORM);
-    }
-    return;
-  }
-  float Rt = row_t.R, Rd = row_d.R;
+  // ======================= this item's draw =======================
+  const float uK = sh.uK;
   DF S_t = row_t.s, S_d = row_d.s;
   uint32_t kt = 0u, kd = 0u;
   int nkt = 0x7fffffff, cntt = 0, nkd = 0x7fffffff, cntd = 0;
-  if (j != i) {
-    const ItemStats* sj = P.stats + (size_t)b * (P.K + 1) + j;
-    Rt = __ldcg(&sj->R_t);
-    Rd = __ldcg(&sj->R_d);
-    S_t = DF{__ldcg(&sj->st_hi), __ldcg(&sj->st_lo)};
-    S_d = DF{__ldcg(&sj->sd_hi), __ldcg(&sj->sd_lo)};
-    if (TOPP) {  // kept masses and cuts
-      S_t = DF{__ldcg(&sj->et_hi), __ldcg(&sj->et_lo)};
-      kt = __ldcg(&sj->key_t);
-      nkt = __ldcg(&sj->nk_t);
-      cntt = __ldcg(&sj->cnt_t);
-      if (j < kb) {
-        S_d = DF{__ldcg(&sj->ed_hi), __ldcg(&sj->ed_lo)};
-        kd = __ldcg(&sj->key_d);
-        nkd = __ldcg(&sj->nk_d);
-        cntd = __ldcg(&sj->cnt_d);
-      }
-    }
-  } else if (TOPP) {
+  if (TOPP) {  // kept masses and cuts of this item's rows
     S_t = sh.ts[0].E;
     kt = sh.ts[0].kstar;
     nkt = sh.ts[0].nk;
     cntt = sh.ts[0].cstar;
-    if (j < kb) {
+    if (i < kb) {
       S_d = sh.ts[1].E;
       kd = sh.ts[1].kstar;
       nkd = sh.ts[1].nk;
       cntd = sh.ts[1].cstar;
     }
   }
-  finish<ES, TOPP>(P, sh, vals, cluster, C, rank, b, kb, T, j, uK, e0, e1, Rt, Rd, S_t, S_d, kt, nkt,
-                   cntt, kd, nkd, cntd);
+  finish<ES, TOPP>(P, sh, vals, cluster, C, rank, b, kb, T, i, uK, e0, e1, row_t.R, row_d.R, S_t, S_d,
+                   kt, nkt, cntt, kd, nkd, cntd);
 }
 
-__global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, int B) {
+__global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, uint32_t* words2,
+                                   int B) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t == 0) *flags = 0u;
-  for (int b = t; b < B; b += gridDim.x * blockDim.x) words[b] = 0ull;
+  for (int b = t; b < B; b += gridDim.x * blockDim.x) {
+    words[b] = 0ull;
+    words2[b] = 0u;
+  }
 }
 
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
-size_t ws_layout(int B, int K, size_t* words_off, size_t* stats_off) {
+size_t ws_layout(int B, int K, size_t* words_off, size_t* words2_off, size_t* stats_off) {
   size_t off = 256;
   *words_off = off;
   off += ((size_t)B * 8 + 255) / 256 * 256;
+  *words2_off = off;
+  off += ((size_t)B * 4 + 255) / 256 * 256;
   *stats_off = off;
   off += (size_t)B * (K + 1) * sizeof(ItemStats);
   return (off + 255) / 256 * 256;
@@ -2044,8 +2108,8 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     return SV_ERR_SHAPE;
   }
   const bool topp = L.top_p < 1.0f;
-  size_t smem = (size_t)rounds * kThreads * sizeof(float);
-  if (smem < (size_t)kRingBytes) smem = kRingBytes;  // the row pass's ring
+  size_t smem = (size_t)rounds * kThreads * sizeof(float);  // the draw's unit sums
+  if (smem < (size_t)kRingBytes) smem = kRingBytes;          // the row pass's ring
   if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
@@ -2058,8 +2122,8 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
     }
     g_configured[gi] = 1;
   }
-  size_t words_off, stats_off;
-  ws_layout(L.B, L.K, &words_off, &stats_off);
+  size_t words_off, words2_off, stats_off;
+  ws_layout(L.B, L.K, &words_off, &words2_off, &stats_off);
   char* ws = static_cast<char*>(L.workspace);
   VerifyParams P;
   P.tgt = static_cast<const char*>(L.target);
@@ -2082,12 +2146,13 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   P.diag = L.diag;
   P.flags = reinterpret_cast<uint32_t*>(ws);
   P.words = reinterpret_cast<unsigned long long*>(ws + words_off);
+  P.words2 = reinterpret_cast<uint32_t*>(ws + words2_off);
   P.stats = reinterpret_cast<ItemStats*>(ws + stats_off);
   P.slice_len = slice;
   cudaStream_t stream = static_cast<cudaStream_t>(L.stream);
 
   const int ib = (L.B + 255) / 256;
-  verify_init_kernel<<<ib < 1 ? 1 : ib, 256, 0, stream>>>(P.flags, P.words, L.B);
+  verify_init_kernel<<<ib < 1 ? 1 : ib, 256, 0, stream>>>(P.flags, P.words, P.words2, L.B);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("init launch: ") + cudaGetErrorString(e);
@@ -2107,7 +2172,8 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
 
 size_t verify_workspace_bytes(int B, int K) {
   size_t a, b;
-  return ws_layout(B, K, &a, &b);
+  size_t c;
+  return ws_layout(B, K, &a, &c, &b);
 }
 
 // ---------------------------------------------------------------------------
