@@ -5,6 +5,7 @@
 // seq_len + n_accepted, and entries at or beyond it are stale.
 #include <cstdint>
 
+#include "sv_common.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -13,6 +14,7 @@ __global__ void kv_commit_kernel(int32_t* __restrict__ seq_lens,
                                  const int32_t* __restrict__ n_accepted,
                                  const int32_t* __restrict__ capacity, int B, int K,
                                  uint32_t* __restrict__ flags) {
+  pdl_wait();  // the launch may overlap the kernel that wrote n_accepted
   uint32_t f = 0;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
     const int n = n_accepted[b];
@@ -34,9 +36,18 @@ int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* c
                   int K, uint32_t* flags, void* stream, std::string* err) {
   int blocks = (B + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  kv_commit_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(seq_lens, n_accepted,
-                                                                          capacity, B, K, flags);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_commit_kernel, seq_lens, n_accepted, capacity, B, K, flags);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("kv_commit launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;

@@ -746,6 +746,12 @@ __device__ __forceinline__ unsigned long long or_acqrel64(unsigned long long* p,
   return old;
 }
 
+__device__ __forceinline__ unsigned long long or_acq64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acquire.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
 __device__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err);
 
 // A sampled sequence's outputs need its prefix resolved (bit 0 of its second
@@ -1674,12 +1680,17 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
                                     const RowAcc& row_t, const RowAcc& row_d, bool bad_t,
                                     bool bad_d, uint32_t errbits, bool reject, const float* dq,
                                     int* j_out, int* err_out, bool* moot_out) {
-  ItemStats s;
-  s.argmax = row_t.amax;
-  s.errbits = errbits;
-  s.y = -1;
-  s.pad = 0;
-  P.stats[(size_t)b * (P.K + 1) + i] = s;
+  // Only a position that can be the cut (an error, a rejection, or k_b) has
+  // statistics that another item reads; the others publish without release.
+  const bool cut_here = errbits != 0u || reject || i == kb;
+  if (cut_here) {
+    ItemStats s;
+    s.argmax = row_t.amax;
+    s.errbits = errbits;
+    s.y = -1;
+    s.pad = 0;
+    P.stats[(size_t)b * (P.K + 1) + i] = s;
+  }
   const bool sel = TOPP && !greedy && !bad_t && !bad_d;
   if (P.diag) {
     float* dg = P.diag + ((size_t)b * (P.K + 1) + i) * SV_DIAG_FIELDS;
@@ -1705,7 +1716,7 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
   else if (reject) bits |= 1ull << (kWordBits + i);
   // release: this item's statistics are visible before its bits; acquire:
   // the outputs then see the statistics every earlier item released
-  const unsigned long long old = or_acqrel64(P.words + b, bits);
+  const unsigned long long old = cut_here ? or_acqrel64(P.words + b, bits) : or_acq64(P.words + b, bits);
   *moot_out = word_moot(old, i);
   int j0, j1;
   bool e0_, e1_;
@@ -1728,14 +1739,18 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   extern __shared__ __align__(16) float vals[];  // cp.async ring; draw's unit sums; top-p histograms
   __shared__ Shared sh;
 
-  // the sequence word, read first so that its latency overlaps the
-  // parameter loads (thread 0 of every CTA)
-  const unsigned long long w0 = (tid == 0 && i > 0) ? __ldcg(P.words + b) : 0ull;
-
   // ---- per-row parameters (identical in every CTA of the cluster) ----
   const int kb = P.kpr ? P.kpr[b] : P.K;
   const int md = P.mode ? (int)P.mode[b] : 0;
   const float T = P.temp ? P.temp[b] : 1.0f;
+  // The launch may overlap the init kernel that clears the sequence words and
+  // the flag word: nothing of the workspace or the outputs is touched before
+  // this.  The kernel after this one may start launching meanwhile.
+  pdl_wait();
+  pdl_launch_dependents();
+  // the sequence word (thread 0 of every CTA); its latency overlaps the
+  // parameter checks
+  const unsigned long long w0 = (tid == 0 && i > 0) ? __ldcg(P.words + b) : 0ull;
   uint32_t seq_err = 0;
   if (kb < 0 || kb > P.K) seq_err |= SV_FLAG_BAD_K;
   else if (md != 0 && md != 1) seq_err |= SV_FLAG_BAD_MODE;
@@ -1890,18 +1905,23 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   if (has_draft) acc_finish_max<ES>(ad);
 
   // ---- combine: lanes -> warps (butterflies) -> CTA (warp 0) -> cluster ----
-  {
+  // (a CTA that skipped its rows has nothing to combine; skip is uniform in
+  // the CTA)
+  if (!skip) {
     const RowAcc wt = lanes_combine(at, true, greedy);
     const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
     if (lane == 0) {
       sh.w_t[warp] = wt;
       sh.w_d[warp] = wd;
     }
+    __syncthreads();
   }
-  __syncthreads();
   if (warp == 0) {
-    const RowAcc ct = lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy);
-    const RowAcc cd = lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false);
+    RowAcc ct = acc_init(), cd = acc_init();
+    if (!skip) {
+      ct = lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy);
+      cd = lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false);
+    }
     // this CTA's moot flag: the word it saw at the start, or at the last
     // step it looked (any thread)
     const int m = (sh.skip | sh.moot) ? 1 : 0;
@@ -1917,8 +1937,15 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
       sh.g_m[0] = m;
     }
   }
+  if (C > 1) cluster.sync();
+  else __syncthreads();
+  {
+    // moot if any CTA saw an earlier rejection (the same OR in every CTA)
+    int m = 0;
+    for (int r = 0; r < C; ++r) m |= sh.g_m[r];
+    if (m) return;  // (uniform in the cluster; no distributed access follows)
+  }
   if (C > 1) {
-    cluster.sync();
     if (warp == 0) {
       const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy);
       const RowAcc rd = lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false);
@@ -1927,13 +1954,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
         sh.row_d = rd;
       }
     }
-  }
-  __syncthreads();
-  {
-    // moot if any CTA saw an earlier rejection (the same OR in every CTA)
-    int m = 0;
-    for (int r = 0; r < C; ++r) m |= sh.g_m[r];
-    if (m) return;  // (uniform in the cluster; no distributed access follows)
+    __syncthreads();
   }
   const RowAcc row_t = sh.row_t, row_d = sh.row_d;
   // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
@@ -2009,6 +2030,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
 
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, uint32_t* words2,
                                    int B) {
+  pdl_launch_dependents();  // the verify kernel may start launching
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t == 0) *flags = 0u;
   for (int b = t; b < B; b += gridDim.x * blockDim.x) {
@@ -2054,13 +2076,16 @@ static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem,
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may overlap the init kernel before it (the kernel waits for it)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, verify_kernel<ES, TOPP>, P);
 }
 
