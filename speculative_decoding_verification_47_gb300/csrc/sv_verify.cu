@@ -45,6 +45,7 @@ namespace sv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCmax = 16;
+static_assert((kWarps & (kWarps - 1)) == 0 && kCmax <= 16, "butterfly widths are powers of two up to 16");
 constexpr int kLoadsInFlight = 2;                  // 16-byte units per row per thread per step
 constexpr int kRingStages = 2;                     // steps of units in flight ahead of the one reduced
 constexpr int kRingBytes = kRingStages * 2 * kLoadsInFlight * kThreads * 16;  // 32 KB
@@ -442,41 +443,64 @@ __device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, in
   }
 }
 
-// Combine row accumulators over the lanes of a warp (lanes with valid ==
-// false contribute nothing).  The butterfly leaves the same bits on every
-// lane, so every CTA that combines the same values gets the same result.
-__device__ __forceinline__ float warp_maxf(float v) {
+// Combine row accumulators over groups of W lanes of a warp (W a power of
+// two; lanes with valid == false contribute nothing): xor butterflies over
+// offsets W/2 .. 1.  Every lane of a group ends with the group's result, and
+// every CTA that combines the same values in the same lanes gets the same
+// bits.
+__device__ __forceinline__ float lanes_maxf(float v, int W) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = W >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-__device__ __forceinline__ float warp_nanmax(float v) {
+__device__ __forceinline__ float lanes_nanmax(float v, int W) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = nanmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = W >> 1; o > 0; o >>= 1) v = nanmax(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-__device__ __forceinline__ int warp_min(int v) {
+__device__ __forceinline__ int lanes_min(int v, int W) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = W >> 1; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-__device__ __forceinline__ RowAcc lanes_combine(RowAcc v, bool valid, bool greedy) {
+__device__ __forceinline__ DF lanes_dfsum(DF v, int W) {
+#pragma unroll
+  for (int o = W >> 1; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_min(int v) { return lanes_min(v, 32); }
+
+// Lane 0's accumulator on every lane of the warp.
+__device__ __forceinline__ RowAcc acc_bcast0(const RowAcc& v) {
+  RowAcc r;
+  r.mx = __shfl_sync(0xffffffffu, v.mx, 0);
+  r.R = __shfl_sync(0xffffffffu, v.R, 0);
+  r.s.hi = __shfl_sync(0xffffffffu, v.s.hi, 0);
+  r.s.lo = __shfl_sync(0xffffffffu, v.s.lo, 0);
+  r.amax = __shfl_sync(0xffffffffu, v.amax, 0);
+  r.pend = 0.f;
+  r.mx2 = kBf16x2NegInf;
+  return r;
+}
+
+__device__ __forceinline__ RowAcc lanes_combine(RowAcc v, bool valid, bool greedy, int W = 32) {
   if (!valid) v = acc_init();
-  const float m = warp_nanmax(v.mx);
+  const float m = lanes_nanmax(v.mx, W);
   if (greedy) {
     const int cand = (v.mx == m) ? v.amax : 0x7fffffff;
-    return RowAcc{m, -INFINITY, DF{0.f, 0.f}, warp_min(cand)};
+    return RowAcc{m, -INFINITY, DF{0.f, 0.f}, lanes_min(cand, W)};
   }
-  const float Rw = warp_maxf(v.R);
+  const float Rw = lanes_maxf(v.R, W);
   DF s = DF{0.f, 0.f};
   if (v.R > kRnone && Rw > kRnone) {
     const float p = pow2i(v.R - Rw);
     s = DF{v.s.hi * p, v.s.lo * p};
   }
-  s = df_warp_sum(s);
+  s = lanes_dfsum(s, W);
   return RowAcc{m, Rw, s, 0x7fffffff};
 }
 
@@ -1919,8 +1943,11 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   if (warp == 0) {
     RowAcc ct = acc_init(), cd = acc_init();
     if (!skip) {
-      ct = lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy);
-      cd = lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false);
+      // (the butterfly covers lanes 0..kWarps-1; lane 0's result goes to
+      // every lane, since lane q sends it to CTA q below)
+      ct = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy, kWarps));
+      if (has_draft)
+        cd = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false, kWarps));
     }
     // this CTA's moot flag: the word it saw at the start, or at the last
     // step it looked (any thread)
@@ -1947,8 +1974,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   }
   if (C > 1) {
     if (warp == 0) {
-      const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy);
-      const RowAcc rd = lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false);
+      const int W = C <= 2 ? 2 : C <= 4 ? 4 : C <= 8 ? 8 : 16;  // lanes of the butterfly
+      const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy, W);
+      const RowAcc rd = has_draft ? lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false, W)
+                                  : acc_init();
       if (lane == 0) {
         sh.row_t = rt;
         sh.row_d = rd;
