@@ -722,6 +722,7 @@ struct Shared {
   int owner, rsel;
   int x;
   float u_i, zt_x, zd_x, uK;
+  float dq[3];  // p'(x), q'(x) and their ratio, for the diagnostics
   uint32_t eb;  // the item's verdict: error bits, rejection
   int rej;
 };
@@ -1275,7 +1276,7 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
 template <int ES>
 __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsigned char* hist,
                                          cg::cluster_group& cluster, int C, int b, int i, int kb,
-                                         bool two, const Expo& X, const RowSlice<ES>& st,
+                                         bool two, const Expo X, const RowSlice<ES>& st,
                                          const RowSlice<ES>& sd, const RowAcc& row_t,
                                          const RowAcc& row_d) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1351,17 +1352,19 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
       hc[kSlotAbove + 1] = __float_as_uint(a.lo);
     }
     csync(cluster, C);  // every CTA's histograms are complete
-    uint32_t w0[8], w1[8], lt0 = 0, lt1 = 0;
-    DF A0{0.f, 0.f}, A1{0.f, 0.f};
-    if (a0) sel_reduce(cluster, C, hist, c0, w0, &lt0, &A0);
-    if (a1) sel_reduce(cluster, C, h1, c1, w1, &lt1, &A1);
-    if (tid == 0) {  // exact mass above each window
-      if (a0) sh.ts[0].A = A0;
-      if (a1) sh.ts[1].A = A1;
+    // one row at a time: gather its totals, then resolve (only this CTA's
+    // state changes, so other CTAs may still be reading its histograms)
+#pragma unroll 1
+    for (int r = 0; r < 2; ++r) {
+      if (!(r ? a1 : a0)) continue;  // (uniform in the cluster)
+      uint32_t w[8], lt = 0;
+      DF A{0.f, 0.f};
+      sel_reduce(cluster, C, r ? h1 : hist, r ? c1 : c0, w, &lt, &A);
+      if (tid == 0) sh.ts[r].A = A;  // exact mass above the window
+      __syncthreads();
+      sel_resolve<ES>(sh, r, w, lt, X);
     }
-    csync(cluster, C);  // every CTA has read every histogram
-    if (a0) sel_resolve<ES>(sh, 0, w0, lt0, X);
-    if (a1) sel_resolve<ES>(sh, 1, w1, lt1, X);
+    csync(cluster, C);  // every CTA has read every histogram before they are cleared
   }
 }
 
@@ -1644,7 +1647,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
 // ratio for the diagnostics.
 template <int ES, bool TOPP>
 __device__ __noinline__ void judge(const VerifyParams& P, Shared& sh, int i, int kb, bool greedy,
-                                   bool has_draft, const Expo& X, const RowAcc& row_t,
+                                   bool has_draft, const Expo X, const RowAcc& row_t,
                                    const RowAcc& row_d, bool bad_t, bool bad_d, float* dq) {
   const int x = sh.x;
   const float u_i = sh.u_i, zt_x = sh.zt_x, zd_x = sh.zd_x;
@@ -1700,7 +1703,7 @@ __device__ __noinline__ void judge(const VerifyParams& P, Shared& sh, int i, int
 // earlier position had already been rejected or failed.
 template <bool TOPP>
 __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, int b, int kb,
-                                    bool greedy, bool has_draft, const Expo& X,
+                                    bool greedy, bool has_draft, const Expo X,
                                     const RowAcc& row_t, const RowAcc& row_d, bool bad_t,
                                     bool bad_d, uint32_t errbits, bool reject, const float* dq,
                                     int* j_out, int* err_out, bool* moot_out) {
@@ -1993,11 +1996,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
                                    !(row_d.R > kRnone && row_d.R < INFINITY));
   if (TOPP && !greedy && !bad_t && !bad_d)
     topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb, has_draft,
-                    X, st, sd, row_t, row_d);
+                    X, st, sd, sh.row_t, sh.row_d);
 
   // ---- verdict (every CTA), publication (rank 0, one thread) ----
-  float dq[3];
-  if (tid == 0) judge<ES, TOPP>(P, sh, i, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d, dq);
+  if (tid == 0) judge<ES, TOPP>(P, sh, i, kb, greedy, has_draft, X, sh.row_t, sh.row_d, bad_t, bad_d, sh.dq);
   __syncthreads();
   const uint32_t eb_i = sh.eb;
   const bool rej = sh.rej != 0;
@@ -2009,8 +2011,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   if (rank == 0 && tid == 0) {
     int j1, e1_;
     bool moot_pub;
-    const int fin = publish<TOPP>(P, sh, i, b, kb, greedy, has_draft, X, row_t, row_d, bad_t, bad_d,
-                                  eb_i, rej, dq, &j1, &e1_, &moot_pub);
+    const int fin = publish<TOPP>(P, sh, i, b, kb, greedy, has_draft, X, sh.row_t, sh.row_d, bad_t,
+                                  bad_d, eb_i, rej, sh.dq, &j1, &e1_, &moot_pub);
     if (fin) {  // this publication resolved the sequence's prefix, cut at j1
       if (e1_) {
         const uint32_t ebj = __ldcg(&P.stats[(size_t)b * (P.K + 1) + j1].errbits);
