@@ -672,7 +672,8 @@ constexpr int kSlotLt = kNB;         // count pass: tokens of key kx before the 
 constexpr int kSlotAbove = kNB + 2;  // count pass: double-float mass above the window
 constexpr int kHistRowBytes = 8448;  // >= (kNB + 4) * 4
 constexpr int kHistBytes = 2 * kHistRowBytes;
-constexpr int kStageBytes = kThreads * kLoadsInFlight * 16;  // each thread's units in flight
+constexpr int kSelLoads = 4;  // units per thread per step of a selection pass
+constexpr int kStageBytes = kThreads * kSelLoads * 16;  // each thread's units of a step
 constexpr int kSelSmemBytes = kHistBytes + kStageBytes;
 constexpr int kMaxSelPasses = 12;
 
@@ -996,23 +997,23 @@ __device__ __noinline__ uint32_t sel_stream(const TopSel* tp, unsigned char* h, 
                                             const RowSlice<ES> rs, int x, float chi, float clo,
                                             DF* above) {
   constexpr int EPU = 16 / ES;
-  static_assert(kLoadsInFlight * EPU <= 32, "one 32-bit mask for the units in flight");
+  static_assert(kSelLoads * EPU <= 32, "one 32-bit mask for the units in flight");
   const SelP p = sel_params(*tp, ES);
   const Expo X{chi, clo};
   const int lane = threadIdx.x & 31;
-  uint4* mine = stage + threadIdx.x * kLoadsInFlight;
-  const unsigned char* wstage = reinterpret_cast<const unsigned char*>(stage + (threadIdx.x - lane) * kLoadsInFlight);
+  uint4* mine = stage + threadIdx.x * kSelLoads;
+  const unsigned char* wstage = reinterpret_cast<const unsigned char*>(stage + (threadIdx.x - lane) * kSelLoads);
   const int NU = rs.n_units, b0 = rs.ub0(), b1 = rs.ub1();
   uint32_t lt = 0;
   DF ab = *above;
   // (every lane runs the same number of steps: the shuffles below need all 32)
-  const int steps = (NU + kThreads * kLoadsInFlight - 1) / (kThreads * kLoadsInFlight);
+  const int steps = (NU + kThreads * kSelLoads - 1) / (kThreads * kSelLoads);
   for (int it = 0; it < steps; ++it) {
-    const int u0 = threadIdx.x + it * kThreads * kLoadsInFlight;
-    uint4 v[kLoadsInFlight];
+    const int u0 = threadIdx.x + it * kThreads * kSelLoads;
+    uint4 v[kSelLoads];
     uint32_t mall = 0;
 #pragma unroll
-    for (int k = 0; k < kLoadsInFlight; ++k) {
+    for (int k = 0; k < kSelLoads; ++k) {
       const int u = u0 + k * kThreads;
       if (u >= b0 && u < b1) {
         v[k] = ldg_unit(rs, u);
@@ -1025,7 +1026,7 @@ __device__ __noinline__ uint32_t sel_stream(const TopSel* tp, unsigned char* h, 
       }
     }
 #pragma unroll
-    for (int k = 0; k < kLoadsInFlight; ++k) {
+    for (int k = 0; k < kSelLoads; ++k) {
       const int u = u0 + k * kThreads;
       if (u >= b0 && u < b1) mall |= window_mask<ES>(v[k], p) << (k * EPU);
     }
@@ -1042,7 +1043,7 @@ __device__ __noinline__ uint32_t sel_stream(const TopSel* tp, unsigned char* h, 
     const int ex = inc - c;
     if (mall) {
 #pragma unroll
-      for (int k = 0; k < kLoadsInFlight; ++k) mine[k] = v[k];
+      for (int k = 0; k < kSelLoads; ++k) mine[k] = v[k];
     }
     __syncwarp();
     for (int base = 0; base < total; base += 32) {
@@ -1059,7 +1060,7 @@ __device__ __noinline__ uint32_t sel_stream(const TopSel* tp, unsigned char* h, 
       if (q < total) {
         const int bit = (int)__fns(mL, 0u, q - exL + 1);
         const int k = bit / EPU, j = bit % EPU;
-        const unsigned char* src = wstage + (size_t)L * kLoadsInFlight * 16 + bit * ES;
+        const unsigned char* src = wstage + (size_t)L * kSelLoads * 16 + bit * ES;
         const uint32_t bits = ES == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(src)
                                       : *reinterpret_cast<const uint32_t*>(src);
         const int eb = rs.ebase0 + (u0 - lane + L + k * kThreads) * EPU;
