@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint16_t* _
                                                                float eps, uint16_t* __restrict__ y,
                                                                int H, uint32_t* flags) {
   __shared__ float part[kNormThreads / 32];
+  pdl_launch_dependents();  // the GEMM may start its set-up meanwhile
   const int m = blockIdx.x, tid = threadIdx.x;
   if (m == 0 && tid == 0) *flags = 0u;
   const uint16_t* hr = h + (size_t)m * H;
@@ -247,6 +248,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // The launch may overlap the RMSNorm kernel before it (programmatic stream
+  // serialization): its set-up above runs meanwhile; the normalised rows, the
+  // flag word and the output are touched only after that kernel completed.
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer: one stage counter across all tiles ----
@@ -513,8 +518,12 @@ static cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int* grid_out
   if (act <= 0) act = num_sms() / CM;
   const int clusters = tiles < act ? tiles : act;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cluster_cfg(&cfg, attr, clusters * CM, CM, st);
+  // the set-up (barriers, TMEM, tensor maps) overlaps the RMSNorm kernel
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   *grid_out = clusters * CM;
   return cudaLaunchKernelEx(&cfg, lmhead_gemm_kernel<BNT, CM>, g.a, g.b, g.out, g.out_f32, g.M, g.N, g.K,
                             g.flags);
