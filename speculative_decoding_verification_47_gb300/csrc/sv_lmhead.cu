@@ -150,10 +150,30 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint16_t* _
   const int m = blockIdx.x, tid = threadIdx.x;
   if (m == 0 && tid == 0) *flags = 0u;
   const uint16_t* hr = h + (size_t)m * H;
+  uint16_t* yr = y + (size_t)m * H;
+  // the row's first kNormKeep * kNormThreads * 8 elements stay in registers
+  // between the sum of squares and the scaling (no second read)
+  constexpr int kNormKeep = 2;
+  uint4 keep[kNormKeep];
   float ss = 0.f;
-  for (int k = tid * 8; k < H; k += kNormThreads * 8) {
+#pragma unroll
+  for (int it = 0; it < kNormKeep; ++it) {
+    const int k = (it * kNormThreads + tid) * 8;
+    keep[it] = k < H ? *reinterpret_cast<const uint4*>(hr + k) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int k = (kNormKeep * kNormThreads + tid) * 8; k < H; k += kNormThreads * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(hr + k);
     const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(q[j]), b = bf16_hi(q[j]);
+      ss = __fmaf_rn(a, a, ss);
+      ss = __fmaf_rn(b, b, ss);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kNormKeep; ++it) {
+    const uint32_t q[4] = {keep[it].x, keep[it].y, keep[it].z, keep[it].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float a = bf16_lo(q[j]), b = bf16_hi(q[j]);
@@ -169,18 +189,33 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint16_t* _
 #pragma unroll
   for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
   const float r = rsqrtf(tot / (float)H + eps);
-  uint16_t* yr = y + (size_t)m * H;
-  for (int k = tid * 8; k < H; k += kNormThreads * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(hr + k);
+  const bool w16 = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;  // (the weight needs only 2-byte alignment)
+  auto scale = [&](const uint4& v, int k) {
+    uint32_t wq[4];
+    if (w16) {
+      const uint4 wv = *reinterpret_cast<const uint4*>(w + k);
+      wq[0] = wv.x;
+      wq[1] = wv.y;
+      wq[2] = wv.z;
+      wq[3] = wv.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wq[j] = (uint32_t)w[k + 2 * j] | ((uint32_t)w[k + 2 * j + 1] << 16);
+    }
     const uint32_t q[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float w0 = bf16_lo((uint32_t)w[k + 2 * j]), w1 = bf16_lo((uint32_t)w[k + 2 * j + 1]);
-      o[j] = pack_bf16x2(bf16_lo(q[j]) * r * w0, bf16_hi(q[j]) * r * w1);
-    }
+    for (int j = 0; j < 4; ++j)
+      o[j] = pack_bf16x2(bf16_lo(q[j]) * r * bf16_lo(wq[j]), bf16_hi(q[j]) * r * bf16_hi(wq[j]));
     *reinterpret_cast<uint4*>(yr + k) = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+#pragma unroll
+  for (int it = 0; it < kNormKeep; ++it) {
+    const int k = (it * kNormThreads + tid) * 8;
+    if (k < H) scale(keep[it], k);
   }
+  for (int k = (kNormKeep * kNormThreads + tid) * 8; k < H; k += kNormThreads * 8)
+    scale(*reinterpret_cast<const uint4*>(hr + k), k);
 }
 
 // ---------------------------------------------------------------------------

@@ -143,3 +143,22 @@ def test_c4_layer_skip_draft_then_verify():
     g = vh.run_gpu(w, dev=dev, strides=(0, 0, (K + 1) * V, V))
     dec, dis = vh.compare(w, g, vh.run_oracle(w))
     assert dec > B
+
+
+def test_lmhead_norm_weight_two_byte_aligned():
+    """The RMSNorm weight needs only 2-byte alignment: a weight vector that
+    starts one element into its buffer gives the same bits as an aligned one."""
+    import torch
+    x = wl.lmhead_inputs(M=130, H=512, V=272, seed=21)
+    a, _ = _run(x, sb.SV_F32)
+    dh = torch.from_numpy(x.hidden.view(np.int16)).cuda()
+    buf = torch.zeros(x.H + 8, dtype=torch.int16, device="cuda")
+    buf[1:1 + x.H] = torch.from_numpy(x.norm_w.view(np.int16)).cuda()
+    dw = buf[1:1 + x.H]
+    assert dw.data_ptr() % 16 != 0
+    dW = torch.from_numpy(x.W.view(np.int16)).cuda()
+    out = torch.full((x.M, x.V), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(sb.sv_lmhead_workspace_size(x.M, x.H), dtype=torch.uint8, device="cuda")
+    sb.sv_lmhead_rmsnorm(dh, dw, x.eps, dW, out, sb.SV_F32, x.M, x.H, x.V, ws, ws.numel())
+    assert sb.sv_read_device_flags(ws) == 0
+    np.testing.assert_array_equal(a.cpu().numpy(), out.cpu().numpy())
