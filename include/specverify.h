@@ -200,6 +200,39 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sv_draft_sample - the draft side of a round: draw each sequence's k_b draft
+ * tokens from its rows of draft logits [FS §3.2; SSD §3.2, §4.2].  Token i of
+ * sequence b comes from row (b, i) with the processing sv_spec_verify applies
+ * to its rows: the temperature softmax, top-p truncation with renormalisation
+ * when top_p < 1, and the inverse CDF in index order with the uniform
+ * uniforms[b*K + i] (the smallest v whose inclusive prefix of p' exceeds
+ * u times the total); a greedy row (mode 1) takes the argmax, lowest index on
+ * ties.  Rows are independent, so the call serves both a whole block of k
+ * rows and one row per draft step (K = 1).
+ *   draft_logits  device [B][K][V] of dtype; element strides per sequence and
+ *                 per position as for sv_spec_verify (0 = dense).
+ *   k_per_row     device int32 [B] in [0, K], or NULL (= K).
+ *   temperature   device float32 [B] (> 0 for sampled rows), or NULL (= 1).
+ *   top_p         in (0, 1].
+ *   uniforms      device float32 [B][K] in [0, 1).
+ *   mode          device uint8 [B] (0 sampled, 1 greedy), or NULL (= 0).
+ *   out_tokens    device int32 [B][K]: the tokens; -1 at positions i >= k_b.
+ *   workspace     device, >= sv_draft_sample_workspace_size() bytes, 256-byte
+ *                 aligned; its first four bytes are the device flag word.
+ * Per-position errors write -1 there and set SV_FLAG_NONFINITE (NaN, +inf or
+ * an all -inf row) or SV_FLAG_BAD_UNIFORM; a bad k_b, mode or temperature
+ * writes -1 at every position of the sequence and sets SV_FLAG_BAD_K /
+ * _BAD_MODE / _BAD_TEMPERATURE.  Host-side argument errors return before any
+ * launch.
+ */
+size_t sv_draft_sample_workspace_size(void);
+sv_status sv_draft_sample(const void* draft_logits, int64_t seq_stride, int64_t pos_stride,
+                          sv_dtype dtype, int B, int K, int V, const int32_t* k_per_row,
+                          const float* temperature, float top_p, const float* uniforms,
+                          const uint8_t* mode, int32_t* out_tokens, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace sv_lmhead_rmsnorm needs for M rows of width H
  * (the normalised, weighted bf16 copy of the hidden states); 0 if out of range. */
 size_t sv_lmhead_workspace_size(int M, int H);

@@ -95,6 +95,11 @@ def lib() -> ctypes.CDLL:
         L.sv_lmhead_rmsnorm.restype = _i32
         L.sv_lmhead_rmsnorm.argtypes = [_vp, _vp, _f32, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
                                         _sz, _vp]
+        L.sv_draft_sample_workspace_size.restype = _sz
+        L.sv_draft_sample_workspace_size.argtypes = []
+        L.sv_draft_sample.restype = _i32
+        L.sv_draft_sample.argtypes = [_vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _f32, _vp,
+                                      _vp, _vp, _vp, _sz, _vp]
         L.sv_read_device_flags.restype = _i32
         L.sv_read_device_flags.argtypes = [_vp, _c.POINTER(_c.c_uint32), _vp]
         L.sv_last_error.restype = _c.c_char_p
@@ -171,6 +176,18 @@ def sv_lmhead_rmsnorm(hidden, norm_w, eps, W, logits, out_dtype, M, H, V, worksp
     _check(lib().sv_lmhead_rmsnorm(_ptr(hidden), _ptr(norm_w), float(eps), _ptr(W), _ptr(logits),
                                    out_dtype, M, H, V, _ptr(workspace), workspace_bytes,
                                    _stream(stream)))
+
+
+def sv_draft_sample_workspace_size() -> int:
+    return lib().sv_draft_sample_workspace_size()
+
+
+def sv_draft_sample(draft_logits, seq_stride, pos_stride, dtype, B, K, V, k_per_row, temperature,
+                    top_p, uniforms, mode, out_tokens, workspace, workspace_bytes, stream=None):
+    _check(lib().sv_draft_sample(
+        _ptr(draft_logits), seq_stride, pos_stride, dtype, B, K, V, _ptr(k_per_row),
+        _ptr(temperature), float(top_p), _ptr(uniforms), _ptr(mode), _ptr(out_tokens),
+        _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def sv_read_device_flags(workspace, stream=None) -> int:

@@ -164,6 +164,52 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
   return SV_OK;
 }
 
+size_t sv_draft_sample_workspace_size(void) { return 256; }
+
+sv_status sv_draft_sample(const void* draft_logits, int64_t seq_stride, int64_t pos_stride,
+                          sv_dtype dtype, int B, int K, int V, const int32_t* k_per_row,
+                          const float* temperature, float top_p, const float* uniforms,
+                          const uint8_t* mode, int32_t* out_tokens, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
+  if (B < 1 || K < 1 || V < 1 || (long long)B * K > 0x7fffffffLL / 16)
+    return fail(SV_ERR_SHAPE, "need B >= 1, K >= 1, V >= 1");
+  if (!draft_logits || !uniforms || !out_tokens)
+    return fail(SV_ERR_ARG, "draft_logits, uniforms and out_tokens are required");
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(SV_ERR_ARG, "top_p must be in (0, 1]");
+  const int es = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(draft_logits, es)) return fail(SV_ERR_ARG, "logits must be aligned to their element size");
+  const long long Vl = V;
+  const long long ss = seq_stride ? seq_stride : (long long)K * Vl;
+  const long long ps = pos_stride ? pos_stride : Vl;
+  if (ss < 0 || ps < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
+  if (ps < Vl && K > 1) return fail(SV_ERR_SHAPE, "position stride is smaller than V");
+  if (!workspace || !aligned(workspace, 256))
+    return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+  if (workspace_bytes < sv_draft_sample_workspace_size())
+    return fail(SV_ERR_WORKSPACE, "workspace smaller than sv_draft_sample_workspace_size()");
+  sv::SampleLaunch L;
+  L.logits = draft_logits;
+  L.l_seq = ss;
+  L.l_pos = ps;
+  L.dtype = dtype;
+  L.B = B;
+  L.K = K;
+  L.V = V;
+  L.kpr = k_per_row;
+  L.temp = temperature;
+  L.top_p = top_p;
+  L.unif = uniforms;
+  L.mode = mode;
+  L.out = out_tokens;
+  L.workspace = workspace;
+  L.stream = stream;
+  std::string err;
+  const int s = sv::sample_launch(L, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
 sv_status sv_lmhead_rmsnorm(const void* hidden, const void* norm_w, float eps, const void* W,
                             void* logits, sv_dtype out_dtype, int M, int H, int V,
                             void* workspace, size_t workspace_bytes, void* stream) {

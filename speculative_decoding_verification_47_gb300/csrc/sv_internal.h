@@ -31,6 +31,24 @@ struct VerifyLaunch {
 
 // Enqueue the verify step.  Returns an sv_status; fills *err on failure.
 int verify_launch(const VerifyLaunch& L, std::string* err);
+
+struct SampleLaunch {
+  const void* logits;
+  long long l_seq, l_pos;  // elements
+  sv_dtype dtype;
+  int B, K, V;
+  const int32_t* kpr;
+  const float* temp;
+  float top_p;
+  const float* unif;
+  const uint8_t* mode;
+  int32_t* out;
+  void* workspace;
+  void* stream;
+};
+
+// Enqueue the draft-side sampler.  Returns an sv_status; fills *err on failure.
+int sample_launch(const SampleLaunch& L, std::string* err);
 size_t verify_workspace_bytes(int B, int K);
 
 // Allocation-free verify: scratch in a fixed device array of this size

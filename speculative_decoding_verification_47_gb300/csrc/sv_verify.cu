@@ -1470,7 +1470,7 @@ __device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group&
 // owner of u*total, the round, the unit and the element.  The token is
 // stored for the sequence's outputs.
 // ---------------------------------------------------------------------------
-template <int ES, bool TOPP>
+template <int ES, bool TOPP, bool SAMPLE = false>
 __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals,
                                     cg::cluster_group& cluster, int C, int rank, int b, int kb,
                                     float T, int j, float uK, int e0, int e1, float Rt, float Rd,
@@ -1639,7 +1639,8 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
     }
   }
   if (y < 0) y = ylast;
-  draw_ready(P, b, j, kb, y);
+  if (SAMPLE) P.out[(size_t)b * P.K + j] = y;  // a draft token: written at once
+  else draw_ready(P, b, j, kb, y);
 }
 
 // Verdict of one item: its error bits and whether x_i is rejected.  Every
@@ -1755,12 +1756,191 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
   return (!was && now) ? 1 : 0;
 }
 
+// Streams this CTA's slices of both rows through the per-thread cp.async ring
+// and reduces them into at / ad (row pass of a1 and a3).  With MOOT, every
+// other step each thread looks at the sequence word and stops reading once
+// an earlier position of the sequence is rejected (it then sets sh.moot).
+template <int ES, bool MOOT>
+__device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh, float* vals,
+                                              const RowSlice<ES>& st, const RowSlice<ES>& sd,
+                                              bool has_draft, bool greedy, bool skip, const Expo& X,
+                                              int b, int i, RowAcc& at, RowAcc& ad) {
+  const int tid = threadIdx.x;
+  {
+    // Each thread keeps kRingStages steps of its units in flight in its own
+    // shared-memory slots (slot k of stage s: ring[(s*2L + k)*kThreads + tid],
+    // k < L target, k >= L draft) and reduces the oldest step from there.
+    constexpr int L = kLoadsInFlight;
+    constexpr int kStep = kThreads * L;
+    uint4* ring = reinterpret_cast<uint4*>(vals);
+    const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
+    const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
+    const int nsteps = (!skip && NU > tid) ? (NU - tid + kStep - 1) / kStep : 0;
+    // Interior steps (every unit of the step inside the aligned bodies of
+    // both rows) take a path without per-unit bounds checks.
+    const int in0 = has_draft ? max(tb0, db0) : tb0, in1 = has_draft ? min(tb1, db1) : tb1;
+    const char* gt = reinterpret_cast<const char*>(st.base16) + 16 * (size_t)tid;
+    const char* gd = reinterpret_cast<const char*>(sd.base16) + 16 * (size_t)tid;
+    auto interior = [&](int u0) { return u0 >= in0 && u0 + (L - 1) * kThreads < in1; };
+    auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
+      const int u0 = tid + n * kStep;
+      uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      if (interior(u0)) {
+        const char* pt = gt + (size_t)n * kStep * 16;
+#pragma unroll
+        for (int k = 0; k < L; ++k) cp_async16(slot + k * kThreads, pt + (size_t)k * kThreads * 16);
+        if (has_draft) {
+          const char* pd = gd + (size_t)n * kStep * 16;
+#pragma unroll
+          for (int k = 0; k < L; ++k)
+            cp_async16(slot + (L + k) * kThreads, pd + (size_t)k * kThreads * 16);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+          const int u = u0 + k * kThreads;
+          if (u >= tb0 && u < tb1)
+            cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
+          if (has_draft && u >= db0 && u < db1)
+            cp_async16(slot + (L + k) * kThreads, reinterpret_cast<const void*>(sd.base16 + 16 * (uintptr_t)u));
+        }
+      }
+      cp_async_commit();
+    };
+    if (!skip) {
+#pragma unroll
+      for (int n = 0; n < kRingStages; ++n) issue(n);
+    }
+    // the sequence word, read two steps before it is looked at (no stall)
+    unsigned long long wseen = (MOOT && i > 0 && !skip) ? __ldcg(P.words + b) : 0ull;
+    for (int n = 0; n < nsteps; ++n) {
+      // every other step each thread looks again whether an earlier
+      // position has been rejected meanwhile; if so it stops reading (the
+      // item is then moot, and the cluster drops it after the combine).  A
+      // plain per-thread load: the lanes of a warp may leave this loop at
+      // different steps, so no warp-synchronous operation may sit in it.
+      if (MOOT && i > 0 && (n & 1)) {
+        if (word_moot(wseen, i)) {
+          sh.moot = 1;  // (a plain store: read after the barriers below)
+          break;
+        }
+        wseen = __ldcg(P.words + b);
+      }
+      cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
+      const int u0 = tid + n * kStep;
+      const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      // units are read from the slots one at a time (the ring, not registers,
+      // holds the step)
+      if (interior(u0)) {
+        constexpr int EPU = 16 / ES;
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+          const uint4 vt = slot[k * kThreads];
+          if (greedy)
+            greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
+          else
+            sampled_unit<ES>(at, vt, X);
+        }
+        if (has_draft) {
+#pragma unroll
+          for (int k = 0; k < L; ++k) sampled_unit<ES>(ad, slot[(L + k) * kThreads], X);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+          const int u = u0 + k * kThreads;
+          const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
+          row_unit_v<ES>(at, st, u, tb0, tb1, vt, greedy, X);
+          if (has_draft) {
+            const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
+            row_unit_v<ES>(ad, sd, u, db0, db1, vd, false, X);
+          }
+        }
+      }
+      if (!greedy) acc_flush(at);
+      if (has_draft) acc_flush(ad);
+      issue(n + kRingStages);  // (the slots were consumed above)
+    }
+    cp_async_wait_all();
+  }
+  if (!greedy) acc_finish_max<ES>(at);
+  if (has_draft) acc_finish_max<ES>(ad);
+}
+
+// Combines the row accumulators: lanes, warps, then the CTAs of the cluster
+// (every CTA ends with the same bits in sh.row_t / sh.row_d).  Returns true,
+// uniformly in the cluster, if any CTA skipped or stopped its rows because an
+// earlier position of the sequence was rejected.
+__device__ __forceinline__ bool combine_rows(Shared& sh, cg::cluster_group& cluster, int C, int rank,
+                                             const RowAcc& at, const RowAcc& ad, bool greedy,
+                                             bool has_draft, bool skip) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // ---- combine: lanes -> warps (butterflies) -> CTA (warp 0) -> cluster ----
+  // (a CTA that skipped its rows has nothing to combine; skip is uniform in
+  // the CTA)
+  if (!skip) {
+    const RowAcc wt = lanes_combine(at, true, greedy);
+    const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
+    if (lane == 0) {
+      sh.w_t[warp] = wt;
+      sh.w_d[warp] = wd;
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    RowAcc ct = acc_init(), cd = acc_init();
+    if (!skip) {
+      // (the butterfly covers lanes 0..kWarps-1; lane 0's result goes to
+      // every lane, since lane q sends it to CTA q below)
+      ct = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy, kWarps));
+      if (has_draft)
+        cd = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false, kWarps));
+    }
+    // this CTA's moot flag: the word it saw at the start, or at the last
+    // step it looked (any thread)
+    const int m = (sh.skip | sh.moot) ? 1 : 0;
+    if (C > 1) {
+      if (lane < C) {
+        *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
+        *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
+        *cluster.map_shared_rank(&sh.g_m[rank], lane) = m;
+      }
+    } else if (lane == 0) {
+      sh.row_t = ct;
+      sh.row_d = cd;
+      sh.g_m[0] = m;
+    }
+  }
+  if (C > 1) cluster.sync();
+  else __syncthreads();
+  {
+    // moot if any CTA saw an earlier rejection (the same OR in every CTA)
+    int m = 0;
+    for (int r = 0; r < C; ++r) m |= sh.g_m[r];
+    if (m) return true;  // (uniform in the cluster; no distributed access follows)
+  }
+  if (C > 1) {
+    if (warp == 0) {
+      const int W = C <= 2 ? 2 : C <= 4 ? 4 : C <= 8 ? 8 : 16;  // lanes of the butterfly
+      const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy, W);
+      const RowAcc rd = has_draft ? lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false, W)
+                                  : acc_init();
+      if (lane == 0) {
+        sh.row_t = rt;
+        sh.row_d = rd;
+      }
+    }
+    __syncthreads();
+  }
+  return false;
+}
+
 template <int ES, bool TOPP>
 __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int item = blockIdx.x / C;
   const int i = item / P.B, b = item % P.B;
 
@@ -1832,163 +2012,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
     sh.zd_x = zd;
   }
   RowAcc at = acc_init(), ad = acc_init();
-  {
-    // Each thread keeps kRingStages steps of its units in flight in its own
-    // shared-memory slots (slot k of stage s: ring[(s*2L + k)*kThreads + tid],
-    // k < L target, k >= L draft) and reduces the oldest step from there.
-    constexpr int L = kLoadsInFlight;
-    constexpr int kStep = kThreads * L;
-    uint4* ring = reinterpret_cast<uint4*>(vals);
-    const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
-    const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
-    const int nsteps = (!skip && NU > tid) ? (NU - tid + kStep - 1) / kStep : 0;
-    // Interior steps (every unit of the step inside the aligned bodies of
-    // both rows) take a path without per-unit bounds checks.
-    const int in0 = has_draft ? max(tb0, db0) : tb0, in1 = has_draft ? min(tb1, db1) : tb1;
-    const char* gt = reinterpret_cast<const char*>(st.base16) + 16 * (size_t)tid;
-    const char* gd = reinterpret_cast<const char*>(sd.base16) + 16 * (size_t)tid;
-    auto interior = [&](int u0) { return u0 >= in0 && u0 + (L - 1) * kThreads < in1; };
-    auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
-      const int u0 = tid + n * kStep;
-      uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
-      if (interior(u0)) {
-        const char* pt = gt + (size_t)n * kStep * 16;
-#pragma unroll
-        for (int k = 0; k < L; ++k) cp_async16(slot + k * kThreads, pt + (size_t)k * kThreads * 16);
-        if (has_draft) {
-          const char* pd = gd + (size_t)n * kStep * 16;
-#pragma unroll
-          for (int k = 0; k < L; ++k)
-            cp_async16(slot + (L + k) * kThreads, pd + (size_t)k * kThreads * 16);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          const int u = u0 + k * kThreads;
-          if (u >= tb0 && u < tb1)
-            cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
-          if (has_draft && u >= db0 && u < db1)
-            cp_async16(slot + (L + k) * kThreads, reinterpret_cast<const void*>(sd.base16 + 16 * (uintptr_t)u));
-        }
-      }
-      cp_async_commit();
-    };
-    if (!skip) {
-#pragma unroll
-      for (int n = 0; n < kRingStages; ++n) issue(n);
-    }
-    // the sequence word, read two steps before it is looked at (no stall)
-    unsigned long long wseen = (i > 0 && !skip) ? __ldcg(P.words + b) : 0ull;
-    for (int n = 0; n < nsteps; ++n) {
-      // every other step each thread looks again whether an earlier
-      // position has been rejected meanwhile; if so it stops reading (the
-      // item is then moot, and the cluster drops it after the combine).  A
-      // plain per-thread load: the lanes of a warp may leave this loop at
-      // different steps, so no warp-synchronous operation may sit in it.
-      if (i > 0 && (n & 1)) {
-        if (word_moot(wseen, i)) {
-          sh.moot = 1;  // (a plain store: read after the barriers below)
-          break;
-        }
-        wseen = __ldcg(P.words + b);
-      }
-      cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
-      const int u0 = tid + n * kStep;
-      const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
-      // units are read from the slots one at a time (the ring, not registers,
-      // holds the step)
-      if (interior(u0)) {
-        constexpr int EPU = 16 / ES;
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          const uint4 vt = slot[k * kThreads];
-          if (greedy)
-            greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
-          else
-            sampled_unit<ES>(at, vt, X);
-        }
-        if (has_draft) {
-#pragma unroll
-          for (int k = 0; k < L; ++k) sampled_unit<ES>(ad, slot[(L + k) * kThreads], X);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          const int u = u0 + k * kThreads;
-          const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
-          row_unit_v<ES>(at, st, u, tb0, tb1, vt, greedy, X);
-          if (has_draft) {
-            const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
-            row_unit_v<ES>(ad, sd, u, db0, db1, vd, false, X);
-          }
-        }
-      }
-      if (!greedy) acc_flush(at);
-      if (has_draft) acc_flush(ad);
-      issue(n + kRingStages);  // (the slots were consumed above)
-    }
-    cp_async_wait_all();
-  }
-  if (!greedy) acc_finish_max<ES>(at);
-  if (has_draft) acc_finish_max<ES>(ad);
-
-  // ---- combine: lanes -> warps (butterflies) -> CTA (warp 0) -> cluster ----
-  // (a CTA that skipped its rows has nothing to combine; skip is uniform in
-  // the CTA)
-  if (!skip) {
-    const RowAcc wt = lanes_combine(at, true, greedy);
-    const RowAcc wd = has_draft ? lanes_combine(ad, true, false) : acc_init();
-    if (lane == 0) {
-      sh.w_t[warp] = wt;
-      sh.w_d[warp] = wd;
-    }
-    __syncthreads();
-  }
-  if (warp == 0) {
-    RowAcc ct = acc_init(), cd = acc_init();
-    if (!skip) {
-      // (the butterfly covers lanes 0..kWarps-1; lane 0's result goes to
-      // every lane, since lane q sends it to CTA q below)
-      ct = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_t[lane] : acc_init(), lane < kWarps, greedy, kWarps));
-      if (has_draft)
-        cd = acc_bcast0(lanes_combine(lane < kWarps ? sh.w_d[lane] : acc_init(), lane < kWarps, false, kWarps));
-    }
-    // this CTA's moot flag: the word it saw at the start, or at the last
-    // step it looked (any thread)
-    const int m = (sh.skip | sh.moot) ? 1 : 0;
-    if (C > 1) {
-      if (lane < C) {
-        *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
-        *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
-        *cluster.map_shared_rank(&sh.g_m[rank], lane) = m;
-      }
-    } else if (lane == 0) {
-      sh.row_t = ct;
-      sh.row_d = cd;
-      sh.g_m[0] = m;
-    }
-  }
-  if (C > 1) cluster.sync();
-  else __syncthreads();
-  {
-    // moot if any CTA saw an earlier rejection (the same OR in every CTA)
-    int m = 0;
-    for (int r = 0; r < C; ++r) m |= sh.g_m[r];
-    if (m) return;  // (uniform in the cluster; no distributed access follows)
-  }
-  if (C > 1) {
-    if (warp == 0) {
-      const int W = C <= 2 ? 2 : C <= 4 ? 4 : C <= 8 ? 8 : 16;  // lanes of the butterfly
-      const RowAcc rt = lanes_combine(lane < C ? sh.g_t[lane] : acc_init(), lane < C, greedy, W);
-      const RowAcc rd = has_draft ? lanes_combine(lane < C ? sh.g_d[lane] : acc_init(), lane < C, false, W)
-                                  : acc_init();
-      if (lane == 0) {
-        sh.row_t = rt;
-        sh.row_d = rd;
-      }
-    }
-    __syncthreads();
-  }
+  stream_slices<ES, true>(P, sh, vals, st, sd, has_draft, greedy, skip, X, b, i, at, ad);
+  if (combine_rows(sh, cluster, C, rank, at, ad, greedy, has_draft, skip)) return;  // (moot: uniform)
   const RowAcc row_t = sh.row_t, row_d = sh.row_d;
   // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
   const bool bad_t = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
@@ -2060,6 +2085,86 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
                    kt, nkt, cntt, kd, nkd, cntd);
 }
 
+// ---------------------------------------------------------------------------
+// Draft-side sampler: item (b, i), i < k_b, draws draft token i of sequence b
+// from its row of draft logits with the verify step's processing - the
+// temperature softmax, top-p truncation (a2) and the inverse CDF in index
+// order (a5's draw, with w = p') - or takes the argmax on a greedy row.
+// Items are independent: no sequence words, no early exit.  Position-major,
+// P.K positions per sequence; uniforms and outputs are [B][K].
+// ---------------------------------------------------------------------------
+template <int ES, bool TOPP>
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyParams P) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int tid = threadIdx.x;
+  const int item = blockIdx.x / C;
+  const int i = item / P.B, b = item % P.B;
+
+  extern __shared__ __align__(16) float vals[];  // cp.async ring; draw's unit sums; top-p histograms
+  __shared__ Shared sh;
+
+  const int kb = P.kpr ? P.kpr[b] : P.K;
+  const int md = P.mode ? (int)P.mode[b] : 0;
+  const float T = P.temp ? P.temp[b] : 1.0f;
+  pdl_wait();  // (the flag word is cleared by the kernel before this one)
+  pdl_launch_dependents();
+  int32_t* out = P.out + (size_t)b * P.K + i;
+  uint32_t seq_err = 0;
+  if (kb < 0 || kb > P.K) seq_err |= SV_FLAG_BAD_K;
+  else if (md != 0 && md != 1) seq_err |= SV_FLAG_BAD_MODE;
+  else if (md == 0 && !(T > 0.f && T < INFINITY)) seq_err |= SV_FLAG_BAD_TEMPERATURE;
+  if (seq_err || i >= kb) {  // padding, or a sequence with bad knobs
+    if (rank == 0 && tid == 0) {
+      *out = -1;
+      if (seq_err && i == 0) atomicOr(P.flags, seq_err);
+    }
+    return;
+  }
+  const bool greedy = md == 1;
+  const Expo X = greedy ? Expo{1.f, 1e-30f} : make_expo(T);
+  const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
+  RowSlice<ES> st;
+  st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
+  if (tid == 0) {
+    sh.skip = 0;
+    sh.moot = 0;
+  }
+  if (tid == 32) sh.uK = greedy ? 0.f : P.unif[(size_t)b * P.K + i];
+  __syncthreads();
+  RowAcc at = acc_init(), ad = acc_init();
+  stream_slices<ES, false>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad);
+  combine_rows(sh, cluster, C, rank, at, ad, greedy, false, false);  // (never moot here)
+  const RowAcc row_t = sh.row_t;
+  const bool bad = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
+                   (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
+  const float u = sh.uK;
+  // (every condition below is uniform in the cluster)
+  if (bad || greedy || !(u >= 0.f && u < 1.f)) {
+    if (rank == 0 && tid == 0) {
+      *out = (bad || !greedy) ? -1 : row_t.amax;
+      if (bad) atomicOr(P.flags, SV_FLAG_NONFINITE);
+      else if (!greedy) atomicOr(P.flags, SV_FLAG_BAD_UNIFORM);
+    }
+    return;
+  }
+  DF S_t = row_t.s;
+  uint32_t kt = 0u;
+  int nkt = 0x7fffffff, cntt = 0;
+  if (TOPP) {  // (kb = i: no draft token of this row enters the tie count)
+    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, i, false, X,
+                    st, st, sh.row_t, sh.row_d);
+    S_t = sh.ts[0].E;
+    kt = sh.ts[0].kstar;
+    nkt = sh.ts[0].nk;
+    cntt = sh.ts[0].cstar;
+  }
+  // j = k_b = i: the draw's weights are p' alone, as for a bonus token
+  finish<ES, TOPP, true>(P, sh, vals, cluster, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
+                         S_t, kt, nkt, cntt, 0u, 0x7fffffff, 0);
+}
+
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, uint32_t* words2,
                                    int B) {
   pdl_launch_dependents();  // the verify kernel may start launching
@@ -2087,20 +2192,20 @@ size_t ws_layout(int B, int K, size_t* words_off, size_t* words2_off, size_t* st
 }
 
 static int g_configured[4] = {0, 0, 0, 0};
+static int g_configured_sample[4] = {0, 0, 0, 0};
 
-template <int ES, bool TOPP>
+template <int ES, bool TOPP, bool SAMPLE = false>
 static cudaError_t configure() {
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto k = SAMPLE ? sample_kernel<ES, TOPP> : verify_kernel<ES, TOPP>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kMaxRounds * kThreads * (int)sizeof(float) > kRingBytes
                                            ? kMaxRounds * kThreads * (int)sizeof(float)
                                            : kRingBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(verify_kernel<ES, TOPP>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-template <int ES, bool TOPP>
+template <int ES, bool TOPP, bool SAMPLE = false>
 static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem, cudaStream_t stream) {
   VerifyParams P = P0;
   cudaLaunchConfig_t cfg = {};
@@ -2118,7 +2223,7 @@ static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<ES, TOPP>, P);
+  return cudaLaunchKernelEx(&cfg, SAMPLE ? sample_kernel<ES, TOPP> : verify_kernel<ES, TOPP>, P);
 }
 
 static int sm_count() {
@@ -2136,9 +2241,9 @@ static int sm_count() {
 // SM about three, but no slice under 32 KB of a row (narrower slices spend
 // more time in the per-item combine and decision than in streaming), and at
 // least wide enough that a slice fits kMaxRounds rounds; at most 16 CTAs.
-static void choose_geometry(int V, int ES, int B, int* C_out, int* slice_out) {
+static void choose_geometry(int V, int ES, int B, int* C_out, int* slice_out, int max_rounds = kMaxRounds) {
   const long long row_bytes = (long long)V * ES;
-  const long long max_slice = (long long)kMaxRounds * kThreads * 16 - 64;
+  const long long max_slice = (long long)max_rounds * kThreads * 16 - 64;
   int C = (3 * sm_count() + B - 1) / (B > 0 ? B : 1);
   const int cwide = (int)((row_bytes + 32767) / 32768);
   if (C > cwide) C = cwide;
@@ -2231,6 +2336,69 @@ size_t verify_workspace_bytes(int B, int K) {
   size_t a, b;
   size_t c;
   return ws_layout(B, K, &a, &c, &b);
+}
+
+int sample_launch(const SampleLaunch& L, std::string* err) {
+  const int ES = L.dtype == SV_BF16 ? 2 : 4;
+  // every item is independent: clusters as narrow as the slice limit allows
+  // (32 rounds, so the draw's unit sums fit the 32 KB the ring takes)
+  int C, slice;
+  choose_geometry(L.V, ES, L.B * L.K, &C, &slice, 32);
+  const long long units = ((long long)slice * ES + 30) / 16 + 1;
+  const long long rounds = (units + kThreads - 1) / kThreads;
+  if (rounds > kMaxRounds) {
+    *err = "vocabulary too large for the cluster slice layout";
+    return SV_ERR_SHAPE;
+  }
+  const bool topp = L.top_p < 1.0f;
+  size_t smem = (size_t)rounds * kThreads * sizeof(float);
+  if (smem < (size_t)kRingBytes) smem = kRingBytes;
+  if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
+  cudaError_t e;
+  const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
+  if (!g_configured_sample[gi]) {
+    e = ES == 2 ? (topp ? configure<2, true, true>() : configure<2, false, true>())
+                : (topp ? configure<4, true, true>() : configure<4, false, true>());
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return SV_ERR_CUDA;
+    }
+    g_configured_sample[gi] = 1;
+  }
+  VerifyParams P = {};
+  P.tgt = static_cast<const char*>(L.logits);
+  P.t_seq = L.l_seq * ES;
+  P.t_pos = L.l_pos * ES;
+  P.B = L.B;
+  P.K = L.K;
+  P.V = L.V;
+  P.kpr = L.kpr;
+  P.temp = L.temp;
+  P.top_p = L.top_p;
+  P.unif = L.unif;
+  P.mode = L.mode;
+  P.out = L.out;
+  P.flags = static_cast<uint32_t*>(L.workspace);
+  P.slice_len = slice;
+  cudaStream_t stream = static_cast<cudaStream_t>(L.stream);
+  verify_init_kernel<<<1, 256, 0, stream>>>(P.flags, nullptr, nullptr, 0);  // the flag word only
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *err = std::string("init launch: ") + cudaGetErrorString(e);
+    return SV_ERR_CUDA;
+  }
+  const int items = L.K * L.B;
+  if (items > 0) {
+    if (ES == 2)
+      e = topp ? launch<2, true, true>(P, C, items, smem, stream) : launch<2, false, true>(P, C, items, smem, stream);
+    else
+      e = topp ? launch<4, true, true>(P, C, items, smem, stream) : launch<4, false, true>(P, C, items, smem, stream);
+    if (e != cudaSuccess) {
+      *err = std::string("sample launch: ") + cudaGetErrorString(e);
+      return SV_ERR_CUDA;
+    }
+  }
+  return SV_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -107,3 +107,25 @@ def test_noalloc_host_checks(lib):
         sb.sv_spec_verify_noalloc(None, 0, 0, P, 0, 0, sb.SV_BF16, 4, 3, 100, P, None, None,
                                   1.0, P, None, P, P, None, 0)
     assert e.value.status == sb.SV_ERR_ARG
+
+
+def test_draft_sample_host_checks(lib):
+    assert "sv_draft_sample" in header_functions()
+    assert sb.sv_draft_sample_workspace_size() == 256
+
+    def call(**kw):
+        a = dict(logits=P, ss=0, ps=0, dtype=sb.SV_BF16, B=4, K=3, V=100, kpr=None, temp=None,
+                 top_p=1.0, unif=P, mode=None, out=P, ws=P, wsb=256)
+        a.update(kw)
+        sb.sv_draft_sample(a["logits"], a["ss"], a["ps"], a["dtype"], a["B"], a["K"], a["V"],
+                           a["kpr"], a["temp"], a["top_p"], a["unif"], a["mode"], a["out"],
+                           a["ws"], a["wsb"], 0)
+
+    for kw, status in [(dict(dtype=5), sb.SV_ERR_DTYPE), (dict(B=0), sb.SV_ERR_SHAPE),
+                       (dict(K=0), sb.SV_ERR_SHAPE), (dict(logits=None), sb.SV_ERR_ARG),
+                       (dict(unif=None), sb.SV_ERR_ARG), (dict(top_p=0.0), sb.SV_ERR_ARG),
+                       (dict(logits=P + 1), sb.SV_ERR_ARG), (dict(ps=50), sb.SV_ERR_SHAPE),
+                       (dict(ws=None), sb.SV_ERR_WORKSPACE), (dict(wsb=255), sb.SV_ERR_WORKSPACE)]:
+        with pytest.raises(sb.SVError) as e:
+            call(**kw)
+        assert e.value.status == status, kw
