@@ -44,6 +44,8 @@ WORKLOADS = {
     "c4": ("layer-skip step: hidden [512,4096] bf16 -> final RMSNorm (eps 1e-5) -> LM head "
            "W[4096,32000] bf16 for the draft and the target logits, then verify B=64, k=7, "
            "T=1, sampled; + kv_commit"),
+    "s2": ("draft-side sampler on the headline batch's draft rows: B=256, K=8, ragged "
+           "k_b~U{2..8}, V=128256 bf16 logits, T_b in {0.1,0.7,1.0}, one uniform per token"),
 }
 COPIES = 3
 
@@ -589,6 +591,162 @@ def run_gpu_c4(args):
         pg.destroy_process_group()
 
 
+def run_gpu_s2(args):
+    """The draft-side sampler over the headline batch's draft rows (k_b per
+    sequence, per-row temperature): one sv_draft_sample call per step."""
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from speculative_decoding_verification_47_gb300 import binding as sb
+    from speculative_decoding_verification_47_gb300 import build as bld
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    if pg is not None:
+        pg.barrier()
+    w = wl.config_by_name("c2")
+    B, K, V = w.B, w.K, w.V
+    unif = np.random.default_rng(5150).uniform(size=(B, K)).astype(np.float32)
+    dev = torch.device("cuda", local)
+    dr = torch.from_numpy(w.draft.view(np.int16))
+    drfs = [dr.to(dev) for _ in range(COPIES)]
+    kpr = torch.from_numpy(w.k_per_row).to(dev)
+    tmp = torch.from_numpy(w.temperature).to(dev)
+    uni = torch.from_numpy(unif).to(dev)
+    mode = torch.from_numpy(w.mode).to(dev)
+    out = torch.empty((B, K), dtype=torch.int32, device=dev)
+    wsb = sb.sv_draft_sample_workspace_size()
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tokens = int(w.k_per_row.sum())
+    row_bytes = V * 2
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import sample as osm
+        n = max(1, min(B, args.cpu_sample // 8))
+        t0 = time.perf_counter()
+        osm.sample_tokens(w.draft[:n], w.dtype, n, K, V, w.k_per_row[:n], w.temperature[:n], 1.0,
+                          unif[:n], w.mode[:n])
+        wall = time.perf_counter() - t0
+        cpu = {"value": int(w.k_per_row[:n].sum()) / wall, "unit": "tokens/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"the first {n} of the {B} sequences, float64 oracle, one core, wall {wall:.2f} s"}
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(max(args.steps, 1))]
+
+    def step(c, i=None):
+        if i is not None:
+            ev[i][0].record(stream)
+        sb.sv_draft_sample(drfs[c], 0, 0, sb.SV_BF16, B, K, V, kpr, tmp, 1.0, uni, mode, out, ws,
+                           wsb, stream)
+        if i is not None:
+            ev[i][1].record(stream)
+
+    for it in range(args.warmup):
+        step(it % COPIES)
+    torch.cuda.synchronize()
+    flags = sb.sv_read_device_flags(ws)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for it in range(args.steps):
+        step(it % COPIES, it)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clk = clocks.stop()
+    ms, total = reduce_timing(t_start.elapsed_time(t_end), tokens, pg, dev)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[:args.steps])
+    ms_step = ms / args.steps
+    value = total / (ms_step * 1e-3)
+    alg_bytes = tokens * row_bytes  # every sampled row read once
+    achieved = alg_bytes / (call_ms * 1e-3) / 1e9
+    peak, psrc = peaks()
+
+    e2e = None
+    if not args.no_e2e:
+        h_d = dr.pin_memory()
+        h_small = [torch.from_numpy(a).pin_memory() for a in (w.k_per_row, w.temperature, unif, w.mode)]
+        d_small = [kpr, tmp, uni, mode]
+        o_out = torch.empty((B, K), dtype=torch.int32).pin_memory()
+        steps_e2e = max(3, min(args.steps, 20))
+
+        def e2e_step():
+            drfs[0].copy_(h_d, non_blocking=True)
+            for d_, h_ in zip(d_small, h_small):
+                d_.copy_(h_, non_blocking=True)
+            step(0)
+            o_out.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b)
+        if pg is not None:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = h_d.numel() * 2 + sum(t_.numel() * t_.element_size() for t_ in h_small)
+        e2e = {"value": tokens * world / (ems / steps_e2e * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(o_out.numel() * 4),
+               "steps": steps_e2e}
+
+    line = {
+        "metric": "draft tokens sampled/s and sampler HBM GB/s (% of GB300 peak) at 1 GPU",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "input_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS["s2"], "name": "s2", "B": B, "K": K, "V": V,
+                   "tokens_per_step": tokens,
+                   "l2": f"{COPIES} rotating input copies ({COPIES * w.draft.nbytes / 1e9:.1f} GB) > 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "hbm": {"bytes_algorithmic_per_call": alg_bytes, "gbs_algorithmic": achieved,
+                "frac_of_peak": achieved / peak, "peak_gbs": peak, "peak_source": psrc},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_for("s2", args.traffic),
+                     "kernel": "sample_kernel<2,false>", "launch_ms": call_ms, "peak_source": psrc},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "device_flags": flags,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -607,6 +765,8 @@ def run_reference(args):
     from speculative_decoding_verification_47_gb300 import workloads as wl
     if args.workload == "c4":
         return run_reference_c4(args)
+    if args.workload == "s2":
+        return run_reference_s2(args)
     spec = wl.row_spec(args.workload, args.B)
     workers = min(16, len(os.sched_getaffinity(0)))
     for _ in range(args.warmup):
@@ -638,6 +798,54 @@ def run_reference(args):
                                    f"(evenly spaced), float64 oracle over {used} spawn workers"},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_s2(args):
+    """The sampler oracle on a few sequences of the headline batch per step,
+    their rows regenerated from the workload's per-sequence seeds."""
+    import numpy as np
+    from oracle import sample as osm
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    spec = wl.row_spec("c2", None)
+    unif = np.random.default_rng(5150).uniform(size=(spec.B, spec.K)).astype(np.float32)
+    n = max(1, min(spec.B, args.ref_sample // 8))
+    tot_tok, tot_wall = 0, 0.0
+    for it in range(args.warmup + args.steps):
+        seqs = [(it * n + j) % spec.B for j in range(n)]
+        rows = [(b,) + tuple(spec.sequence(b)) for b in seqs]
+        t0 = time.perf_counter()
+        tok = 0
+        for b, t, d, x, u in rows:
+            kb = int(spec.k_per_row[b])
+            osm.sample_tokens(np.asarray(d)[None], spec.dtype, 1, spec.K, spec.V, [kb],
+                              [spec.temperature[b]], 1.0, unif[b:b + 1], [spec.mode[b]])
+            tok += kb
+        wall = time.perf_counter() - t0
+        if it >= args.warmup:
+            tot_tok += tok
+            tot_wall += wall
+    value = tot_tok / tot_wall
+    line = {
+        "impl": "reference",
+        "metric": "draft tokens sampled/s and sampler HBM GB/s (% of GB300 peak) at 1 GPU",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": tot_wall / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS["s2"], "name": "s2", "B": spec.B, "K": spec.K, "V": spec.V,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {n} of the {spec.B} sequences, float64 oracle, one core"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -701,6 +909,8 @@ def main():
         run_reference(args)
     elif args.workload == "c4":
         run_gpu_c4(args)
+    elif args.workload == "s2":
+        run_gpu_s2(args)
     else:
         run_gpu(args)
 

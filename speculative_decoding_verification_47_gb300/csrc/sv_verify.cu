@@ -563,18 +563,9 @@ struct Weight {
 // Weight sum of one full unit (both rows hold the same elements in it).
 template <int ES>
 __device__ __forceinline__ float wsum_full(const uint4& vt, const uint4& vd, const Weight& W) {
-  if (W.p_only) {
-    const float nR = -W.Rt;
-    if (ES == 2) {
-      const float e0 = e2(bf16_lo(vt.x), W.x, nR), e1 = e2(bf16_hi(vt.x), W.x, nR);
-      const float f0 = e2(bf16_lo(vt.y), W.x, nR), f1 = e2(bf16_hi(vt.y), W.x, nR);
-      const float g0 = e2(bf16_lo(vt.z), W.x, nR), g1 = e2(bf16_hi(vt.z), W.x, nR);
-      const float h0 = e2(bf16_lo(vt.w), W.x, nR), h1 = e2(bf16_hi(vt.w), W.x, nR);
-      return ((e0 + e1) + (f0 + f1)) + ((g0 + g1) + (h0 + h1));
-    }
-    const float e0 = e2(__uint_as_float(vt.x), W.x, nR), e1 = e2(__uint_as_float(vt.y), W.x, nR);
-    const float f0 = e2(__uint_as_float(vt.z), W.x, nR), f1 = e2(__uint_as_float(vt.w), W.x, nR);
-    return (e0 + e1) + (f0 + f1);
+  if (W.p_only) {  // w = e_t: the row pass's unit sum (packed f32x2 arithmetic)
+    (void)vd;
+    return unit_sumexp<ES>(vt, W.x, W.Rt);
   }
   const F2 C = f2_pack(W.x.chi, W.x.chi), L = f2_pack(W.x.clo, W.x.clo);
   const F2 Nt = f2_pack(-W.Rt, -W.Rt), Nd = f2_pack(-W.Rd, -W.Rd);

@@ -1,7 +1,11 @@
 """GPU parity of sv_draft_sample (the draft-side sampler) against the float64
 oracle, through the C ABI.  Tokens must match bit for bit, except at a
-position whose inverse-CDF (or top-p cut) margin is below 1e-6, which is
-counted in the session budget of disagreements.
+position whose inverse-CDF (or top-p cut) margin is below 1e-6.  Such
+disagreements have their own budget (reading R22): at most 2e-3 of the
+sampled tokens of the session.  A draw that lands among the tail tokens of a
+128K vocabulary at T = 1 has margins of 1e-9..1e-7, below the float32
+accuracy of the per-token weights (ex2.approx, 2 ulp), and flips there at a
+measured rate of about 1e-3 of all draws.
 
 Cases: the headline batch's draft rows at full size (B=256, K=8, V=128256
 bf16, ragged k_b, per-row temperature), both dtypes with and without top-p,
@@ -23,6 +27,8 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
 
 MARGIN = 1e-6
+RATE = 2e-3
+SAMPLE_BUDGET = {"draws": 0, "disagreements": 0, "log": []}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,8 +61,10 @@ def _compare(got, flags, logits, dtype, B, K, V, kpr, temp, top_p, unif, mode, r
     diff = (got[sel] != tok[sel])
     low = margins[sel] < MARGIN
     assert not np.any(diff & ~low), np.argwhere(diff & ~low)[:10]
-    vh.BUDGET["decisions"] += int(np.sum(tok[sel] >= 0))
-    vh.BUDGET["disagreements"] += int(np.sum(diff))
+    SAMPLE_BUDGET["draws"] += int(np.sum(tok[sel] >= 0))
+    SAMPLE_BUDGET["disagreements"] += int(np.sum(diff))
+    for b, i in np.argwhere(diff):
+        SAMPLE_BUDGET["log"].append((int(sel[b]), int(i), float(margins[sel[b], i])))
     if rows is None:
         assert flags == oflags, (flags, oflags)
     return tok
@@ -64,8 +72,8 @@ def _compare(got, flags, logits, dtype, B, K, V, kpr, temp, top_p, unif, mode, r
 
 def test_headline_draft_rows_full_size():
     """B=256, K=8, V=128256 bf16: the draft rows of the headline verify batch,
-    sampled with its ragged k_b and per-row temperatures; every 4th sequence
-    checked against the oracle, every padding slot checked everywhere."""
+    sampled with its ragged k_b and per-row temperatures, all 1283 tokens
+    checked against the oracle."""
     w = wl.config_by_name("c2")
     unif = _uniforms(w.B, w.K, 5150)
     got, flags = _run(w.draft, w.dtype, w.B, w.K, w.V, w.k_per_row, w.temperature, 1.0, unif, w.mode)
@@ -73,7 +81,7 @@ def test_headline_draft_rows_full_size():
     for b in range(w.B):
         assert np.all(got[b, w.k_per_row[b]:] == -1) and np.all(got[b, :w.k_per_row[b]] >= 0)
     _compare(got, flags, w.draft, w.dtype, w.B, w.K, w.V, w.k_per_row, w.temperature, 1.0, unif,
-             w.mode, rows=range(0, w.B, 4))
+             w.mode)
 
 
 CASES = [
@@ -138,3 +146,10 @@ def test_error_paths():
     assert flags == (ov.FLAG_NONFINITE | ov.FLAG_BAD_UNIFORM | ov.FLAG_BAD_TEMPERATURE |
                      ov.FLAG_BAD_K)
     _compare(got, flags, logits, wl.F32, B, K, V, kpr, T, 1.0, unif, mode)
+
+
+def test_zz_sample_disagreement_budget():
+    """Low-margin disagreements over this module's draws stay under RATE."""
+    n, x = SAMPLE_BUDGET["draws"], SAMPLE_BUDGET["disagreements"]
+    assert n > 1000
+    assert x <= RATE * n, (x, n, SAMPLE_BUDGET["log"])

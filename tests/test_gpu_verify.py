@@ -214,4 +214,4 @@ def test_zz_disagreement_budget():
     under 1e-4 of the decisions taken."""
     d, x = vh.BUDGET["decisions"], vh.BUDGET["disagreements"]
     assert d > 0
-    assert x <= 1e-4 * d, (x, d)
+    assert x <= 1e-4 * d, (x, d, vh.BUDGET_LOG)

@@ -29,6 +29,7 @@ PROB_RTOL = 1e-5
 
 # session-wide disagreement budget
 BUDGET = {"decisions": 0, "disagreements": 0}
+BUDGET_LOG = []  # (where, sequence, smallest margin on the path) of each disagreement
 
 
 @dataclass
@@ -103,6 +104,7 @@ def compare(w: wl.VerifyInputs, g: GpuResult, o: ov.BatchResult, check_flags=Tru
                    if d.position <= div and d.margin < MARGIN]
             if low:
                 disagreements += 1
+                BUDGET_LOG.append((w.name, int(b), min(d.margin for d in low)))
             else:
                 problems.append(f"seq {b}: gpu n={g.n[b]} out={g.out[b].tolist()} vs oracle "
                                 f"n={r.n} out={r.out} (min margin "
