@@ -201,6 +201,37 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sv_dynk_init / sv_dynk_update - the dynamic draft length that feeds
+ * k_per_row ["Self-speculative decoding with layer skip and KV reuse" §3.2,
+ * §5.3]: each sequence's k follows its acceptance rate over the last 64
+ * rounds in which it proposed drafts (tokens accepted / tokens proposed);
+ * when that rate crosses above 0.85, k grows by one; when it crosses below
+ * 0.7, it shrinks by one; k stays in [2, 8].  A crossing counts once, in the
+ * round where the rate passes the threshold, and the tests are exact
+ * (20*accepted > 17*proposed, 10*accepted < 7*proposed).
+ *   state       device buffer of sv_dynk_state_size(B) bytes, 16-byte
+ *               aligned, owned by the caller and kept between rounds;
+ *               sv_dynk_init sets every k to k0 clamped to [2, 8] and empties
+ *               the windows.
+ *   n_accepted  device int32 [B]: the round's accepted lengths (e.g. from
+ *               sv_spec_verify).
+ *   k_used      device int32 [B]: the round's k_per_row (0: the sequence did
+ *               not speculate; the round is not recorded).
+ *   cap         device int32 [B] or NULL: bounds the next round's k (e.g. a
+ *               context-length policy); the controller's own k is unchanged.
+ *   k_next      device int32 [B]: min(k, cap), or 0 (no speculation) when
+ *               that is below 2.
+ *   workspace   a flag word (e.g. the verify workspace): a round with k_used
+ *               outside [0, 255] or n_accepted outside [0, k_used] is not
+ *               recorded and sets SV_FLAG_BAD_N.
+ */
+size_t sv_dynk_state_size(int B);
+sv_status sv_dynk_init(void* state, int B, int k0, void* stream);
+sv_status sv_dynk_update(void* state, int B, const int32_t* n_accepted, const int32_t* k_used,
+                         const int32_t* cap, int32_t* k_next, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * sv_draft_sample - the draft side of a round: draw each sequence's k_b draft
  * tokens from its rows of draft logits [FS §3.2; SSD §3.2, §4.2].  Token i of
  * sequence b comes from row (b, i) with the processing sv_spec_verify applies

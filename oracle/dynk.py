@@ -22,6 +22,8 @@ Readings (also listed in the design doc):
       k handed to the next round: k_next = min(k, cap); if that is below 2
       the round does not speculate (k_next = 0).  The controller's own k is
       unchanged by the cap.
+  R27 a round with k_used outside [0, 255] or n_accepted outside [0, k_used]
+      is not recorded and raises the bad-n flag (bit value 256).
 """
 
 from __future__ import annotations
@@ -39,6 +41,7 @@ class DynK:
         self.k = min(max(int(k0), K_MIN), K_MAX)
         self.hist = deque()      # (accepted, proposed) of the last WINDOW proposing rounds
         self.prev = None         # (acc, prop) sums of the window after the previous update
+        self.flags = 0
 
     @staticmethod
     def _above(acc: int, prop: int) -> bool:   # alpha > 0.85
@@ -51,7 +54,9 @@ class DynK:
     def update(self, n_accepted: int, k_used: int, cap: int | None = None) -> int:
         """Record one round (n_accepted of k_used drafts accepted) and return
         the k for the next round."""
-        if k_used > 0:
+        if not (0 <= k_used <= 255 and 0 <= n_accepted <= k_used):
+            self.flags |= 256
+        elif k_used > 0:
             self.hist.append((int(n_accepted), int(k_used)))
             if len(self.hist) > WINDOW:
                 self.hist.popleft()

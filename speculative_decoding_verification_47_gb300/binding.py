@@ -100,6 +100,12 @@ def lib() -> ctypes.CDLL:
         L.sv_draft_sample.restype = _i32
         L.sv_draft_sample.argtypes = [_vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _f32, _vp,
                                       _vp, _vp, _vp, _sz, _vp]
+        L.sv_dynk_state_size.restype = _sz
+        L.sv_dynk_state_size.argtypes = [_i32]
+        L.sv_dynk_init.restype = _i32
+        L.sv_dynk_init.argtypes = [_vp, _i32, _i32, _vp]
+        L.sv_dynk_update.restype = _i32
+        L.sv_dynk_update.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.sv_read_device_flags.restype = _i32
         L.sv_read_device_flags.argtypes = [_vp, _c.POINTER(_c.c_uint32), _vp]
         L.sv_last_error.restype = _c.c_char_p
@@ -188,6 +194,20 @@ def sv_draft_sample(draft_logits, seq_stride, pos_stride, dtype, B, K, V, k_per_
         _ptr(draft_logits), seq_stride, pos_stride, dtype, B, K, V, _ptr(k_per_row),
         _ptr(temperature), float(top_p), _ptr(uniforms), _ptr(mode), _ptr(out_tokens),
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def sv_dynk_state_size(B: int) -> int:
+    return lib().sv_dynk_state_size(B)
+
+
+def sv_dynk_init(state, B, k0, stream=None):
+    _check(lib().sv_dynk_init(_ptr(state), B, k0, _stream(stream)))
+
+
+def sv_dynk_update(state, B, n_accepted, k_used, cap, k_next, workspace, workspace_bytes,
+                   stream=None):
+    _check(lib().sv_dynk_update(_ptr(state), B, _ptr(n_accepted), _ptr(k_used), _ptr(cap),
+                                _ptr(k_next), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def sv_read_device_flags(workspace, stream=None) -> int:

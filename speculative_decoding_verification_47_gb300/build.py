@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["sv_verify.cu", "sv_commit.cu", "sv_lmhead.cu", "sv_api.cu"]
+SOURCES = ["sv_verify.cu", "sv_commit.cu", "sv_dynk.cu", "sv_lmhead.cu", "sv_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -164,6 +164,32 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
   return SV_OK;
 }
 
+size_t sv_dynk_state_size(int B) { return B < 1 ? 0 : sv::dynk_state_bytes(B); }
+
+sv_status sv_dynk_init(void* state, int B, int k0, void* stream) {
+  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (!state || !aligned(state, 16)) return fail(SV_ERR_ARG, "state must be non-NULL and 16-byte aligned");
+  std::string err;
+  const int s = sv::dynk_init_launch(state, B, k0, stream, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
+sv_status sv_dynk_update(void* state, int B, const int32_t* n_accepted, const int32_t* k_used,
+                         const int32_t* cap, int32_t* k_next, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (!state || !aligned(state, 16)) return fail(SV_ERR_ARG, "state must be non-NULL and 16-byte aligned");
+  if (!n_accepted || !k_used || !k_next) return fail(SV_ERR_ARG, "n_accepted, k_used and k_next are required");
+  if (!workspace || workspace_bytes < 4 || !aligned(workspace, 4))
+    return fail(SV_ERR_WORKSPACE, "workspace (its flag word) must be non-NULL, aligned, >= 4 bytes");
+  std::string err;
+  const int s = sv::dynk_update_launch(state, B, n_accepted, k_used, cap, k_next,
+                                       static_cast<uint32_t*>(workspace), stream, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
 size_t sv_draft_sample_workspace_size(void) { return 256; }
 
 sv_status sv_draft_sample(const void* draft_logits, int64_t seq_stride, int64_t pos_stride,

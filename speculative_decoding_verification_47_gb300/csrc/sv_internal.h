@@ -57,6 +57,12 @@ constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
 constexpr int kMaxDevices = 64;
 int verify_launch_noalloc(const VerifyLaunch& L, std::string* err);
 
+size_t dynk_state_bytes(int B);
+int dynk_init_launch(void* state, int B, int k0, void* stream, std::string* err);
+int dynk_update_launch(void* state, int B, const int32_t* n_accepted, const int32_t* k_used,
+                       const int32_t* cap, int32_t* k_next, uint32_t* flags, void* stream,
+                       std::string* err);
+
 int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
                   int K, uint32_t* flags, void* stream, std::string* err);
 

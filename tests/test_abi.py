@@ -129,3 +129,20 @@ def test_draft_sample_host_checks(lib):
         with pytest.raises(sb.SVError) as e:
             call(**kw)
         assert e.value.status == status, kw
+
+
+def test_dynk_host_checks(lib):
+    assert sb.sv_dynk_state_size(0) == 0
+    assert sb.sv_dynk_state_size(256) >= 256 * (7 * 4 + 128)
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_dynk_init(P, 0, 4, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_dynk_init(None, 4, 4, 0)
+    assert e.value.status == sb.SV_ERR_ARG
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_dynk_update(P, 4, None, P, None, P, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_ARG
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_dynk_update(P, 4, P, P, None, P, None, 256, 0)
+    assert e.value.status == sb.SV_ERR_WORKSPACE

@@ -107,3 +107,11 @@ def test_random_histories_match_direct_window_sums():
                         k = max(k - 1, 2)
                 prev = (acc, prop)
             assert got == k, (trial, r)
+
+
+def test_invalid_round_is_not_recorded():
+    c = dynk.DynK(5)
+    c.update(3, 4)
+    before = (list(c.hist), c.prev)
+    assert c.update(5, 4) == 5 and c.flags == 256
+    assert (list(c.hist), c.prev) == before
