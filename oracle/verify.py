@@ -23,7 +23,9 @@ Readings of points the pages leave open (each also listed in the design doc):
       inclusive prefix; zero-weight tokens can never be drawn.
   R6  top-p: order tokens by (p desc, index asc); keep v iff the mass strictly
       before v is <= top_p; renormalise over the kept set ([FS §3.2] code).
-  R7  top-p is applied identically to target and draft.
+  R7  top-p is applied identically to target and draft; the variant with
+      ``topp_draft=False`` truncates only the target and leaves the draft
+      untruncated (the option [SSD §3.4] prefers; NEXT-4 reading R28).
   R8  temperature: exp((z - m) / T) with m the row max, same T both sides
       ([SSD §2.4], [FS §2.3]).
   R9  one uniform per tested position (column i), one for the single
@@ -226,7 +228,7 @@ def verify_from_distributions(P, Q, x, k: int, u, K: int):
 
 
 def verify_sequence(zt_rows, zd_rows, x, k: int, K: int, V: int, T: float,
-                    top_p: float, u, mode: int) -> SeqResult:
+                    top_p: float, u, mode: int, topp_draft: bool = True) -> SeqResult:
     """Verify one sequence.  zt_rows: K+1 target logit rows (float64, only rows
     0..k are looked at), zd_rows: K draft rows, x: K draft tokens, u: K+1
     uniforms.  Rows, tokens and uniforms are examined lazily in position
@@ -284,7 +286,7 @@ def verify_sequence(zt_rows, zd_rows, x, k: int, K: int, V: int, T: float,
         zd = zd_rows[i]
         if pt is None or not _finite_row(zd):
             return _error(K, FLAG_NONFINITE, res)
-        qd = process_row(zd, T, top_p)
+        qd = process_row(zd, T, top_p if topp_draft else 1.0)
         res.m_d[i], res.S_d[i], res.M_d[i] = qd.m, qd.S, qd.M
         if qd.kept is not None:
             res.decisions.append(Decision("topp", i, qd.cut_margin))
@@ -337,7 +339,7 @@ class BatchResult:
 
 def spec_verify(target, draft, dtype: str, B: int, K: int, V: int, draft_tokens,
                 k_per_row, temperature, top_p: float, uniforms, mode,
-                rows=None) -> BatchResult:
+                rows=None, topp_draft: bool = True) -> BatchResult:
     """Batched verify: every sequence independently (reading R9 for the
     uniform layout).  ``target`` [B, K+1, V] and ``draft`` [B, K, V] hold the
     stored logits (bf16 bit patterns or float32).  ``rows`` optionally
@@ -355,7 +357,8 @@ def spec_verify(target, draft, dtype: str, B: int, K: int, V: int, draft_tokens,
         zd = _LazyRows(draft[b], dtype) if draft is not None else None
         r = verify_sequence(zt, zd, np.asarray(draft_tokens[b]), k, K, V,
                             float(temperature[b]), float(top_p),
-                            np.asarray(uniforms[b], dtype=np.float64), int(mode[b]))
+                            np.asarray(uniforms[b], dtype=np.float64), int(mode[b]),
+                            topp_draft=topp_draft)
         out[b] = r.out
         n[b] = r.n
         flags |= r.flags

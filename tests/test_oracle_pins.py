@@ -61,7 +61,7 @@ def cells(breaks):
     return [((a + b) / 2.0, b - a) for a, b in zip(pts[:-1], pts[1:]) if b > a]
 
 
-def enumerate_sequence(zt, zd, k, T=1.0, top_p=1.0):
+def enumerate_sequence(zt, zd, k, T=1.0, top_p=1.0, topp_draft=True):
     """Exact output law of oracle.verify_sequence for one sequence with k
     drafts, by enumeration: draft tokens x_i over their law q_i, each accept
     uniform over its two pieces [0, r_i) / [r_i, 1), and the resample/bonus
@@ -71,7 +71,7 @@ def enumerate_sequence(zt, zd, k, T=1.0, top_p=1.0):
     V = len(zt[0])
     K = k
     P = [textbook_probs(zt[i], T, top_p) for i in range(k + 1)]
-    Q = [textbook_probs(zd[i], T, top_p) for i in range(k)]
+    Q = [textbook_probs(zd[i], T, top_p if topp_draft else 1.0) for i in range(k)]
     ubreaks = set(cdf_breaks(P[k]))
     for i in range(k):
         ubreaks |= set(cdf_breaks(textbook_residual(P[i], Q[i])))
@@ -89,7 +89,7 @@ def enumerate_sequence(zt, zd, k, T=1.0, top_p=1.0):
             for um, ul in ucells:
                 u = np.array([c[0] for c in combo] + [um])
                 res = ov.verify_sequence(zt, zd, np.array(xs), k, K, V, T, top_p,
-                                         u, ov.SAMPLED)
+                                         u, ov.SAMPLED, topp_draft=topp_draft)
                 key = (res.n, tuple(res.out))
                 law[key] = law.get(key, 0.0) + wx * wu * ul
     return law, P, Q
@@ -458,3 +458,23 @@ def test_kv_commit_invariant():
     bad[1] = K + 1
     s3, flags = ov.kv_commit(s0, bad, None, K)
     assert flags == ov.FLAG_BAD_N and s3[0] == s0[0] and s3[1] == s0[1]
+
+
+@pytest.mark.parametrize("case", ["top_p", "top_p_ties"])
+@pytest.mark.parametrize("k", [1, 2])
+def test_enumeration_target_only_top_p(case, k):
+    """Target-only truncation (the draft untruncated): the output law is still
+    exactly the truncated target p' at every position, whatever q is."""
+    V = 8
+    cfg = ENUM_CASES[case]
+    rng = np.random.default_rng(zlib.crc32(f"target-only/{case}/{k}".encode()))
+    zt, zd = _case_logits(cfg["kind"], rng, V, k)
+    law, P, Q = enumerate_sequence(zt, zd, k, cfg["T"], cfg["top_p"], topp_draft=False)
+    assert math.isclose(sum(law.values()), 1.0, abs_tol=1e-12)
+    assert np.count_nonzero(Q[0]) == V  # the draft really is untruncated
+    m0, _ = marginal(law, 0, V)
+    np.testing.assert_allclose(m0, P[0], atol=1e-12, rtol=0)
+    m1, tot = marginal(law, 1, V, cond_min_n=1)
+    assert math.isclose(tot, math.fsum(np.minimum(P[0], Q[0])), abs_tol=1e-12)
+    if tot > 0:
+        np.testing.assert_allclose(m1, P[1], atol=1e-12, rtol=0)
