@@ -149,6 +149,25 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
                          size_t workspace_bytes, void* stream);
 
 /*
+ * sv_spec_verify_target_topp - sv_spec_verify with top-p applied to the target
+ * rows only: the draft keeps its untruncated temperature softmax q in the
+ * ratio p'(x)/q(x) and in the residual max(0, p' - q), the option
+ * "Self-speculative decoding with layer skip and KV reuse" §3.4 prefers.  The
+ * emitted tokens still follow the truncated target p'.  Same arguments,
+ * layouts, ownership and errors as sv_spec_verify; with top_p = 1 the two
+ * calls are identical.
+ */
+sv_status sv_spec_verify_target_topp(const void* target_logits, int64_t target_seq_stride,
+                                     int64_t target_pos_stride, const void* draft_logits,
+                                     int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                     sv_dtype dtype, int B, int K, int V,
+                                     const int32_t* draft_tokens, const int32_t* k_per_row,
+                                     const float* temperature, float top_p, const float* uniforms,
+                                     const uint8_t* mode, int32_t* out_tokens, int32_t* n_accepted,
+                                     float* diag, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * sv_spec_verify_noalloc - sv_spec_verify for callers that cannot allocate
  * device memory.  The pages describe no such call; it exists for embedders
  * such as plugins inside an inference server whose device memory is owned

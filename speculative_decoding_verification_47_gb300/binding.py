@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.sv_spec_verify.restype = _i32
         L.sv_spec_verify.argtypes = [_vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32, _i32,
                                      _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.sv_spec_verify_target_topp.restype = _i32
+        L.sv_spec_verify_target_topp.argtypes = L.sv_spec_verify.argtypes
         L.sv_spec_verify_noalloc.restype = _i32
         L.sv_spec_verify_noalloc.argtypes = [_vp, _i64, _i64, _vp, _i64, _i64, _i32, _i32, _i32,
                                              _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp,
@@ -154,6 +156,18 @@ def sv_spec_verify(target_logits, target_seq_stride, target_pos_stride, draft_lo
                    temperature, top_p, uniforms, mode, out_tokens, n_accepted, diag, workspace,
                    workspace_bytes, stream=None):
     _check(lib().sv_spec_verify(
+        _ptr(target_logits), target_seq_stride, target_pos_stride, _ptr(draft_logits),
+        draft_seq_stride, draft_pos_stride, dtype, B, K, V, _ptr(draft_tokens), _ptr(k_per_row),
+        _ptr(temperature), float(top_p), _ptr(uniforms), _ptr(mode), _ptr(out_tokens),
+        _ptr(n_accepted), _ptr(diag), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def sv_spec_verify_target_topp(target_logits, target_seq_stride, target_pos_stride, draft_logits,
+                               draft_seq_stride, draft_pos_stride, dtype, B, K, V, draft_tokens,
+                               k_per_row, temperature, top_p, uniforms, mode, out_tokens, n_accepted,
+                               diag, workspace, workspace_bytes, stream=None):
+    """sv_spec_verify with top-p on the target rows only (the draft untruncated)."""
+    _check(lib().sv_spec_verify_target_topp(
         _ptr(target_logits), target_seq_stride, target_pos_stride, _ptr(draft_logits),
         draft_seq_stride, draft_pos_stride, dtype, B, K, V, _ptr(draft_tokens), _ptr(k_per_row),
         _ptr(temperature), float(top_p), _ptr(uniforms), _ptr(mode), _ptr(out_tokens),

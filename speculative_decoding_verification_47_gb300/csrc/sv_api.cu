@@ -36,14 +36,14 @@ size_t sv_lmhead_workspace_size(int M, int H) {
   return sv::lmhead_workspace_bytes(M, H);
 }
 
-sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
-                         int64_t target_pos_stride, const void* draft_logits,
-                         int64_t draft_seq_stride, int64_t draft_pos_stride, sv_dtype dtype,
-                         int B, int K, int V, const int32_t* draft_tokens,
-                         const int32_t* k_per_row, const float* temperature, float top_p,
-                         const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
-                         int32_t* n_accepted, float* diag, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+static sv_status spec_verify_impl(const void* target_logits, int64_t target_seq_stride,
+                                  int64_t target_pos_stride, const void* draft_logits,
+                                  int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                  sv_dtype dtype, int B, int K, int V, const int32_t* draft_tokens,
+                                  const int32_t* k_per_row, const float* temperature, float top_p,
+                                  const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                                  int32_t* n_accepted, float* diag, void* workspace,
+                                  size_t workspace_bytes, void* stream, int topp_draft) {
   if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
   if (B < 1 || K < 0 || K > kMaxK || V < 1)
     return fail(SV_ERR_SHAPE, "need B >= 1, 0 <= K <= 20, V >= 1");
@@ -90,10 +90,40 @@ sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
   L.diag = diag;
   L.workspace = workspace;
   L.stream = stream;
+  L.topp_draft = topp_draft;
   std::string err;
   int s = sv::verify_launch(L, &err);
   if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
   return SV_OK;
+}
+
+sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
+                         int64_t target_pos_stride, const void* draft_logits,
+                         int64_t draft_seq_stride, int64_t draft_pos_stride, sv_dtype dtype,
+                         int B, int K, int V, const int32_t* draft_tokens,
+                         const int32_t* k_per_row, const float* temperature, float top_p,
+                         const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                         int32_t* n_accepted, float* diag, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return spec_verify_impl(target_logits, target_seq_stride, target_pos_stride, draft_logits,
+                          draft_seq_stride, draft_pos_stride, dtype, B, K, V, draft_tokens,
+                          k_per_row, temperature, top_p, uniforms, mode, out_tokens, n_accepted,
+                          diag, workspace, workspace_bytes, stream, 1);
+}
+
+sv_status sv_spec_verify_target_topp(const void* target_logits, int64_t target_seq_stride,
+                                     int64_t target_pos_stride, const void* draft_logits,
+                                     int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                     sv_dtype dtype, int B, int K, int V,
+                                     const int32_t* draft_tokens, const int32_t* k_per_row,
+                                     const float* temperature, float top_p, const float* uniforms,
+                                     const uint8_t* mode, int32_t* out_tokens, int32_t* n_accepted,
+                                     float* diag, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return spec_verify_impl(target_logits, target_seq_stride, target_pos_stride, draft_logits,
+                          draft_seq_stride, draft_pos_stride, dtype, B, K, V, draft_tokens,
+                          k_per_row, temperature, top_p, uniforms, mode, out_tokens, n_accepted,
+                          diag, workspace, workspace_bytes, stream, 0);
 }
 
 sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_stride,

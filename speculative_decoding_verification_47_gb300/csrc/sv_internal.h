@@ -27,6 +27,7 @@ struct VerifyLaunch {
   float* diag;
   void* workspace;
   void* stream;
+  int topp_draft = 1;  // top_p < 1: truncate the draft rows too (1) or only the target rows (0)
 };
 
 // Enqueue the verify step.  Returns an sv_status; fills *err on failure.

@@ -78,6 +78,7 @@ struct VerifyParams {
   uint32_t* flags;
   unsigned long long* words;
   uint32_t* words2;  // per sequence: bit 0 prefix resolved, bit 1+i draw of position i stored
+  int topp_draft;    // top_p < 1: also truncate the draft rows (1) or only the target rows (0)
   ItemStats* stats;
   int slice_len;  // elements per CTA slice
 };
@@ -1662,11 +1663,13 @@ __device__ __noinline__ void judge(const VerifyParams& P, Shared& sh, int i, int
       bool keep_t = true, keep_d = true;
       if (TOPP) {
         const TopSel& a = sh.ts[0];
-        const TopSel& d = sh.ts[1];
         Et = a.E;
-        Ed = d.E;
         keep_t = a.kx > a.kstar || (a.kx == a.kstar && a.lt < a.nk);
-        keep_d = d.kx > d.kstar || (d.kx == d.kstar && d.lt < d.nk);
+        if (P.topp_draft) {  // (else the draft keeps its untruncated softmax)
+          const TopSel& d = sh.ts[1];
+          Ed = d.E;
+          keep_d = d.kx > d.kstar || (d.kx == d.kstar && d.lt < d.nk);
+        }
       }
       const float lt = (zt_x - row_t.mx) * X.chi, ld = (zd_x - row_d.mx) * X.chi;
       float r;
@@ -1724,7 +1727,7 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
       if (has_draft && !bad_d) {
         dg[SV_DIAG_M_D] = row_d.mx;
         dg[SV_DIAG_S_D] = df_to_float(row_d.s) * ex2(-earg(row_d.mx, X, row_d.R));
-        dg[SV_DIAG_MASS_D] = sel ? df_to_float(df_div(sh.ts[1].E, row_d.s)) : 1.f;
+        dg[SV_DIAG_MASS_D] = sel && P.topp_draft ? df_to_float(df_div(sh.ts[1].E, row_d.s)) : 1.f;
         dg[SV_DIAG_P_X] = dq[0];
         dg[SV_DIAG_Q_X] = dq[1];
         dg[SV_DIAG_RATIO] = dq[2];
@@ -2012,8 +2015,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   const bool bad_d = has_draft && (!(row_d.mx > -INFINITY && row_d.mx < INFINITY) ||
                                    !(row_d.R > kRnone && row_d.R < INFINITY));
   if (TOPP && !greedy && !bad_t && !bad_d)
-    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb, has_draft,
-                    X, st, sd, sh.row_t, sh.row_d);
+    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb,
+                    has_draft && P.topp_draft, X, st, sd, sh.row_t, sh.row_d);
 
   // ---- verdict (every CTA), publication (rank 0, one thread) ----
   if (tid == 0) judge<ES, TOPP>(P, sh, i, kb, greedy, has_draft, X, sh.row_t, sh.row_d, bad_t, bad_d, sh.dq);
@@ -2065,7 +2068,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
     kt = sh.ts[0].kstar;
     nkt = sh.ts[0].nk;
     cntt = sh.ts[0].cstar;
-    if (i < kb) {
+    if (i < kb && P.topp_draft) {
       S_d = sh.ts[1].E;
       kd = sh.ts[1].kstar;
       nkd = sh.ts[1].nk;
@@ -2300,6 +2303,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   P.flags = reinterpret_cast<uint32_t*>(ws);
   P.words = reinterpret_cast<unsigned long long*>(ws + words_off);
   P.words2 = reinterpret_cast<uint32_t*>(ws + words2_off);
+  P.topp_draft = L.topp_draft;
   P.stats = reinterpret_cast<ItemStats*>(ws + stats_off);
   P.slice_len = slice;
   cudaStream_t stream = static_cast<cudaStream_t>(L.stream);

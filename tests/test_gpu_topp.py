@@ -143,3 +143,40 @@ def test_top_p_one_and_just_below_one():
     w.top_p = float(np.float32(1.0 - 2.0 ** -24))
     g2 = vh.run_gpu(w)
     vh.compare(w, g2, vh.run_oracle(w))
+
+
+TARGET_ONLY = [
+    # id, B, K, V, dtype, T, top_p, mode
+    ("bf16_p0.9", 6, 4, 1000, wl.BF16, [0.7, 1.0], 0.9, 0),
+    ("f32_p0.5", 5, 3, 4099, wl.F32, 1.0, 0.5, 0),
+    ("bf16_p0.99_mix", 6, 5, 32003, wl.BF16, [0.1, 0.7, 1.7], 0.99, [0, 1, 0, 0, 1, 0]),
+    ("bf16_one_token", 8, 3, 5003, wl.BF16, 1.0, 0.001, 0),
+]
+
+
+@pytest.mark.parametrize("case", TARGET_ONLY, ids=[c[0] for c in TARGET_ONLY])
+def test_target_only_top_p(case):
+    """sv_spec_verify_target_topp: the draft keeps its untruncated softmax
+    (draft tokens outside the target nucleus are rejected by p' = 0)."""
+    _, B, K, V, dt, T, p, m = case
+    T = np.resize(np.asarray(T, np.float32), B)
+    w = wl.synth_verify("tonly", B, K, V, dt, K, T, 1.0, m, top_p=p,
+                        seeds=(8700 + V, 8800 + B, 8900 + K))
+    g = vh.run_gpu(w, target_topp=True)
+    vh.compare(w, g, vh.run_oracle(w, topp_draft=False))
+
+
+def test_c3_full_size_target_only_top_p():
+    """The mixed top-p batch at full size with the draft untruncated."""
+    w = wl.config_c3()
+    g = vh.run_gpu(w, target_topp=True)
+    dec, _ = vh.compare(w, g, vh.run_oracle(w, topp_draft=False))
+    assert dec > 0
+
+
+def test_target_only_equals_both_at_top_p_one():
+    B, K, V = 4, 3, 3001
+    w = wl.synth_verify("t1", B, K, V, wl.BF16, K, 1.0, 1.0, 0, top_p=1.0, seeds=(8950, 8951, 8952))
+    a = vh.run_gpu(w)
+    b = vh.run_gpu(w, target_topp=True)
+    assert np.array_equal(a.out, b.out) and np.array_equal(a.n, b.n)

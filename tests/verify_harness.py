@@ -58,7 +58,9 @@ def to_device(w: wl.VerifyInputs, device="cuda"):
 
 
 def run_gpu(w: wl.VerifyInputs, dev=None, diag=True, strides=(0, 0, 0, 0), draft=True,
-            workspace=None, pass_kpr=True, pass_mode=True, pass_temp=True) -> GpuResult:
+            workspace=None, pass_kpr=True, pass_mode=True, pass_temp=True,
+            target_topp=False) -> GpuResult:
+    """target_topp: call sv_spec_verify_target_topp (top-p on the target rows only)."""
     import torch
     dev = dev or to_device(w)
     B, K, V = w.B, w.K, w.V
@@ -69,19 +71,21 @@ def run_gpu(w: wl.VerifyInputs, dev=None, diag=True, strides=(0, 0, 0, 0), draft
     dt = sb.SV_BF16 if w.dtype == wl.BF16 else sb.SV_F32
     wsb = sb.sv_workspace_size(B, K, V, dt)
     ws = workspace if workspace is not None else torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    sb.sv_spec_verify(dev["target"], strides[0], strides[1], dev["draft"] if draft else None,
-                      strides[2], strides[3], dt, B, K, V, dev["tokens"],
-                      dev["kpr"] if pass_kpr else None, dev["temp"] if pass_temp else None,
-                      w.top_p, dev["unif"], dev["mode"] if pass_mode else None, out, n, dg, ws,
-                      ws.numel())
+    fn = sb.sv_spec_verify_target_topp if target_topp else sb.sv_spec_verify
+    fn(dev["target"], strides[0], strides[1], dev["draft"] if draft else None,
+       strides[2], strides[3], dt, B, K, V, dev["tokens"],
+       dev["kpr"] if pass_kpr else None, dev["temp"] if pass_temp else None,
+       w.top_p, dev["unif"], dev["mode"] if pass_mode else None, out, n, dg, ws,
+       ws.numel())
     flags = sb.sv_read_device_flags(ws)
     return GpuResult(out=out.cpu().numpy(), n=n.cpu().numpy(),
                      diag=dg.cpu().numpy() if diag else None, flags=flags)
 
 
-def run_oracle(w: wl.VerifyInputs, rows=None) -> ov.BatchResult:
+def run_oracle(w: wl.VerifyInputs, rows=None, topp_draft=True) -> ov.BatchResult:
     return ov.spec_verify(w.target, w.draft, w.dtype, w.B, w.K, w.V, w.draft_tokens,
-                          w.k_per_row, w.temperature, w.top_p, w.uniforms, w.mode, rows=rows)
+                          w.k_per_row, w.temperature, w.top_p, w.uniforms, w.mode, rows=rows,
+                          topp_draft=topp_draft)
 
 
 def _rel(a, b):
