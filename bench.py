@@ -53,9 +53,10 @@ COPIES = 3
 # from the ncu captures summarised in profiles/; reported only while the
 # kernel source still has the hash it had when the counters were taken.
 MEASURED_TRAFFIC = {
-    "c2": ("sv_verify.cu", "b8a25d062de5cedd", 491.784192e6 + 9.750528e6),
-    "c3": ("sv_verify.cu", "b8a25d062de5cedd", 473.832960e6 + 64.258048e6),
-    "c4": ("sv_lmhead.cu", "0e369d20a97eb4be", 272.729088e6 + 21.835008e6),
+    "c2": ("sv_verify.cu", "4e72065c2dfc4313", 491.854080e6 + 8.162048e6),
+    "c3": ("sv_verify.cu", "4e72065c2dfc4313", 477.332992e6 + 64.789760e6),
+    "c4": ("sv_lmhead.cu", "0e369d20a97eb4be", 272.628736e6 + 21.940224e6),
+    "s2": ("sv_verify.cu", "4e72065c2dfc4313", 356.943616e6 + 3.793664e6),
 }
 
 
