@@ -19,9 +19,11 @@ Readings (also listed in the design doc):
       on the free stack and its table entry set to -1.  The free stack's
       order is not part of the result (only the set of released ids is).
   R30 n_b outside [0, k_b], or k_b outside [0, max_pages * P - L_b], leaves
-      the sequence unchanged and raises the bad-n flag (bit value 256); a
-      release that would overflow the free stack leaves the sequence
-      unchanged and raises the capacity flag (bit value 64).
+      the sequence unchanged and raises the bad-n flag (bit value 256).  If
+      the call's releases together would overflow the free stack, no
+      sequence changes at all and the capacity flag (bit value 64) is raised:
+      all or nothing, so the result does not depend on the order in which
+      sequences are handled.
 """
 
 from __future__ import annotations
@@ -39,6 +41,7 @@ def kv_commit_paged(seq_lens, n_accepted, k_per_row, block_table, page_size: int
     table = [list(map(int, row)) for row in block_table]
     max_pages = len(table[0]) if table else 0
     released, flags, top = [], 0, int(free_top)
+    plan = []  # (b, L + n, first page to release, released ids)
     for b in range(len(lens)):
         L, n, k = lens[b], int(n_accepted[b]), int(k_per_row[b])
         if not (0 <= k <= max_pages * P - L and 0 <= n <= k):
@@ -46,10 +49,10 @@ def kv_commit_paged(seq_lens, n_accepted, k_per_row, block_table, page_size: int
             continue
         Ln = L + n
         keep = -(-Ln // P)  # ceil(Ln / P)
-        rel = [table[b][j] for j in range(keep, max_pages) if table[b][j] >= 0]
-        if top + len(rel) > free_capacity:
-            flags |= FLAG_CAPACITY
-            continue
+        plan.append((b, Ln, keep, [table[b][j] for j in range(keep, max_pages) if table[b][j] >= 0]))
+    if top + sum(len(r) for *_, r in plan) > free_capacity:
+        return lens, table, [], top, flags | FLAG_CAPACITY
+    for b, Ln, keep, rel in plan:
         for j in range(keep, max_pages):
             table[b][j] = -1
         released.extend(rel)

@@ -61,3 +61,12 @@ def test_random_against_token_ownership():
         before = {x for row in table for x in row if x >= 0}
         after = {x for row in tab for x in row if x >= 0}
         assert before == after | set(rel) and not (after & set(rel))
+
+
+def test_capacity_is_all_or_nothing():
+    """Room for one of two releases: neither happens."""
+    table = [[1, 2], [3, 4]]
+    lens, tab, rel, top, flags = opg.kv_commit_paged([1, 1], [0, 0], [2, 2], table, 2, 0, 1)
+    assert flags == opg.FLAG_CAPACITY and rel == [] and tab == table and lens == [1, 1]
+    lens, tab, rel, top, flags = opg.kv_commit_paged([1, 1], [0, 0], [2, 2], table, 2, 0, 2)
+    assert flags == 0 and sorted(rel) == [2, 4] and lens == [1, 1] and top == 2
