@@ -220,6 +220,34 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sv_kv_commit_paged - sv_kv_commit for a paged KV cache ["Self-speculative
+ * decoding with layer skip and KV reuse" §3.3, §4.5]: the write pointer moves
+ * to seq_lens[b] + n_accepted[b] (= L'), pages 0 .. ceil(L'/page_size) - 1 of
+ * the sequence stay, and every allocated page from index ceil(L'/page_size)
+ * on is pushed on the free stack and its block-table entry set to -1.
+ *   seq_lens      device int32 [B], read and written: the length at the start
+ *                 of the round (the drafts were written at L .. L + k_b - 1).
+ *   n_accepted    device int32 [B]; k_per_row device int32 [B] (the round's k).
+ *   block_table   device int32 [B][max_pages], read and written: page ids,
+ *                 -1 for none.
+ *   free_pages    device int32 [free_capacity]: the free stack; released ids
+ *                 are written at free_top onwards, in no fixed order.
+ *   free_top      device int32 [1]: the stack's size, read and advanced.
+ *   workspace     device, >= 16 bytes, 16-byte aligned: word 0 is the flag
+ *                 word (OR-ed, not cleared; e.g. the verify workspace), words 1
+ *                 and 2 are scratch.
+ * A sequence with n_accepted outside [0, k_b], or with L + k_b beyond its
+ * table, is left unchanged and sets SV_FLAG_BAD_N.  If the call's releases
+ * together would overflow the free stack, nothing changes and
+ * SV_FLAG_CAPACITY is set.
+ */
+sv_status sv_kv_commit_paged(int32_t* seq_lens, const int32_t* n_accepted,
+                             const int32_t* k_per_row, int32_t* block_table, int max_pages,
+                             int page_size, int32_t* free_pages, int32_t* free_top,
+                             int free_capacity, int B, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
  * sv_dynk_init / sv_dynk_update - the dynamic draft length that feeds
  * k_per_row ["Self-speculative decoding with layer skip and KV reuse" §3.2,
  * §5.3]: each sequence's k follows its acceptance rate over the last 64

@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.sv_draft_sample.restype = _i32
         L.sv_draft_sample.argtypes = [_vp, _i64, _i64, _i32, _i32, _i32, _i32, _vp, _vp, _f32, _vp,
                                       _vp, _vp, _vp, _sz, _vp]
+        L.sv_kv_commit_paged.restype = _i32
+        L.sv_kv_commit_paged.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp,
+                                         _sz, _vp]
         L.sv_dynk_state_size.restype = _sz
         L.sv_dynk_state_size.argtypes = [_i32]
         L.sv_dynk_init.restype = _i32
@@ -208,6 +211,15 @@ def sv_draft_sample(draft_logits, seq_stride, pos_stride, dtype, B, K, V, k_per_
         _ptr(draft_logits), seq_stride, pos_stride, dtype, B, K, V, _ptr(k_per_row),
         _ptr(temperature), float(top_p), _ptr(uniforms), _ptr(mode), _ptr(out_tokens),
         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def sv_kv_commit_paged(seq_lens, n_accepted, k_per_row, block_table, max_pages, page_size,
+                       free_pages, free_top, free_capacity, B, workspace, workspace_bytes,
+                       stream=None):
+    _check(lib().sv_kv_commit_paged(_ptr(seq_lens), _ptr(n_accepted), _ptr(k_per_row),
+                                    _ptr(block_table), max_pages, page_size, _ptr(free_pages),
+                                    _ptr(free_top), free_capacity, B, _ptr(workspace),
+                                    workspace_bytes, _stream(stream)))
 
 
 def sv_dynk_state_size(B: int) -> int:

@@ -194,6 +194,25 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
   return SV_OK;
 }
 
+sv_status sv_kv_commit_paged(int32_t* seq_lens, const int32_t* n_accepted,
+                             const int32_t* k_per_row, int32_t* block_table, int max_pages,
+                             int page_size, int32_t* free_pages, int32_t* free_top,
+                             int free_capacity, int B, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (B < 1 || max_pages < 1 || page_size < 1 || free_capacity < 0)
+    return fail(SV_ERR_SHAPE, "need B >= 1, max_pages >= 1, page_size >= 1, free_capacity >= 0");
+  if (!seq_lens || !n_accepted || !k_per_row || !block_table || !free_pages || !free_top)
+    return fail(SV_ERR_ARG, "every array argument is required");
+  if (!workspace || workspace_bytes < 16 || !aligned(workspace, 16))
+    return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL, 16-byte aligned and >= 16 bytes");
+  std::string err;
+  const int s = sv::paged_commit_launch(seq_lens, n_accepted, k_per_row, block_table, max_pages,
+                                        page_size, free_pages, free_top, free_capacity, B,
+                                        static_cast<uint32_t*>(workspace), stream, &err);
+  if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
+  return SV_OK;
+}
+
 size_t sv_dynk_state_size(int B) { return B < 1 ? 0 : sv::dynk_state_bytes(B); }
 
 sv_status sv_dynk_init(void* state, int B, int k0, void* stream) {

@@ -55,4 +55,90 @@ int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* c
   return SV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Paged-KV commit ([SSD §3.3, §4.5]): the cache of sequence b is a block table
+// of pages of P tokens.  After verification its length is L' = L + n; pages
+// 0 .. ceil(L'/P)-1 stay and every allocated page from index ceil(L'/P) on
+// goes back to the free stack (its table entry becomes -1).  Two launches:
+// the first checks every sequence and counts the call's releases (and keeps
+// the free stack's top as it was), the second applies them all, or none if
+// together they would overflow the free stack.  Scratch: workspace words 1
+// (release count) and 2 (the top before the call).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool paged_ok(int L, int n, int k, int max_pages, int P) {
+  return k >= 0 && (long long)L + k <= (long long)max_pages * P && n >= 0 && n <= k && L >= 0;
+}
+
+__global__ void paged_count_kernel(const int32_t* __restrict__ seq_lens,
+                                   const int32_t* __restrict__ n_accepted,
+                                   const int32_t* __restrict__ k_per_row,
+                                   const int32_t* __restrict__ table, int max_pages, int P, int B,
+                                   const int32_t* __restrict__ free_top, uint32_t* ws) {
+  pdl_wait();  // the launch may overlap the kernel that wrote n_accepted
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b == 0) ws[2] = (uint32_t)*free_top;
+  if (b >= B) return;
+  const int L = seq_lens[b], n = n_accepted[b], k = k_per_row[b];
+  if (!paged_ok(L, n, k, max_pages, P)) {
+    atomicOr(ws, SV_FLAG_BAD_N);
+    return;
+  }
+  const int keep = (L + n + P - 1) / P;
+  const int32_t* row = table + (size_t)b * max_pages;
+  uint32_t c = 0;
+  for (int j = keep; j < max_pages; ++j) c += row[j] >= 0 ? 1u : 0u;
+  if (c) atomicAdd(ws + 1, c);
+}
+
+__global__ void paged_apply_kernel(int32_t* __restrict__ seq_lens,
+                                   const int32_t* __restrict__ n_accepted,
+                                   const int32_t* __restrict__ k_per_row, int32_t* __restrict__ table,
+                                   int max_pages, int P, int B, int32_t* __restrict__ free_pages,
+                                   int32_t* __restrict__ free_top, int free_capacity, uint32_t* ws) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if ((long long)ws[2] + ws[1] > (long long)free_capacity) {  // (the same test in every thread)
+    if (b == 0) atomicOr(ws, SV_FLAG_CAPACITY);
+    return;
+  }
+  if (b >= B) return;
+  const int L = seq_lens[b], n = n_accepted[b], k = k_per_row[b];
+  if (!paged_ok(L, n, k, max_pages, P)) return;
+  const int keep = (L + n + P - 1) / P;
+  int32_t* row = table + (size_t)b * max_pages;
+  int c = 0;
+  for (int j = keep; j < max_pages; ++j) c += row[j] >= 0 ? 1 : 0;
+  int pos = c ? atomicAdd(free_top, c) : 0;
+  for (int j = keep; j < max_pages; ++j) {
+    if (row[j] >= 0) free_pages[pos++] = row[j];
+    row[j] = -1;
+  }
+  seq_lens[b] = L + n;
+}
+
+int paged_commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* k_per_row,
+                        int32_t* block_table, int max_pages, int page_size, int32_t* free_pages,
+                        int32_t* free_top, int free_capacity, int B, uint32_t* ws, void* stream,
+                        std::string* err) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws + 1, 0, sizeof(uint32_t), st);  // the release count
+  const int threads = 256, blocks = (B + threads - 1) / threads;
+  if (e == cudaSuccess) {
+    paged_count_kernel<<<blocks, threads, 0, st>>>(seq_lens, n_accepted, k_per_row, block_table,
+                                                  max_pages, page_size, B, free_top, ws);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    paged_apply_kernel<<<blocks, threads, 0, st>>>(seq_lens, n_accepted, k_per_row, block_table,
+                                                  max_pages, page_size, B, free_pages, free_top,
+                                                  free_capacity, ws);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    *err = std::string("paged kv_commit launch: ") + cudaGetErrorString(e);
+    return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}
+
 }  // namespace sv

@@ -64,6 +64,11 @@ int dynk_update_launch(void* state, int B, const int32_t* n_accepted, const int3
                        const int32_t* cap, int32_t* k_next, uint32_t* flags, void* stream,
                        std::string* err);
 
+int paged_commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* k_per_row,
+                        int32_t* block_table, int max_pages, int page_size, int32_t* free_pages,
+                        int32_t* free_top, int free_capacity, int B, uint32_t* ws, void* stream,
+                        std::string* err);
+
 int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
                   int K, uint32_t* flags, void* stream, std::string* err);
 

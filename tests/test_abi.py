@@ -146,3 +146,15 @@ def test_dynk_host_checks(lib):
     with pytest.raises(sb.SVError) as e:
         sb.sv_dynk_update(P, 4, P, P, None, P, None, 256, 0)
     assert e.value.status == sb.SV_ERR_WORKSPACE
+
+
+def test_kv_commit_paged_host_checks(lib):
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit_paged(P, P, P, P, 0, 16, P, P, 10, 4, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit_paged(P, P, None, P, 4, 16, P, P, 10, 4, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_ARG
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit_paged(P, P, P, P, 4, 16, P, P, 10, 4, P, 8, 0)
+    assert e.value.status == sb.SV_ERR_WORKSPACE
