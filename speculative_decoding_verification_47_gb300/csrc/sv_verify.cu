@@ -599,8 +599,8 @@ __device__ __noinline__ float masked_unit(const Weight& W, uint4 vt, uint4 vd, i
   return acc;
 }
 
-// Rows of the cut position as the finisher reads them (usually from L2: they
-// were streamed moments earlier).  Full units of both rows are read as 16-byte
+// The rows of a drawing item as the draw reads them a second time (from L2
+// when they are still there).  Full units of both rows are read as 16-byte
 // vectors when the rows share their 16-byte phase, else element by element.
 template <int ES>
 struct PairRead {
@@ -1981,7 +1981,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   __syncthreads();
   const bool skip = sh.skip != 0;
 
-  // ---- stream the slices: one pass per row, loads straight to registers ----
+  // ---- stream the slices: one pass per row, through the cp.async ring ----
   const int e0 = min(P.V, rank * P.slice_len), e1 = min(P.V, e0 + P.slice_len);
   RowSlice<ES> st, sd;
   st.init(P.tgt + (long long)b * P.t_seq + (long long)i * P.t_pos, e0, e1);
