@@ -132,7 +132,7 @@ def gumbel_draft_token(z_draft: np.ndarray, T: float, rng: np.random.Generator) 
     return int(np.argmax(z_draft / T + g))
 
 
-def _gen_sequence(b, B, K, V, dtype, k_b, T_b, sigma_b, mode_b, seeds):
+def _gen_sequence(b, B, K, V, dtype, k_b, T_b, sigma_b, mode_b, seeds, draft_scale=1.0):
     logit_seed, token_seed, uniform_seed = seeds
     rl = np.random.Generator(np.random.PCG64(np.random.SeedSequence([logit_seed, b])))
     rt = np.random.Generator(np.random.PCG64(np.random.SeedSequence([token_seed, b])))
@@ -153,7 +153,7 @@ def _gen_sequence(b, B, K, V, dtype, k_b, T_b, sigma_b, mode_b, seeds):
         else:
             tgt[i] = nan
         if i < K:
-            zd = zt + sigma_b * rl.standard_normal(V)
+            zd = (zt if draft_scale == 1.0 else draft_scale * zt) + sigma_b * rl.standard_normal(V)
             if i < k_b:
                 drf[i] = _stored(zd, dtype)
                 zd_dec = _decoded(drf[i], dtype)
@@ -183,11 +183,14 @@ def synth_verify(
     top_p: float = 1.0,
     seeds=(1000, 2000, 0),
     threads: int | None = None,
+    draft_scale: float = 1.0,
 ) -> VerifyInputs:
     """Draw a verify batch.  ``k_per_row``, ``temperature``, ``sigma`` and
     ``mode`` are per-row arrays (or scalars broadcast over B).  ``top_p`` is
     kept as the float32 value the verify call receives, so that the oracle
-    and the library cut at the same threshold."""
+    and the library cut at the same threshold.  ``draft_scale`` multiplies the
+    target logits before the draft noise is added (1 = the plain recipe; below 1
+    an under-confident draft)."""
     k_per_row = np.broadcast_to(np.asarray(k_per_row, dtype=np.int32), (B,)).copy()
     temperature = np.broadcast_to(np.asarray(temperature, dtype=np.float32), (B,)).copy()
     sigma = np.broadcast_to(np.asarray(sigma, dtype=np.float64), (B,)).copy()
@@ -202,7 +205,7 @@ def synth_verify(
     def work(b):
         t, d, x, u = _gen_sequence(b, B, K, V, dtype, int(k_per_row[b]),
                                    float(temperature[b]), float(sigma[b]),
-                                   int(mode[b]), seeds)
+                                   int(mode[b]), seeds, draft_scale)
         target[b], draft[b], tokens[b], uniforms[b] = t, d, x, u
 
     nthreads = threads or min(16, os.cpu_count() or 1)
