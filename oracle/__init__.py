@@ -20,6 +20,17 @@ Parity status of each function (what pins it, see tests/test_oracle_*.py):
                                invariance of RMSNorm
   analytics.*                  pinned: the pages' printed speedup table and
                                worked examples (tests/golden/)
+  sample.sample_row / sample_tokens
+                               pinned: exact u-grid frequencies against a
+                               plain-loop softmax and nucleus, greedy ties,
+                               padding and flags
+  dynk.DynK                    pinned: hand-worked crossings, exact
+                               thresholds, window expiry, caps, direct
+                               window sums over random histories
+  paged.kv_commit_paged        pinned: hand-worked page boundaries, per-token
+                               page ownership on random cases, all-or-nothing
+                               capacity
+Planted mistakes that the pins must catch: tests/test_oracle_mutations*.py.
 """
 
-from . import analytics, lmhead, verify  # noqa: F401
+from . import analytics, dynk, lmhead, paged, sample, verify  # noqa: F401
