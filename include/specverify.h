@@ -121,7 +121,9 @@ size_t sv_workspace_size(int B, int K, int V, sv_dtype dt);
  *                   i in 0..K-1; 0 strides select [B][K][V].  May be NULL only if
  *                   every row is greedy (mode non-NULL).
  *   dtype           SV_F32 or SV_BF16 (both logit tensors).
- *   B, K, V         sequences, max drafts (0 <= K <= 20), vocabulary (V >= 1).
+ *   B, K, V         sequences, max drafts (0 <= K <= 20), vocabulary (V >= 1);
+ *                   B * (K + 1) <= 134217727 (each position is one cluster of
+ *                   up to 16 CTAs and the grid holds at most 2^31 - 1).
  *   draft_tokens    device int32 [B][K]; only the first k_b of a row are read.
  *   k_per_row       device int32 [B] (each 0..K) or NULL for K everywhere.
  *   temperature     device float32 [B] (> 0 on sampled rows) or NULL for 1.0.
@@ -215,6 +217,7 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
  *               and sets SV_FLAG_BAD_N; if < 0 only n < 0 is rejected.
  *   workspace   the verify workspace (its flag word is OR-ed, not cleared);
  *               at least 256 bytes.
+ *   B           1 <= B <= 2^30, else SV_ERR_SHAPE.
  */
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream);
@@ -236,6 +239,9 @@ sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32
  *   workspace     device, >= 16 bytes, 16-byte aligned: word 0 is the flag
  *                 word (OR-ed, not cleared; e.g. the verify workspace), words 1
  *                 and 2 are scratch.
+ *   B, max_pages, page_size  1 <= B <= 2^30; lengths are int32 on the device,
+ *                 so (max_pages + 1) * page_size must fit in int32; else
+ *                 SV_ERR_SHAPE.
  * A sequence with n_accepted outside [0, k_b], or with L + k_b beyond its
  * table, is left unchanged and sets SV_FLAG_BAD_N.  If the call's releases
  * together would overflow the free stack, nothing changes and
@@ -271,6 +277,8 @@ sv_status sv_kv_commit_paged(int32_t* seq_lens, const int32_t* n_accepted,
  *   workspace   a flag word (e.g. the verify workspace): a round with k_used
  *               outside [0, 255] or n_accepted outside [0, k_used] is not
  *               recorded and sets SV_FLAG_BAD_N.
+ *   B           1 <= B <= 2^30 (sv_dynk_state_size returns 0 outside it, the
+ *               other two SV_ERR_SHAPE).
  */
 size_t sv_dynk_state_size(int B);
 sv_status sv_dynk_init(void* state, int B, int k0, void* stream);
@@ -290,6 +298,7 @@ sv_status sv_dynk_update(void* state, int B, const int32_t* n_accepted, const in
  * rows and one row per draft step (K = 1).
  *   draft_logits  device [B][K][V] of dtype; element strides per sequence and
  *                 per position as for sv_spec_verify (0 = dense).
+ *   B, K, V       each >= 1, B * K <= 134217727 (one cluster per row).
  *   k_per_row     device int32 [B] in [0, K], or NULL (= K).
  *   temperature   device float32 [B] (> 0 for sampled rows), or NULL (= 1).
  *   top_p         in (0, 1].

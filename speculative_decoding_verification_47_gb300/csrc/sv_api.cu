@@ -17,6 +17,8 @@ sv_status fail(sv_status s, const std::string& msg) {
 }
 
 constexpr int kMaxK = 20;
+constexpr long long kMaxItems = 0x7fffffffLL / 16;  // items per call: the grid is items x <= 16 CTAs
+constexpr int kMaxSeqs = 1 << 30;                   // one thread per sequence
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -36,17 +38,22 @@ size_t sv_lmhead_workspace_size(int M, int H) {
   return sv::lmhead_workspace_bytes(M, H);
 }
 
-static sv_status spec_verify_impl(const void* target_logits, int64_t target_seq_stride,
-                                  int64_t target_pos_stride, const void* draft_logits,
-                                  int64_t draft_seq_stride, int64_t draft_pos_stride,
-                                  sv_dtype dtype, int B, int K, int V, const int32_t* draft_tokens,
-                                  const int32_t* k_per_row, const float* temperature, float top_p,
-                                  const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
-                                  int32_t* n_accepted, float* diag, void* workspace,
-                                  size_t workspace_bytes, void* stream, int topp_draft) {
+// Host-checkable arguments of the three verify entry points; fills *L with
+// everything but the workspace.
+static sv_status verify_args(const void* target_logits, int64_t target_seq_stride,
+                             int64_t target_pos_stride, const void* draft_logits,
+                             int64_t draft_seq_stride, int64_t draft_pos_stride, sv_dtype dtype,
+                             int B, int K, int V, const int32_t* draft_tokens,
+                             const int32_t* k_per_row, const float* temperature, float top_p,
+                             const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                             int32_t* n_accepted, float* diag, void* stream,
+                             sv::VerifyLaunch* L) {
   if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
   if (B < 1 || K < 0 || K > kMaxK || V < 1)
     return fail(SV_ERR_SHAPE, "need B >= 1, 0 <= K <= 20, V >= 1");
+  // one cluster of up to 16 CTAs per (sequence, position): the grid must fit 2^31 - 1 blocks
+  if ((long long)B * (K + 1) > kMaxItems)
+    return fail(SV_ERR_SHAPE, "B * (K + 1) must be at most 134217727");
   if (!target_logits || !uniforms || !out_tokens || !n_accepted)
     return fail(SV_ERR_ARG, "target_logits, uniforms, out_tokens and n_accepted are required");
   if (K > 0 && !draft_tokens) return fail(SV_ERR_ARG, "draft_tokens is required when K > 0");
@@ -57,39 +64,56 @@ static sv_status spec_verify_impl(const void* target_logits, int64_t target_seq_
   if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)))
     return fail(SV_ERR_ARG, "logit pointers must be aligned to their element size");
   const long long Vl = V;
-  long long ts = target_seq_stride ? target_seq_stride : (long long)(K + 1) * Vl;
-  long long tp = target_pos_stride ? target_pos_stride : Vl;
-  long long ds = draft_seq_stride ? draft_seq_stride : (long long)K * Vl;
-  long long dp = draft_pos_stride ? draft_pos_stride : Vl;
+  const long long ts = target_seq_stride ? target_seq_stride : (long long)(K + 1) * Vl;
+  const long long tp = target_pos_stride ? target_pos_stride : Vl;
+  const long long ds = draft_seq_stride ? draft_seq_stride : (long long)K * Vl;
+  const long long dp = draft_pos_stride ? draft_pos_stride : Vl;
   if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
   if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
   if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
+  L->target = target_logits;
+  L->t_seq = ts;
+  L->t_pos = tp;
+  L->draft = draft_logits;
+  L->d_seq = ds;
+  L->d_pos = dp;
+  L->dtype = dtype;
+  L->B = B;
+  L->K = K;
+  L->V = V;
+  L->tokens = draft_tokens;
+  L->kpr = k_per_row;
+  L->temp = temperature;
+  L->top_p = top_p;
+  L->unif = uniforms;
+  L->mode = mode;
+  L->out = out_tokens;
+  L->nacc = n_accepted;
+  L->diag = diag;
+  L->workspace = nullptr;
+  L->stream = stream;
+  return SV_OK;
+}
+
+static sv_status spec_verify_impl(const void* target_logits, int64_t target_seq_stride,
+                                  int64_t target_pos_stride, const void* draft_logits,
+                                  int64_t draft_seq_stride, int64_t draft_pos_stride,
+                                  sv_dtype dtype, int B, int K, int V, const int32_t* draft_tokens,
+                                  const int32_t* k_per_row, const float* temperature, float top_p,
+                                  const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
+                                  int32_t* n_accepted, float* diag, void* workspace,
+                                  size_t workspace_bytes, void* stream, int topp_draft) {
+  sv::VerifyLaunch L;
+  const sv_status a = verify_args(target_logits, target_seq_stride, target_pos_stride,
+                                  draft_logits, draft_seq_stride, draft_pos_stride, dtype, B, K,
+                                  V, draft_tokens, k_per_row, temperature, top_p, uniforms, mode,
+                                  out_tokens, n_accepted, diag, stream, &L);
+  if (a != SV_OK) return a;
   if (!workspace || !aligned(workspace, 256))
     return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
   if (workspace_bytes < sv::verify_workspace_bytes(B, K))
     return fail(SV_ERR_WORKSPACE, "workspace smaller than sv_workspace_size()");
-  sv::VerifyLaunch L;
-  L.target = target_logits;
-  L.t_seq = ts;
-  L.t_pos = tp;
-  L.draft = draft_logits;
-  L.d_seq = ds;
-  L.d_pos = dp;
-  L.dtype = dtype;
-  L.B = B;
-  L.K = K;
-  L.V = V;
-  L.tokens = draft_tokens;
-  L.kpr = k_per_row;
-  L.temp = temperature;
-  L.top_p = top_p;
-  L.unif = uniforms;
-  L.mode = mode;
-  L.out = out_tokens;
-  L.nacc = n_accepted;
-  L.diag = diag;
   L.workspace = workspace;
-  L.stream = stream;
   L.topp_draft = topp_draft;
   std::string err;
   int s = sv::verify_launch(L, &err);
@@ -133,48 +157,12 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
                                  const int32_t* k_per_row, const float* temperature, float top_p,
                                  const float* uniforms, const uint8_t* mode, int32_t* out_tokens,
                                  int32_t* n_accepted, float* diag, void* stream) {
-  if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
-  if (B < 1 || K < 0 || K > kMaxK || V < 1)
-    return fail(SV_ERR_SHAPE, "need B >= 1, 0 <= K <= 20, V >= 1");
-  if (!target_logits || !uniforms || !out_tokens || !n_accepted)
-    return fail(SV_ERR_ARG, "target_logits, uniforms, out_tokens and n_accepted are required");
-  if (K > 0 && !draft_tokens) return fail(SV_ERR_ARG, "draft_tokens is required when K > 0");
-  if (K > 0 && !draft_logits && !mode)
-    return fail(SV_ERR_ARG, "draft_logits may be NULL only when every row is greedy (mode given)");
-  if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(SV_ERR_ARG, "top_p must be in (0, 1]");
-  const int es = dtype == SV_BF16 ? 2 : 4;
-  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)))
-    return fail(SV_ERR_ARG, "logit pointers must be aligned to their element size");
-  const long long Vl = V;
-  long long ts = target_seq_stride ? target_seq_stride : (long long)(K + 1) * Vl;
-  long long tp = target_pos_stride ? target_pos_stride : Vl;
-  long long ds = draft_seq_stride ? draft_seq_stride : (long long)K * Vl;
-  long long dp = draft_pos_stride ? draft_pos_stride : Vl;
-  if (ts < 0 || tp < 0 || ds < 0 || dp < 0) return fail(SV_ERR_SHAPE, "strides must be >= 0");
-  if (tp < Vl && K > 0) return fail(SV_ERR_SHAPE, "target position stride is smaller than V");
-  if (dp < Vl && K > 1) return fail(SV_ERR_SHAPE, "draft position stride is smaller than V");
   sv::VerifyLaunch L;
-  L.target = target_logits;
-  L.t_seq = ts;
-  L.t_pos = tp;
-  L.draft = draft_logits;
-  L.d_seq = ds;
-  L.d_pos = dp;
-  L.dtype = dtype;
-  L.B = B;
-  L.K = K;
-  L.V = V;
-  L.tokens = draft_tokens;
-  L.kpr = k_per_row;
-  L.temp = temperature;
-  L.top_p = top_p;
-  L.unif = uniforms;
-  L.mode = mode;
-  L.out = out_tokens;
-  L.nacc = n_accepted;
-  L.diag = diag;
-  L.workspace = nullptr;
-  L.stream = stream;
+  const sv_status a = verify_args(target_logits, target_seq_stride, target_pos_stride,
+                                  draft_logits, draft_seq_stride, draft_pos_stride, dtype, B, K,
+                                  V, draft_tokens, k_per_row, temperature, top_p, uniforms, mode,
+                                  out_tokens, n_accepted, diag, stream, &L);
+  if (a != SV_OK) return a;
   std::string err;
   int s = sv::verify_launch_noalloc(L, &err);
   if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
@@ -183,7 +171,7 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
 
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
                        int B, int K, void* workspace, size_t workspace_bytes, void* stream) {
-  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (B < 1 || B > kMaxSeqs) return fail(SV_ERR_SHAPE, "need 1 <= B <= 2^30");
   if (!seq_lens || !n_accepted) return fail(SV_ERR_ARG, "seq_lens and n_accepted are required");
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256)
     return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL, 256-byte aligned, >= 256 bytes");
@@ -199,8 +187,11 @@ sv_status sv_kv_commit_paged(int32_t* seq_lens, const int32_t* n_accepted,
                              int page_size, int32_t* free_pages, int32_t* free_top,
                              int free_capacity, int B, void* workspace, size_t workspace_bytes,
                              void* stream) {
-  if (B < 1 || max_pages < 1 || page_size < 1 || free_capacity < 0)
-    return fail(SV_ERR_SHAPE, "need B >= 1, max_pages >= 1, page_size >= 1, free_capacity >= 0");
+  if (B < 1 || B > kMaxSeqs || max_pages < 1 || page_size < 1 || free_capacity < 0)
+    return fail(SV_ERR_SHAPE, "need 1 <= B <= 2^30, max_pages >= 1, page_size >= 1, free_capacity >= 0");
+  // lengths and page counts are int32 on the device: a full table plus one page must fit
+  if ((long long)max_pages * page_size + page_size > 0x7fffffffLL)
+    return fail(SV_ERR_SHAPE, "(max_pages + 1) * page_size must fit in int32");
   if (!seq_lens || !n_accepted || !k_per_row || !block_table || !free_pages || !free_top)
     return fail(SV_ERR_ARG, "every array argument is required");
   if (!workspace || workspace_bytes < 16 || !aligned(workspace, 16))
@@ -213,10 +204,10 @@ sv_status sv_kv_commit_paged(int32_t* seq_lens, const int32_t* n_accepted,
   return SV_OK;
 }
 
-size_t sv_dynk_state_size(int B) { return B < 1 ? 0 : sv::dynk_state_bytes(B); }
+size_t sv_dynk_state_size(int B) { return B < 1 || B > kMaxSeqs ? 0 : sv::dynk_state_bytes(B); }
 
 sv_status sv_dynk_init(void* state, int B, int k0, void* stream) {
-  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (B < 1 || B > kMaxSeqs) return fail(SV_ERR_SHAPE, "need 1 <= B <= 2^30");
   if (!state || !aligned(state, 16)) return fail(SV_ERR_ARG, "state must be non-NULL and 16-byte aligned");
   std::string err;
   const int s = sv::dynk_init_launch(state, B, k0, stream, &err);
@@ -227,7 +218,7 @@ sv_status sv_dynk_init(void* state, int B, int k0, void* stream) {
 sv_status sv_dynk_update(void* state, int B, const int32_t* n_accepted, const int32_t* k_used,
                          const int32_t* cap, int32_t* k_next, void* workspace,
                          size_t workspace_bytes, void* stream) {
-  if (B < 1) return fail(SV_ERR_SHAPE, "need B >= 1");
+  if (B < 1 || B > kMaxSeqs) return fail(SV_ERR_SHAPE, "need 1 <= B <= 2^30");
   if (!state || !aligned(state, 16)) return fail(SV_ERR_ARG, "state must be non-NULL and 16-byte aligned");
   if (!n_accepted || !k_used || !k_next) return fail(SV_ERR_ARG, "n_accepted, k_used and k_next are required");
   if (!workspace || workspace_bytes < 4 || !aligned(workspace, 4))
@@ -247,8 +238,8 @@ sv_status sv_draft_sample(const void* draft_logits, int64_t seq_stride, int64_t 
                           const uint8_t* mode, int32_t* out_tokens, void* workspace,
                           size_t workspace_bytes, void* stream) {
   if (dtype != SV_F32 && dtype != SV_BF16) return fail(SV_ERR_DTYPE, "dtype must be SV_F32 or SV_BF16");
-  if (B < 1 || K < 1 || V < 1 || (long long)B * K > 0x7fffffffLL / 16)
-    return fail(SV_ERR_SHAPE, "need B >= 1, K >= 1, V >= 1");
+  if (B < 1 || K < 1 || V < 1) return fail(SV_ERR_SHAPE, "need B >= 1, K >= 1, V >= 1");
+  if ((long long)B * K > kMaxItems) return fail(SV_ERR_SHAPE, "B * K must be at most 134217727");
   if (!draft_logits || !uniforms || !out_tokens)
     return fail(SV_ERR_ARG, "draft_logits, uniforms and out_tokens are required");
   if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(SV_ERR_ARG, "top_p must be in (0, 1]");

@@ -75,6 +75,7 @@ def _verify(**kw):
     (dict(ws=None), sb.SV_ERR_WORKSPACE),
     (dict(ws=P + 16), sb.SV_ERR_WORKSPACE),
     (dict(wsb=16), sb.SV_ERR_WORKSPACE),
+    (dict(B=(1 << 27) // 21 + 1, K=20), sb.SV_ERR_SHAPE),  # grid of B*(K+1) clusters
 ])
 def test_spec_verify_host_checks(lib, kw, status):
     with pytest.raises(sb.SVError) as e:
@@ -158,3 +159,24 @@ def test_kv_commit_paged_host_checks(lib):
     with pytest.raises(sb.SVError) as e:
         sb.sv_kv_commit_paged(P, P, P, P, 4, 16, P, P, 10, 4, P, 8, 0)
     assert e.value.status == sb.SV_ERR_WORKSPACE
+    # lengths are int32 on the device: a full table plus one page must fit
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit_paged(P, P, P, P, (1 << 31) // 16 - 1, 16, P, P, 10, 4, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit_paged(P, P, P, P, 4, 16, P, P, 10, (1 << 30) + 1, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+
+
+def test_sequence_count_limits(lib):
+    assert sb.sv_dynk_state_size((1 << 30) + 1) == 0
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_dynk_init(P, (1 << 30) + 1, 4, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_kv_commit(P, P, None, (1 << 30) + 1, 3, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
+    with pytest.raises(sb.SVError) as e:
+        sb.sv_draft_sample(P, 0, 0, sb.SV_BF16, (1 << 27) // 8 + 1, 8, 100, None, None, 1.0, P,
+                           None, P, P, 256, 0)
+    assert e.value.status == sb.SV_ERR_SHAPE
