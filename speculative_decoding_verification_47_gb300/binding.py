@@ -120,10 +120,16 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(x):
+    """Device address of a tensor argument.  Every pointer of the ABI is a
+    device pointer, so a tensor elsewhere (a CPU or pinned host tensor) is
+    refused here rather than handed to a kernel as an address it cannot read."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    dev = getattr(x, "device", None)
+    if dev is not None and dev.type != "cuda":
+        raise ValueError(f"expected a CUDA tensor, got a tensor on {dev}")
     return x.data_ptr()
 
 

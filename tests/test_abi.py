@@ -180,3 +180,13 @@ def test_sequence_count_limits(lib):
         sb.sv_draft_sample(P, 0, 0, sb.SV_BF16, (1 << 27) // 8 + 1, 8, 100, None, None, 1.0, P,
                            None, P, P, 256, 0)
     assert e.value.status == sb.SV_ERR_SHAPE
+
+
+def test_host_tensors_are_refused(lib):
+    """A host tensor never reaches a device-pointer argument."""
+    import torch
+    host = torch.zeros(16, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        sb.sv_kv_commit(host, P, None, 4, 3, P, 256, 0)
+    with pytest.raises(ValueError):
+        sb.sv_read_device_flags(host.pin_memory() if torch.cuda.is_available() else host, 0)
