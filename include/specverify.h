@@ -23,6 +23,9 @@
  *     sequence's outputs become n_accepted = 0 and out_tokens = -1, and a bit
  *     is set in the workspace's flag word (SV_FLAG_*), readable with
  *     sv_read_device_flags.
+ *   - A process uses the library on one GPU: the kernels' launch attributes
+ *     are set once, on the first device the process launches on, so a call
+ *     on another device may fail with SV_ERR_CUDA (it never runs wrongly).
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
