@@ -1,0 +1,57 @@
+"""bench.py's JSON line, checked on the CPU through its reference arm (the
+float64 oracle on the host cores; no GPU needed): the keys and types every
+line carries, the warm-up floor, and that ranks other than 0 of a multi-rank
+launch exit without work or output."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(*argv, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *argv], cwd=ROOT,
+                       env=e, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return r.stdout
+
+
+def _line(out):
+    lines = [l for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("workload,unit", [("c1", "positions/s"), ("s2", "tokens/s")])
+def test_reference_line_carries_the_contract_keys(workload, unit):
+    d = _line(_bench("--impl", "reference", "--workload", workload, "--steps", "1",
+                     "--warmup", "1", "--ref-sample", "2"))
+    assert d["impl"] == "reference"
+    assert isinstance(d["metric"], str) and d["metric"]
+    assert d["unit"] == unit and d["value"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["warmup"] == 3  # raised to the floor of three warm-up steps
+    assert d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["dtype"] == "f64" and d["data"] == "synthetic"
+    cfg = d["config"]
+    assert isinstance(cfg["workload"], str) and cfg["workload"]
+    assert not {"model", "seq_len", "global_batch"} & set(cfg)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == unit
+    assert cb["cores"] >= 1 and isinstance(cb["sample"], str) and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e == {"value": d["value"], "unit": unit, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    out = _bench("--impl", "reference", "--workload", "c1", "--steps", "1", "--warmup", "3",
+                 "--ref-sample", "2", env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert out.strip() == ""
