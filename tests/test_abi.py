@@ -190,3 +190,13 @@ def test_host_tensors_are_refused(lib):
         sb.sv_kv_commit(host, P, None, 4, 3, P, 256, 0)
     with pytest.raises(ValueError):
         sb.sv_read_device_flags(host.pin_memory() if torch.cuda.is_available() else host, 0)
+
+
+def test_noalloc_limits_match_the_header(lib):
+    """The header's examples of batches the allocation-free call accepts
+    (workspace <= 2 MiB) and refuses, checked on sv_workspace_size."""
+    cap = 2 << 20
+    for B, K in [(4096, 20), (8192, 14), (16384, 6)]:
+        assert sb.sv_workspace_size(B, K, 128256, sb.SV_BF16) <= cap, (B, K)
+    for B, K in [(8192, 15), (16384, 7)]:
+        assert sb.sv_workspace_size(B, K, 128256, sb.SV_BF16) > cap, (B, K)
