@@ -46,7 +46,15 @@ WORKLOADS = {
            "T=1, sampled; + kv_commit"),
     "s2": ("draft-side sampler on the headline batch's draft rows: B=256, K=8, ragged "
            "k_b~U{2..8}, V=128256 bf16 logits, T_b in {0.1,0.7,1.0}, one uniform per token"),
+    "c3t": ("the c3 batch through the target-only top-p call: top_p=0.9 truncates the target "
+            "rows only, the draft rows enter untruncated; + kv_commit"),
+    "kvp": ("paged KV commit after a round: B=1024 sequences, block tables of 64 pages of 16 "
+            "tokens, lengths ~U[100,512), k_b~U{2..8}, n_b~U{0..k_b}"),
+    "dynk": ("dynamic-k controller update: B=256 sequences, 64-round windows, k_used~U{2..8}, "
+             "n~U{0..k_used} per round"),
 }
+# workloads that run the c3 rows through another entry point
+ROW_WORKLOAD = {"c3t": "c3"}
 COPIES = 3
 
 # DRAM bytes (read + written) per launch of each workload's dominant kernel,
@@ -146,6 +154,8 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 def _oracle_worker(args):
     name, B, seqs = args
+    topp_draft = name != "c3t"
+    name = ROW_WORKLOAD.get(name, name)
     sys.path.insert(0, ROOT)
     import numpy as np
     from oracle import verify as ov
@@ -158,7 +168,7 @@ def _oracle_worker(args):
         kb = int(spec.k_per_row[b])
         ov.verify_sequence(ov._LazyRows(t, spec.dtype), ov._LazyRows(d, spec.dtype), x, kb,
                            spec.K, spec.V, float(spec.temperature[b]), spec.top_p,
-                           u.astype(np.float64), int(spec.mode[b]))
+                           u.astype(np.float64), int(spec.mode[b]), topp_draft)
         pos += kb
     return pos, time.perf_counter() - t0
 
@@ -226,16 +236,18 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         workers = min(16, len(os.sched_getaffinity(0)))
-        Bw = args.B or wl.row_spec(args.workload).B
+        Bw = args.B or wl.row_spec(ROW_WORKLOAD.get(args.workload, args.workload)).B
         pos, wall, used = cpu_oracle(args.workload, Bw, args.cpu_sample, workers)
         cpu = {"value": pos / wall, "unit": "positions/s", "cores": used, "kind": "oracle",
                "sample": f"{min(args.cpu_sample, Bw)} of the {Bw} sequences of the same workload "
                          f"(evenly spaced), float64 oracle, {used} spawn workers, "
                          f"wall {wall:.2f} s"}
 
-    w = wl.config_by_name(args.workload, args.B)
+    w = wl.config_by_name(ROW_WORKLOAD.get(args.workload, args.workload), args.B)
     B, K, V = w.B, w.K, w.V
     es = 2 if w.dtype == wl.BF16 else 4
+    # c3t: top-p on the target rows only (the draft untruncated)
+    verify = sb.sv_spec_verify_target_topp if args.workload == "c3t" else sb.sv_spec_verify
     svdt = sb.SV_BF16 if w.dtype == wl.BF16 else sb.SV_F32
     top_p = w.top_p
     dev = torch.device("cuda", local)
@@ -258,7 +270,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(c):
-        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
+        verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
         sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
 
@@ -293,7 +305,7 @@ def run_gpu(args):
     for it in range(args.steps):
         c = it % COPIES
         ev[it][0].record(stream)
-        sb.sv_spec_verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
+        verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
         ev[it][1].record(stream)
         sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
@@ -325,7 +337,7 @@ def run_gpu(args):
             drfs[0].copy_(h_d, non_blocking=True)
             for d_, h_ in zip(d_small, h_small):
                 d_.copy_(h_, non_blocking=True)
-            sb.sv_spec_verify(tgts[0], 0, 0, drfs[0], 0, 0, svdt, B, K, V, tok, kpr, tmp,
+            verify(tgts[0], 0, 0, drfs[0], 0, 0, svdt, B, K, V, tok, kpr, tmp,
                               top_p, uni, mode, out, nacc, None, ws, wsb, stream)
             sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
             o_out.copy_(out, non_blocking=True)
@@ -748,6 +760,334 @@ def run_gpu_s2(args):
         pg.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# Round bookkeeping: the paged-KV commit and the dynamic-k update.  Both run
+# one thread per sequence and are launch-latency bound; each call is timed
+# with CUDA events on its stream.
+# --------------------------------------------------------------------------
+def _small_call_line(args, name, metric, unit, units, call_ms, ms_step, alg_bytes, kernel, cfg,
+                     cpu, e2e, launches, clk, flags, world):
+    peak, psrc = peaks()
+    achieved = alg_bytes / (call_ms * 1e-3) / 1e9
+    return {
+        "metric": metric,
+        "value": units * world / (ms_step * 1e-3),
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": dict({"workload": WORKLOADS[name], "name": name,
+                        "parallelism": f"replicas x{world}"}, **cfg),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": kernel,
+                     "launch_ms": call_ms, "peak_source": psrc,
+                     "note": "one thread per sequence: launch-latency bound, far from the "
+                             "HBM roof at any batch a round has"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "device_flags": flags,
+    }
+
+
+def _gpu_setup(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from speculative_decoding_verification_47_gb300 import build as bld
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    if pg is not None:
+        pg.barrier()
+    return world, rank, local, pg
+
+
+def _timed_calls(args, stream, call, between=None, pg=None):
+    """Warm-up, then args.steps calls, each bracketed by CUDA events on the
+    launching stream; ``between`` (state restore) runs outside the events.
+    Returns (mean call ms, clocks)."""
+    import torch
+    for it in range(args.warmup):
+        if between:
+            between(it)
+        call(it)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.25)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for it in range(args.steps):
+        if between:
+            between(args.warmup + it)
+        ev[it][0].record(stream)
+        call(args.warmup + it)
+        ev[it][1].record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if pg is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, clk
+
+
+def _e2e_time(args, stream, e2e_step, pg=None):
+    import torch
+    steps = max(3, min(args.steps, 20))
+    e2e_step(0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        e2e_step(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ems = a.elapsed_time(b)
+    if pg is not None:
+        t = torch.tensor([ems], dtype=torch.float64, device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ems = float(t.item())
+    return ems / steps, steps
+
+
+def run_gpu_kvp(args):
+    """sv_kv_commit_paged on one round's state; the state is restored by
+    device copies between calls, outside the timed events."""
+    import numpy as np
+    import torch
+    world, rank, local, pg = _gpu_setup(args)
+    from speculative_decoding_verification_47_gb300 import binding as sb
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    r = wl.paged_round()
+    B, maxp = r.block_table.shape
+    P, cap = r.page_size, r.pool_pages
+    dev = torch.device("cuda", local)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    lens0, table0, n, k = d(r.seq_lens), d(r.block_table), d(r.n_accepted), d(r.k_per_row)
+    lens, table = lens0.clone(), table0.clone()
+    free = torch.full((cap,), -1, dtype=torch.int32, device=dev)
+    top = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import paged as opg
+        calls, t0 = 0, time.perf_counter()
+        while calls < 3 or time.perf_counter() - t0 < 2.0:
+            opg.kv_commit_paged(r.seq_lens, r.n_accepted, r.k_per_row, r.block_table, P, 0, cap)
+            calls += 1
+        wall = time.perf_counter() - t0
+        cpu = {"value": B * calls / wall, "unit": "sequences/s", "cores": 1, "kind": "oracle",
+               "sample": f"the whole batch of {B} sequences, {calls} calls, Python oracle, "
+                         f"one core, wall {wall:.2f} s"}
+
+    def restore(_):
+        lens.copy_(lens0)
+        table.copy_(table0)
+        top.zero_()
+
+    def call(_):
+        sb.sv_kv_commit_paged(lens, n, k, table, maxp, P, free, top, cap, B, ws, 256, stream)
+
+    call_ms, clk = _timed_calls(args, stream, call, restore, pg)
+    flags = sb.sv_read_device_flags(ws)
+    released = int(top.item())
+    # lengths read and written, n and k read; each table row scanned once;
+    # every release writes a table entry and a free-stack slot
+    alg = B * 16 + B * maxp * 4 + released * 8
+
+    e2e = None
+    if not args.no_e2e:
+        h_in = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                for a in (r.seq_lens, r.n_accepted, r.k_per_row, r.block_table)]
+        d_in = [lens, n, k, table]
+        outs = [(torch.empty(t.shape, dtype=torch.int32).pin_memory(), t)
+                for t in (lens, table, free, top)]
+
+        def e2e_step(_):
+            for d_, h_ in zip(d_in, h_in):
+                d_.copy_(h_, non_blocking=True)
+            top.zero_()
+            call(0)
+            for h_, d_ in outs:
+                h_.copy_(d_, non_blocking=True)
+
+        ems, steps = _e2e_time(args, stream, e2e_step, pg)
+        e2e = {"value": B * world / (ems * 1e-3), "unit": "sequences/s",
+               "h2d_bytes_per_step": int(sum(x.numel() * 4 for x in h_in)) + 4,
+               "d2h_bytes_per_step": int(sum(h_.numel() * 4 for h_, _ in outs)),
+               "steps": steps}
+
+    line = _small_call_line(
+        args, "kvp", "paged KV commits/s (sequences) at 1 GPU", "sequences/s", B, call_ms,
+        call_ms, alg, "paged_count_kernel + paged_apply_kernel",
+        {"B": B, "max_pages": int(maxp), "page_size": P, "released_pages": released,
+         "bytes_algorithmic_per_call": alg,
+         "l2": "state restored between calls by device copies outside the timed events; "
+               "the 0.3 MB state stays in L2"},
+        cpu, e2e, 2 * args.steps, clk, flags, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_gpu_dynk(args):
+    """sv_dynk_update over a history of rounds (one update per call)."""
+    import numpy as np
+    import torch
+    world, rank, local, pg = _gpu_setup(args)
+    from speculative_decoding_verification_47_gb300 import binding as sb
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    B = 256
+    rounds = args.warmup + args.steps + 1
+    nh, kh = wl.dynk_history(B, rounds)
+    dev = torch.device("cuda", local)
+    dn = torch.from_numpy(nh).to(dev)
+    dk = torch.from_numpy(kh).to(dev)
+    state = torch.zeros(sb.sv_dynk_state_size(B), dtype=torch.uint8, device=dev)
+    kn = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sb.sv_dynk_init(state, B, 4, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import dynk as odk
+        ctl = [odk.DynK(4) for _ in range(B)]
+        t0 = time.perf_counter()
+        for i in range(rounds):
+            for b in range(B):
+                ctl[b].update(int(nh[i, b]), int(kh[i, b]))
+        wall = time.perf_counter() - t0
+        cpu = {"value": B * rounds / wall, "unit": "sequences/s", "cores": 1, "kind": "oracle",
+               "sample": f"the same {rounds} rounds of {B} controllers, Python oracle, one core, "
+                         f"wall {wall:.2f} s"}
+
+    def call(i):
+        sb.sv_dynk_update(state, B, dn[i], dk[i], None, kn, ws, 256, stream)
+
+    call_ms, clk = _timed_calls(args, stream, call, None, pg)
+    flags = sb.sv_read_device_flags(ws)
+    # per sequence: seven int32 state words read and written, one ring byte
+    # pair read and written, n and k_used read, k_next written
+    alg = B * 72
+
+    e2e = None
+    if not args.no_e2e:
+        h_n = torch.from_numpy(nh[-1].copy()).pin_memory()
+        h_k = torch.from_numpy(kh[-1].copy()).pin_memory()
+        n1, k1 = dn[-1], dk[-1]
+        o_k = torch.empty(B, dtype=torch.int32).pin_memory()
+
+        def e2e_step(_):
+            n1.copy_(h_n, non_blocking=True)
+            k1.copy_(h_k, non_blocking=True)
+            sb.sv_dynk_update(state, B, n1, k1, None, kn, ws, 256, stream)
+            o_k.copy_(kn, non_blocking=True)
+
+        ems, steps = _e2e_time(args, stream, e2e_step, pg)
+        e2e = {"value": B * world / (ems * 1e-3), "unit": "sequences/s",
+               "h2d_bytes_per_step": 2 * B * 4, "d2h_bytes_per_step": B * 4, "steps": steps}
+
+    line = _small_call_line(
+        args, "dynk", "dynamic-k controller updates/s (sequences) at 1 GPU", "sequences/s", B,
+        call_ms, call_ms, alg, "dynk_update_kernel",
+        {"B": B, "window": 64, "bytes_algorithmic_per_call": alg,
+         "l2": f"controller state {sb.sv_dynk_state_size(B)} bytes, resident in L2"},
+        cpu, e2e, args.steps, clk, flags, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def _reference_line(args, name, metric, unit, value, ms_step, cfg, sample):
+    return {
+        "impl": "reference",
+        "metric": metric,
+        "value": value,
+        "unit": unit,
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int64",
+        "data": "synthetic",
+        "config": dict({"workload": WORKLOADS[name], "name": name, "parallelism": "host cores"},
+                       **cfg),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_kvp(args):
+    """The paged-commit oracle on the whole round, one call per step."""
+    from oracle import paged as opg
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    r = wl.paged_round()
+    B, maxp = r.block_table.shape
+    wall = 0.0
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        opg.kv_commit_paged(r.seq_lens, r.n_accepted, r.k_per_row, r.block_table, r.page_size, 0,
+                            r.pool_pages)
+        if it >= args.warmup:
+            wall += time.perf_counter() - t0
+    print(json.dumps(_reference_line(
+        args, "kvp", "paged KV commits/s (sequences) at 1 GPU", "sequences/s",
+        B * args.steps / wall, wall / args.steps * 1e3,
+        {"B": B, "max_pages": int(maxp), "page_size": r.page_size},
+        f"each step: the whole batch of {B} sequences, Python oracle, one core")), flush=True)
+
+
+def run_reference_dynk(args):
+    """The controller oracle, one round of B updates per step."""
+    from oracle import dynk as odk
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    B = 256
+    nh, kh = wl.dynk_history(B, args.warmup + args.steps)
+    ctl = [odk.DynK(4) for _ in range(B)]
+    wall = 0.0
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for b in range(B):
+            ctl[b].update(int(nh[it, b]), int(kh[it, b]))
+        if it >= args.warmup:
+            wall += time.perf_counter() - t0
+    print(json.dumps(_reference_line(
+        args, "dynk", "dynamic-k controller updates/s (sequences) at 1 GPU", "sequences/s",
+        B * args.steps / wall, wall / args.steps * 1e3, {"B": B, "window": 64},
+        f"each step: one round of {B} controllers, Python oracle, one core")), flush=True)
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -768,7 +1108,11 @@ def run_reference(args):
         return run_reference_c4(args)
     if args.workload == "s2":
         return run_reference_s2(args)
-    spec = wl.row_spec(args.workload, args.B)
+    if args.workload == "kvp":
+        return run_reference_kvp(args)
+    if args.workload == "dynk":
+        return run_reference_dynk(args)
+    spec = wl.row_spec(ROW_WORKLOAD.get(args.workload, args.workload), args.B)
     workers = min(16, len(os.sched_getaffinity(0)))
     for _ in range(args.warmup):
         cpu_oracle(args.workload, spec.B, workers, workers)  # one sequence per worker
@@ -912,6 +1256,10 @@ def main():
         run_gpu_c4(args)
     elif args.workload == "s2":
         run_gpu_s2(args)
+    elif args.workload == "kvp":
+        run_gpu_kvp(args)
+    elif args.workload == "dynk":
+        run_gpu_dynk(args)
     else:
         run_gpu(args)
 

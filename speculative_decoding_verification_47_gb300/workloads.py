@@ -402,3 +402,47 @@ def draw_draft_tokens(draft_stored: np.ndarray, dtype: str, k_per_row, temperatu
             out[b, i] = (int(np.argmax(z)) if int(mode[b]) == GREEDY
                          else gumbel_draft_token(z, float(temperature[b]), r))
     return out
+
+
+# ----------------------------------------------------------------------------
+# Round bookkeeping around the verify step: paged KV cache, dynamic k
+# ----------------------------------------------------------------------------
+
+@dataclass
+class PagedRound:
+    """One round's paged-KV state before the commit: sequence b holds
+    seq_lens[b] committed tokens, its k_per_row[b] drafts were written after
+    them, and block_table[b] lists the pages that cover all of those tokens
+    (-1 past them); n_accepted[b] in [0, k_b] came back from verification."""
+    seq_lens: np.ndarray
+    n_accepted: np.ndarray
+    k_per_row: np.ndarray
+    block_table: np.ndarray
+    page_size: int
+    pool_pages: int
+
+
+def paged_round(B: int = 1024, max_pages: int = 64, page_size: int = 16,
+                seed: int = 4100) -> PagedRound:
+    """Lengths ~U[100, max_pages*page_size/2), k_b ~U{2..8}, n_b ~U{0..k_b};
+    page ids drawn without replacement from a pool of B*max_pages pages."""
+    r = np.random.Generator(np.random.PCG64(seed))
+    L = r.integers(100, max_pages * page_size // 2, size=B).astype(np.int32)
+    k = r.integers(2, 9, size=B).astype(np.int32)
+    n = np.array([r.integers(0, kb + 1) for kb in k], dtype=np.int32)
+    ids = r.permutation(B * max_pages).astype(np.int32)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    for b in range(B):
+        used = -(-(int(L[b]) + int(k[b])) // page_size)
+        table[b, :used] = ids[b * max_pages: b * max_pages + used]
+    return PagedRound(L, n, k, table, page_size, B * max_pages)
+
+
+def dynk_history(B: int = 256, rounds: int = 64, seed: int = 4200):
+    """A history of rounds for B controllers: k_used ~U{2..8} and
+    n_accepted ~U{0..k_used} per (round, sequence), as int32
+    [rounds, B] arrays."""
+    r = np.random.Generator(np.random.PCG64(seed))
+    k = r.integers(2, 9, size=(rounds, B)).astype(np.int32)
+    n = (r.uniform(size=(rounds, B)) * (k + 1)).astype(np.int32)
+    return n, k

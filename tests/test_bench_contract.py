@@ -28,8 +28,10 @@ def _line(out):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload,unit", [("c1", "positions/s"), ("s2", "tokens/s")])
-def test_reference_line_carries_the_contract_keys(workload, unit):
+@pytest.mark.parametrize("workload,unit,dtype", [
+    ("c1", "positions/s", "f64"), ("s2", "tokens/s", "f64"),
+    ("kvp", "sequences/s", "int64"), ("dynk", "sequences/s", "int64")])
+def test_reference_line_carries_the_contract_keys(workload, unit, dtype):
     d = _line(_bench("--impl", "reference", "--workload", workload, "--steps", "1",
                      "--warmup", "1", "--ref-sample", "2"))
     assert d["impl"] == "reference"
@@ -39,7 +41,7 @@ def test_reference_line_carries_the_contract_keys(workload, unit):
     assert d["warmup"] == 3  # raised to the floor of three warm-up steps
     assert d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert d["scaling"] == "weak" and d["vs_baseline"] is None
-    assert d["dtype"] == "f64" and d["data"] == "synthetic"
+    assert d["dtype"] == dtype and d["data"] == "synthetic"
     cfg = d["config"]
     assert isinstance(cfg["workload"], str) and cfg["workload"]
     assert not {"model", "seq_len", "global_batch"} & set(cfg)

@@ -76,3 +76,20 @@ def test_row_spec_regenerates_the_batch_sequences():
             np.testing.assert_array_equal(d, w.draft[b])
             np.testing.assert_array_equal(x, w.draft_tokens[b])
             np.testing.assert_array_equal(u, w.uniforms[b])
+
+
+def test_paged_round_tables_cover_each_sequence_exactly():
+    r = wl.paged_round(B=64, max_pages=32, page_size=16, seed=7)
+    ids = r.block_table[r.block_table >= 0]
+    assert len(np.unique(ids)) == len(ids) and ids.max() < r.pool_pages
+    for b in range(64):
+        need = -(-(int(r.seq_lens[b]) + int(r.k_per_row[b])) // 16)
+        assert np.all(r.block_table[b, :need] >= 0) and np.all(r.block_table[b, need:] == -1)
+        assert 0 <= r.n_accepted[b] <= r.k_per_row[b] and 2 <= r.k_per_row[b] <= 8
+
+
+def test_dynk_history_ranges():
+    n, k = wl.dynk_history(B=32, rounds=100, seed=3)
+    assert n.shape == k.shape == (100, 32) and n.dtype == k.dtype == np.int32
+    assert k.min() >= 2 and k.max() <= 8 and n.min() >= 0 and np.all(n <= k)
+    assert len(np.unique(n)) == 9  # every count 0..8 occurs
