@@ -10,7 +10,7 @@ follows the acceptance rate alpha measured over a sliding window of the last
 0.7, k shrinks by one; k stays within [2, 8]; with long contexts k is
 shortened further, and below 2 speculation is switched off.
 
-Readings (also listed in the design doc):
+Readings (the points the pages leave open, and the reading taken):
   R24 alpha over the window = tokens accepted / tokens proposed over the last
       64 rounds in which the sequence proposed (k_b > 0); rounds without a
       proposal do not enter the window.

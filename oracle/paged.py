@@ -10,7 +10,7 @@ Sources: "Self-speculative decoding with layer skip and KV reuse" (xdnf.cn),
 paged KV cache the rollback is page-granular, and positions that straddle a
 page boundary are the usual source of bugs).
 
-Readings (also listed in the design doc):
+Readings (the points the pages leave open, and the reading taken):
   R29 the cache of sequence b is a list of pages of P tokens (block_table[b],
       page ids, -1 = none).  At the start of the round it holds L_b tokens;
       the drafts were written at L_b .. L_b + k_b - 1.  After verification the

@@ -13,7 +13,7 @@ Sources (pages cited by title and section):
   [SSD] "Self-speculative decoding with layer skip and KV reuse" (xdnf.cn),
         §3.2, §4.2: the layer-skip draft produces k candidates the same way.
 
-Readings (also listed in the design doc):
+Readings (the points the pages leave open, and the reading taken):
   R22 one uniform per sampled position (column i of a [B, K] array); the token
       is the verify step's inverse CDF in index order (R5) over the processed
       row p' (R6, R8); greedy rows take the argmax, lowest index on ties (R11).

@@ -14,7 +14,7 @@ Sources (pages cited by title and section):
 Notation: p = target distribution, q = draft distribution ([SD §2.1],
 [SSD §2.4]; the FlashSpec page swaps the letters, we do not).
 
-Readings of points the pages leave open (each also listed in the design doc):
+Readings of points the pages leave open:
   R2  accept iff u < min(1, p(x)/q(x)), strict '<' (the comparison operator is
       lost in the extracted code of [SSD §4.3]); with u < 1 this equals u < r.
   R3  q(x) = 0 gives ratio 0, i.e. rejection ([SSD §4.3] code).
