@@ -66,3 +66,27 @@ def test_dynk_init_clamps():
         out = torch.empty(B, dtype=torch.int32, device="cuda")
         sb.sv_dynk_update(state, B, z, z, None, out, ws, 256, None)
         assert out.cpu().numpy().tolist() == [want] * B
+
+
+def test_dynk_bench_workload():
+    """The history bench.py times at its defaults (--workload dynk: 20 warm-up
+    rounds, 2000 timed rounds and one more): B=256 controllers, k_used ~U{2..8},
+    n ~U{0..k_used}; k_next identical to the oracle in every round."""
+    import torch
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    B, R = 256, 2021
+    nh, kh = wl.dynk_history(B, R)
+    state = torch.zeros(sb.sv_dynk_state_size(B), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    sb.sv_dynk_init(state, B, 4, None)
+    dn = torch.from_numpy(nh).cuda()
+    dk = torch.from_numpy(kh).cuda()
+    outs = torch.full((R, B), -7, dtype=torch.int32, device="cuda")
+    for r in range(R):
+        sb.sv_dynk_update(state, B, dn[r], dk[r], None, outs[r], ws, 256, None)
+    got = outs.cpu().numpy()
+    ctl = [dynk.DynK(4) for _ in range(B)]
+    ref = np.array([[c.update(int(nh[r, b]), int(kh[r, b])) for b, c in enumerate(ctl)]
+                    for r in range(R)], np.int32)
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+    assert sb.sv_read_device_flags(ws) == 0

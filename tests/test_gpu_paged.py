@@ -73,3 +73,16 @@ def test_paged_commit_capacity_all_or_nothing():
     assert np.array_equal(lens, L) and np.array_equal(tab, table)
     lens, tab, rel, top, flags = _run(L, n, k, table, P, 3, 3 + need)
     assert flags == 0 and top == 3 + need and sorted(rel.tolist()) == sorted(rr)
+
+
+def test_paged_commit_bench_workload():
+    """The round bench.py times (--workload kvp): B=1024 sequences, 64 pages
+    of 16 tokens, lengths ~U[100, 512), k_b ~U{2..8}."""
+    from speculative_decoding_verification_47_gb300 import workloads as wl
+    r = wl.paged_round()
+    args = (r.seq_lens, r.n_accepted, r.k_per_row, r.block_table, r.page_size, 0, r.pool_pages)
+    lens, tab, rel, top, flags = _run(*args)
+    rl, rt, rr, rtop, rflags = opg.kv_commit_paged(*args)
+    assert flags == rflags == 0
+    assert np.array_equal(lens, np.array(rl)) and np.array_equal(tab, np.array(rt))
+    assert sorted(rel.tolist()) == sorted(rr) and top == rtop == len(rr) > 0
