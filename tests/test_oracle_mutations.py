@@ -101,3 +101,20 @@ def test_strict_accept_comparison_is_pinned(monkeypatch):
     monkeypatch.setattr(ov, "_uniform_ok", lambda u: u < 1.0)
     with pytest.raises(AssertionError):
         pins.test_error_rows_and_laziness()
+
+
+def test_target_only_flag_is_pinned(monkeypatch):
+    """Target-only top-p leaves the output law at p' whatever q is, so only
+    the acceptance law can show a draft that was truncated after all: an
+    oracle that ignores topp_draft=False must fail the target-only pin."""
+    orig = ov.verify_sequence
+
+    def always_both(*args, topp_draft=True, **kw):
+        return orig(*args, topp_draft=True, **kw)
+
+    pins.test_enumeration_target_only_top_p("top_p", 1)  # passes unmutated
+    monkeypatch.setattr(ov, "verify_sequence", always_both)
+    with pytest.raises(AssertionError):
+        for case in ("top_p", "top_p_ties"):
+            for k in (1, 2):
+                pins.test_enumeration_target_only_top_p(case, k)
