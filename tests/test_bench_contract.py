@@ -57,3 +57,37 @@ def test_reference_arm_other_ranks_exit_without_work():
     out = _bench("--impl", "reference", "--workload", "c1", "--steps", "1", "--warmup", "3",
                  "--ref-sample", "2", env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert out.strip() == ""
+
+
+def test_clock_sampler_reads_clocks_and_throttle_reasons():
+    """The clocks object of the JSON line: the median SM clock under load, the
+    maximum, and every throttle reason reported active in any sample."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cs = bench.ClockSampler(0)
+    cs.proc = type("P", (), {"terminate": lambda self: None, "wait": lambda self, timeout=None: 0,
+                             "kill": lambda self: None})()
+    cs.lines = [
+        "2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "1980, 2070, 0x4, Not Active, Not Active, Not Active, Active",
+        "2070, 2070, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+        "[N/A], 2070, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    clk = cs.stop()
+    assert clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"] and clk["samples"] == 3
+    cs.lines = ["2070, 2070, 0x0, Active, Not Active, Active, Not Active"]
+    assert bench.ClockSampler.stop(cs)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
+    """roofline.traffic comes from an ncu capture and is dropped (None) as soon
+    as the kernel source differs from the one the capture was taken on."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.traffic_for("c2", 123.0) == 123.0  # an explicit override
+    assert bench.traffic_for("no-such-workload", None) is None
+    src, digest, value = bench.MEASURED_TRAFFIC["c2"]
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "c2", (src, "0" * 16, value))
+    assert bench.traffic_for("c2", None) is None
