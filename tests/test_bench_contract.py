@@ -29,7 +29,7 @@ def _line(out):
 
 
 @pytest.mark.parametrize("workload,unit,dtype", [
-    ("c1", "positions/s", "f64"), ("s2", "tokens/s", "f64"),
+    ("c1", "positions/s", "f64"), ("s2", "tokens/s", "f64"), ("c3t", "positions/s", "f64"),
     ("kvp", "sequences/s", "int64"), ("dynk", "sequences/s", "int64")])
 def test_reference_line_carries_the_contract_keys(workload, unit, dtype):
     d = _line(_bench("--impl", "reference", "--workload", workload, "--steps", "1",
