@@ -9,7 +9,11 @@ rotated over three identical copies (3.3 GB > the 129 MB L2) so no step
 reuses data cached by the previous one.  ``--workload c1|c3`` times the
 other batch workloads the same way (c3: half greedy, top_p = 0.9);
 ``--workload c4`` times the layer-skip step: draft and target logits from
-hidden states through sv_lmhead_rmsnorm (tcgen05 GEMM), then verify + commit.
+hidden states through sv_lmhead_rmsnorm (tcgen05 GEMM), then verify + commit;
+it runs on one GPU per process only and exits with an error under a
+multi-rank launch.  On one GPU the headline run (c2) then also times the
+LM head (c4), the top-p batch (c3) and the draft sampler (s2) in the same
+process and reports them under "secondary" (``--no-secondary`` skips them).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle on bounded samples of the same workload instead.  Under torchrun each
@@ -272,7 +276,7 @@ def run_gpu(args):
     def step(c):
         verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
-        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+        sb.sv_kv_commit(seq, nacc, cap, kpr, B, K, ws, wsb, stream)
 
     for it in range(args.warmup):
         step(it % COPIES)
@@ -308,7 +312,7 @@ def run_gpu(args):
         verify(tgts[c], 0, 0, drfs[c], 0, 0, svdt, B, K, V, tok, kpr, tmp, top_p,
                           uni, mode, out, nacc, None, ws, wsb, stream)
         ev[it][1].record(stream)
-        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+        sb.sv_kv_commit(seq, nacc, cap, kpr, B, K, ws, wsb, stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if pg is not None:
@@ -339,7 +343,7 @@ def run_gpu(args):
                 d_.copy_(h_, non_blocking=True)
             verify(tgts[0], 0, 0, drfs[0], 0, 0, svdt, B, K, V, tok, kpr, tmp,
                               top_p, uni, mode, out, nacc, None, ws, wsb, stream)
-            sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+            sb.sv_kv_commit(seq, nacc, cap, kpr, B, K, ws, wsb, stream)
             o_out.copy_(out, non_blocking=True)
             o_n.copy_(nacc, non_blocking=True)
             o_seq.copy_(seq, non_blocking=True)
@@ -405,10 +409,9 @@ def run_gpu(args):
         "clocks": clk,
         "device_flags": flags,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+    return line if rank == 0 else None
 
 
 # --------------------------------------------------------------------------
@@ -428,24 +431,24 @@ def _c4_oracle_step(x, tokens, knobs, B, K):
     return int(knobs["k_per_row"].sum())
 
 
+C4_ONE_GPU = ("c4 runs sv_lmhead_rmsnorm, whose GEMM multicasts W tiles between the CTAs of a "
+              "cluster: it is run on one GPU per process only (--gpus 1, WORLD_SIZE unset or 1)")
+
+
 def run_gpu_c4(args):
     import numpy as np
     import torch
 
     world, rank, local = dist_setup(args)
+    if world > 1 or args.gpus > 1:
+        # refused before anything is built or launched
+        sys.stderr.write("bench.py: " + C4_ONE_GPU + "\n")
+        sys.exit(2)
     torch.cuda.set_device(local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        pg = dist
     from speculative_decoding_verification_47_gb300 import binding as sb
     from speculative_decoding_verification_47_gb300 import build as bld
     from speculative_decoding_verification_47_gb300 import workloads as wl
-    if rank == 0 or not os.path.exists(bld.LIB):
-        bld.build()
-    if pg is not None:
-        pg.barrier()
+    bld.build()
     B, K = 64, 7
     x = wl.lmhead_inputs()
     M, H, V = x.M, x.H, x.V
@@ -501,7 +504,7 @@ def run_gpu_c4(args):
         sb.sv_lmhead_rmsnorm(d_ht, d_w, x.eps, d_W, tl, sb.SV_BF16, M, H, V, ws2, wsl, stream)
         sb.sv_spec_verify(tl, 0, 0, dl, (K + 1) * V, V, sb.SV_BF16, B, K, V, tok, kpr, tmp, 1.0,
                           uni, mode, out, nacc, None, ws, wsb, stream)
-        sb.sv_kv_commit(seq, nacc, cap, B, K, ws, wsb, stream)
+        sb.sv_kv_commit(seq, nacc, cap, kpr, B, K, ws, wsb, stream)
 
     for _ in range(args.warmup):
         step()
@@ -511,8 +514,6 @@ def run_gpu_c4(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
-    if pg is not None:
-        pg.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -521,10 +522,8 @@ def run_gpu_c4(args):
         step(it)
     t_end.record(stream)
     torch.cuda.synchronize()
-    if pg is not None:
-        pg.barrier()
     clk = clocks.stop()
-    ms, total_positions = reduce_timing(t_start.elapsed_time(t_end), positions, pg, dev)
+    ms, total_positions = t_start.elapsed_time(t_end), positions
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[:args.steps])
     ms_step = ms / args.steps
     value = total_positions / (ms_step * 1e-3)
@@ -562,13 +561,9 @@ def run_gpu_c4(args):
         b.record(stream)
         torch.cuda.synchronize()
         ems = a.elapsed_time(b)
-        if pg is not None:
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            ems = float(t.item())
         h2d = (h_h.numel() + h_ht.numel()) * 2 + sum(t_.numel() * t_.element_size() for t_ in h_small)
         d2h = (o_out.numel() + o_n.numel() + o_seq.numel()) * 4
-        e2e = {"value": positions * world / (ems / steps_e2e * 1e-3), "unit": "positions/s",
+        e2e = {"value": positions / (ems / steps_e2e * 1e-3), "unit": "positions/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps_e2e}
 
     tpeak, tsrc = tensor_peak()
@@ -576,7 +571,7 @@ def run_gpu_c4(args):
         "metric": METRIC,
         "value": value,
         "unit": "positions/s",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_step,
@@ -587,7 +582,7 @@ def run_gpu_c4(args):
         "data": "synthetic",
         "config": {"workload": WORKLOADS["c4"], "name": "c4", "B": B, "K": K, "V": V, "M": M, "H": H,
                    "l2": "W (262 MB) > 129 MB L2, streamed from HBM by every LM-head call",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": "one GPU (the LM head is run on one GPU per process)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
                      "frac": achieved / tpeak, "traffic": traffic_for("c4", args.traffic),
                      "kernel": "sv_lmhead_rmsnorm (rmsnorm_kernel + lmhead_gemm_kernel), draft call",
@@ -598,10 +593,7 @@ def run_gpu_c4(args):
         "clocks": clk,
         "device_flags": list(flags),
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    return line
 
 
 def run_gpu_s2(args):
@@ -754,10 +746,9 @@ def run_gpu_s2(args):
         "clocks": clk,
         "device_flags": flags,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+    return line if rank == 0 else None
 
 
 # --------------------------------------------------------------------------
@@ -1088,6 +1079,32 @@ def run_reference_dynk(args):
         f"each step: one round of {B} controllers, Python oracle, one core")), flush=True)
 
 
+def secondary(args):
+    """After the headline (one GPU only): the LM-head GEMM (c4), the top-p
+    verify batch (c3) and the draft sampler (s2), each with its own CUDA-event
+    timing of its dominant kernel, roofline and clock record."""
+    import copy
+    out = {}
+    for name, fn in (("c4_lmhead", run_gpu_c4), ("c3", run_gpu), ("s2", run_gpu_s2)):
+        a = copy.copy(args)
+        a.workload = name.split("_")[0]
+        a.steps = max(3, min(args.steps, args.secondary_steps))
+        a.no_e2e = True
+        a.no_cpu_baseline = True
+        a.traffic = None
+        a.B = None
+        try:
+            ln = fn(a)
+        except Exception as exc:  # a secondary failure must not hide the headline
+            out[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            continue
+        out[name] = {k: ln.get(k) for k in ("metric", "value", "unit", "ms_per_step", "steps",
+                                            "warmup", "roofline", "clocks", "device_flags")}
+        out[name]["config"] = {k: ln["config"].get(k) for k in ("name", "B", "K", "V", "M", "H",
+                                                                 "top_p") if k in ln["config"]}
+    return out
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -1245,6 +1262,10 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="c2 only: skip the LM-head (c4), top-p (c3) and sampler (s2) timings "
+                         "that follow the headline in the same process")
+    ap.add_argument("--secondary-steps", type=int, default=100)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per verify launch, if measured for this kernel")
     args = ap.parse_args()
@@ -1253,15 +1274,22 @@ def main():
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "c4":
-        run_gpu_c4(args)
+        print(json.dumps(run_gpu_c4(args)), flush=True)
     elif args.workload == "s2":
-        run_gpu_s2(args)
+        line = run_gpu_s2(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
     elif args.workload == "kvp":
         run_gpu_kvp(args)
     elif args.workload == "dynk":
         run_gpu_dynk(args)
     else:
-        run_gpu(args)
+        line = run_gpu(args)
+        if line is not None:
+            world = int(os.environ.get("WORLD_SIZE", "1"))
+            if args.workload == "c2" and world == 1 and args.gpus == 1 and not args.no_secondary:
+                line["secondary"] = secondary(args)
+            print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -65,7 +65,7 @@ enum {
   SV_FLAG_BAD_MODE = 32,       /* mode[b] not SV_SAMPLED / SV_GREEDY               */
   SV_FLAG_CAPACITY = 64,       /* kv_commit: seq_len + n would pass capacity       */
   SV_FLAG_TIMEOUT = 128,       /* a bounded device wait ran out                    */
-  SV_FLAG_BAD_N = 256          /* kv_commit: n_accepted outside [0, K]             */
+  SV_FLAG_BAD_N = 256          /* kv_commit: n_accepted outside [0, K] or above k_b */
 };
 
 /* Optional per-(sequence, position) diagnostics, float32 [B][K+1][SV_DIAG_FIELDS],
@@ -142,7 +142,8 @@ size_t sv_workspace_size(int B, int K, int V, sv_dtype dt);
  *                   aligned; contents need no initialisation; calls that share
  *                   a workspace must be ordered on one stream.
  * Outputs must not alias inputs.  Logit rows need not be 16-byte aligned
- * (aligned rows are copied with the bulk-copy engine, the rest with loads).
+ * (the 16-byte-aligned body of a row is read with 16-byte asynchronous
+ * copies, cp.async, and its ragged ends element by element).
  */
 sv_status sv_spec_verify(const void* target_logits, int64_t target_seq_stride,
                          int64_t target_pos_stride, const void* draft_logits,
@@ -216,14 +217,20 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
  *   n_accepted  device int32 [B] (e.g. from sv_spec_verify).
  *   capacity    device int32 [B] or NULL: a row whose new length would exceed
  *               capacity[b] is left unchanged and sets SV_FLAG_CAPACITY.
+ *   k_per_row   device int32 [B] (the round's k_b) or NULL: with it, a row
+ *               whose n_accepted exceeds k_b (more accepted than drafted) is
+ *               left unchanged and sets SV_FLAG_BAD_N.
  *   K           if >= 0, n_accepted outside [0, K] leaves the row unchanged
- *               and sets SV_FLAG_BAD_N; if < 0 only n < 0 is rejected.
+ *               and sets SV_FLAG_BAD_N; if < 0 only n < 0 (and n > k_b when
+ *               k_per_row is given) is rejected.  Without k_per_row, n in
+ *               (k_b, K] of a ragged round cannot be told from a valid one.
  *   workspace   the verify workspace (its flag word is OR-ed, not cleared);
  *               at least 256 bytes.
  *   B           1 <= B <= 2^30, else SV_ERR_SHAPE.
  */
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
-                       int B, int K, void* workspace, size_t workspace_bytes, void* stream);
+                       const int32_t* k_per_row, int B, int K, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * sv_kv_commit_paged - sv_kv_commit for a paged KV cache ["Self-speculative

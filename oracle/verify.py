@@ -366,18 +366,19 @@ def spec_verify(target, draft, dtype: str, B: int, K: int, V: int, draft_tokens,
     return BatchResult(out_tokens=out, n_accepted=n, flags=flags, seqs=seqs)
 
 
-def kv_commit(seq_lens, n_accepted, capacity=None, K: int | None = None):
+def kv_commit(seq_lens, n_accepted, capacity=None, K: int | None = None, k_per_row=None):
     """KV write-pointer rollback [SSD §3.3, §4.3; SD §4.3]: each sequence's
     pointer, which stood at the round-start length while the drafts were
     written speculatively, moves to seq_len + n_accepted; entries at and
     beyond it are discarded (reading R10).  A row that would pass its
-    capacity, or whose n is negative (or above K when K is given), is left
-    unchanged and flagged.  Returns (new seq_lens, flags)."""
+    capacity, or whose n is negative (or above K when K is given, or above
+    the round's k_b when k_per_row is given: more tokens accepted than
+    drafted), is left unchanged and flagged.  Returns (new seq_lens, flags)."""
     s = np.asarray(seq_lens, dtype=np.int64).copy()
     flags = 0
     for b in range(s.shape[0]):
         nb = int(n_accepted[b])
-        if nb < 0 or (K is not None and nb > K):
+        if nb < 0 or (K is not None and nb > K) or (k_per_row is not None and nb > int(k_per_row[b])):
             flags |= FLAG_BAD_N
             continue
         new = int(s[b]) + nb

@@ -93,7 +93,7 @@ def lib() -> ctypes.CDLL:
                                              _i32, _vp, _vp, _vp, _f32, _vp, _vp, _vp, _vp, _vp,
                                              _vp]
         L.sv_kv_commit.restype = _i32
-        L.sv_kv_commit.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _sz, _vp]
+        L.sv_kv_commit.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz, _vp]
         L.sv_lmhead_rmsnorm.restype = _i32
         L.sv_lmhead_rmsnorm.argtypes = [_vp, _vp, _f32, _vp, _vp, _i32, _i32, _i32, _i32, _vp,
                                         _sz, _vp]
@@ -195,8 +195,9 @@ def sv_spec_verify_noalloc(target_logits, target_seq_stride, target_pos_stride, 
         _ptr(n_accepted), _ptr(diag), _stream(stream)))
 
 
-def sv_kv_commit(seq_lens, n_accepted, capacity, B, K, workspace, workspace_bytes, stream=None):
-    _check(lib().sv_kv_commit(_ptr(seq_lens), _ptr(n_accepted), _ptr(capacity), B, K,
+def sv_kv_commit(seq_lens, n_accepted, capacity, k_per_row, B, K, workspace, workspace_bytes,
+                 stream=None):
+    _check(lib().sv_kv_commit(_ptr(seq_lens), _ptr(n_accepted), _ptr(capacity), _ptr(k_per_row), B, K,
                               _ptr(workspace), workspace_bytes, _stream(stream)))
 
 

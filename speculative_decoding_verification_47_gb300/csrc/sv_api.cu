@@ -170,13 +170,14 @@ sv_status sv_spec_verify_noalloc(const void* target_logits, int64_t target_seq_s
 }
 
 sv_status sv_kv_commit(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
-                       int B, int K, void* workspace, size_t workspace_bytes, void* stream) {
+                       const int32_t* k_per_row, int B, int K, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   if (B < 1 || B > kMaxSeqs) return fail(SV_ERR_SHAPE, "need 1 <= B <= 2^30");
   if (!seq_lens || !n_accepted) return fail(SV_ERR_ARG, "seq_lens and n_accepted are required");
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < 256)
     return fail(SV_ERR_WORKSPACE, "workspace must be non-NULL, 256-byte aligned, >= 256 bytes");
   std::string err;
-  int s = sv::commit_launch(seq_lens, n_accepted, capacity, B, K,
+  int s = sv::commit_launch(seq_lens, n_accepted, capacity, k_per_row, B, K,
                             static_cast<uint32_t*>(workspace), stream, &err);
   if (s != SV_OK) return fail(static_cast<sv_status>(s), err);
   return SV_OK;

@@ -12,13 +12,16 @@ namespace sv {
 
 __global__ void kv_commit_kernel(int32_t* __restrict__ seq_lens,
                                  const int32_t* __restrict__ n_accepted,
-                                 const int32_t* __restrict__ capacity, int B, int K,
+                                 const int32_t* __restrict__ capacity,
+                                 const int32_t* __restrict__ k_per_row, int B, int K,
                                  uint32_t* __restrict__ flags) {
   pdl_wait();  // the launch may overlap the kernel that wrote n_accepted
   uint32_t f = 0;
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
     const int n = n_accepted[b];
-    if (n < 0 || (K >= 0 && n > K)) {
+    // more accepted than this sequence drafted: the pointer would move past
+    // the entries the round wrote
+    if (n < 0 || (K >= 0 && n > K) || (k_per_row && n > k_per_row[b])) {
       f |= SV_FLAG_BAD_N;
       continue;
     }
@@ -32,8 +35,9 @@ __global__ void kv_commit_kernel(int32_t* __restrict__ seq_lens,
   if (f) atomicOr(flags, f);
 }
 
-int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
-                  int K, uint32_t* flags, void* stream, std::string* err) {
+int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
+                  const int32_t* k_per_row, int B, int K, uint32_t* flags, void* stream,
+                  std::string* err) {
   int blocks = (B + 255) / 256;
   if (blocks > 1024) blocks = 1024;
   cudaLaunchConfig_t cfg = {};
@@ -46,7 +50,8 @@ int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_commit_kernel, seq_lens, n_accepted, capacity, B, K, flags);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_commit_kernel, seq_lens, n_accepted, capacity, k_per_row, B, K,
+                                     flags);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *err = std::string("kv_commit launch: ") + cudaGetErrorString(e);

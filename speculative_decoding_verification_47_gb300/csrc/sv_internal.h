@@ -69,7 +69,8 @@ int paged_commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int3
                         int32_t* free_top, int free_capacity, int B, uint32_t* ws, void* stream,
                         std::string* err);
 
-int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity, int B,
+int commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* capacity,
+                  const int32_t* k_per_row, int B,
                   int K, uint32_t* flags, void* stream, std::string* err);
 
 int lmhead_launch(const void* hidden, const void* norm_w, float eps, const void* W, void* logits,

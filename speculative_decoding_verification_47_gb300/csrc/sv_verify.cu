@@ -86,8 +86,9 @@ struct VerifyParams {
 // ---------------------------------------------------------------------------
 // One CTA's slice [e0, e1) of one logit row, in 16-byte units: unit u holds
 // global bytes [base16 + 16u, base16 + 16u + 16).  Units inside the aligned
-// body [a0, a1) are fully valid and arrive by bulk copy; the (at most two)
-// partial units at the ends are read element by element from global memory.
+// body [a0, a1) are fully valid and are read as 16-byte vectors (cp.async
+// into shared memory in the row pass, plain loads in the others); the (at most
+// two) partial units at the ends are read element by element.
 // ---------------------------------------------------------------------------
 template <int ES>
 struct RowSlice {

@@ -19,3 +19,14 @@ def gpu_available() -> bool:
         return torch.cuda.is_available()
     except Exception:
         return False
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the disagreement budgets of the parity tests (decisions,
+    disagreements, low-margin decisions), pass or fail."""
+    import sys as _sys
+    vh = _sys.modules.get("tests.verify_harness")
+    if vh is None:
+        return
+    for line in vh.budget_lines():
+        terminalreporter.write_line("disagreement budget: " + line)

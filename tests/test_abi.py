@@ -86,10 +86,10 @@ def test_spec_verify_host_checks(lib, kw, status):
 
 def test_kv_commit_and_lmhead_host_checks(lib):
     with pytest.raises(sb.SVError) as e:
-        sb.sv_kv_commit(None, P, None, 4, 3, P, 256, 0)
+        sb.sv_kv_commit(None, P, None, None, 4, 3, P, 256, 0)
     assert e.value.status == sb.SV_ERR_ARG
     with pytest.raises(sb.SVError) as e:
-        sb.sv_kv_commit(P, P, None, 4, 3, P + 8, 256, 0)
+        sb.sv_kv_commit(P, P, None, None, 4, 3, P + 8, 256, 0)
     assert e.value.status == sb.SV_ERR_WORKSPACE
     with pytest.raises(sb.SVError) as e:
         sb.sv_lmhead_rmsnorm(P, P, 1e-5, P, P, sb.SV_BF16, 4, 100, 128, P, 1 << 30, 0)
@@ -174,7 +174,7 @@ def test_sequence_count_limits(lib):
         sb.sv_dynk_init(P, (1 << 30) + 1, 4, 0)
     assert e.value.status == sb.SV_ERR_SHAPE
     with pytest.raises(sb.SVError) as e:
-        sb.sv_kv_commit(P, P, None, (1 << 30) + 1, 3, P, 256, 0)
+        sb.sv_kv_commit(P, P, None, None, (1 << 30) + 1, 3, P, 256, 0)
     assert e.value.status == sb.SV_ERR_SHAPE
     with pytest.raises(sb.SVError) as e:
         sb.sv_draft_sample(P, 0, 0, sb.SV_BF16, (1 << 27) // 8 + 1, 8, 100, None, None, 1.0, P,
@@ -187,7 +187,7 @@ def test_host_tensors_are_refused(lib):
     import torch
     host = torch.zeros(16, dtype=torch.int32)
     with pytest.raises(ValueError):
-        sb.sv_kv_commit(host, P, None, 4, 3, P, 256, 0)
+        sb.sv_kv_commit(host, P, None, None, 4, 3, P, 256, 0)
     with pytest.raises(ValueError):
         sb.sv_read_device_flags(host.pin_memory() if torch.cuda.is_available() else host, 0)
 

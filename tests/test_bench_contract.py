@@ -91,3 +91,21 @@ def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
     src, digest, value = bench.MEASURED_TRAFFIC["c2"]
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, "c2", (src, "0" * 16, value))
     assert bench.traffic_for("c2", None) is None
+
+
+@pytest.mark.parametrize("env,argv", [
+    ({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}, ()),
+    ({}, ("--gpus", "2")),
+])
+def test_c4_refuses_a_multi_gpu_launch(env, argv):
+    """The LM head's GEMM multicasts W tiles inside a cluster: bench.py runs
+    it on one GPU per process only and refuses a multi-rank or --gpus > 1
+    launch before it builds or launches anything (so this needs no GPU)."""
+    e = dict(os.environ)
+    e.update(env)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "c4",
+                        "--steps", "1", "--warmup", "3", *argv], cwd=ROOT, env=e,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0
+    assert "one GPU per process only" in r.stderr
+    assert r.stdout.strip() == ""

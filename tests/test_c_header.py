@@ -31,7 +31,7 @@ int main(void) {
   s = sv_spec_verify(dummy, 0, 0, dummy, 0, 0, SV_BF16, 0, 3, 100, dummy, NULL, NULL, 1.0f,
                      (const float*)dummy, NULL, dummy, dummy, NULL, dummy, 1024, NULL);
   if (s != SV_ERR_SHAPE || strlen(sv_last_error()) == 0) return 7;
-  s = sv_kv_commit(NULL, dummy, NULL, 4, 3, dummy, 256, NULL);
+  s = sv_kv_commit(NULL, dummy, NULL, NULL, 4, 3, dummy, 256, NULL);
   if (s != SV_ERR_ARG) return 8;
   printf("ok %d\n", sv_version());
   return 0;

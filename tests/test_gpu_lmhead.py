@@ -107,14 +107,15 @@ def test_lmhead_norm_is_applied():
     np.testing.assert_array_equal(a, b)
 
 
-def test_lmhead_c4_full_size_sampled_rows():
-    """M=512, H=4096, V=32000 (the layer-skip workload): 24 rows checked in
-    full against the oracle."""
+def test_lmhead_c4_full_size_every_row():
+    """M=512, H=4096, V=32000 (the layer-skip workload, on the persistent
+    BN=224 cluster schedule that only this size takes): every one of the
+    512 x 32000 outputs checked against the float64 oracle and the
+    bf16-mimic bound."""
     x = wl.lmhead_inputs()
     out, flags = _run(x, sb.SV_BF16)
     assert flags == 0
-    rows = np.random.default_rng(4).choice(x.M, size=24, replace=False)
-    _check(x, out.float().cpu().numpy().astype(np.float64), sb.SV_BF16, rows=rows)
+    _check(x, out.float().cpu().numpy().astype(np.float64), sb.SV_BF16)
 
 
 def test_c4_layer_skip_draft_then_verify():

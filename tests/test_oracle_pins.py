@@ -458,6 +458,14 @@ def test_kv_commit_invariant():
     bad[1] = K + 1
     s3, flags = ov.kv_commit(s0, bad, None, K)
     assert flags == ov.FLAG_BAD_N and s3[0] == s0[0] and s3[1] == s0[1]
+    # with the round's k_b: one more accepted than drafted is refused, even
+    # below K; exactly k_b is fine
+    kb = np.minimum(k, K - 1)
+    more = np.minimum(kb + 1, K).astype(np.int32)
+    s4, flags = ov.kv_commit(s0, more, None, K, kb)
+    assert flags == ov.FLAG_BAD_N and np.all(s4 == s0)
+    s5, flags = ov.kv_commit(s0, kb.astype(np.int32), None, K, kb)
+    assert flags == 0 and np.all(s5 - s0 == kb)
 
 
 @pytest.mark.parametrize("case", ["top_p", "top_p_ties"])
