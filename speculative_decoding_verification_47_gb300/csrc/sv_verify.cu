@@ -347,8 +347,12 @@ __device__ __forceinline__ float unit_sumexp(const uint4& v, const Expo& x, floa
   return sx + sy;
 }
 
-template <int ES>
-__device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
+// Adds a full unit to the row accumulator.  With MAX it returns the unit's
+// max (NaN if it holds one), which callers that keep per-thread candidate
+// lists compare; without, it returns 0 and forms the max only when the
+// reference exponent must rise.
+template <int ES, bool MAX = false>
+__device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
   uint32_t um = 0;
   if (ES == 2) {
     um = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
@@ -356,9 +360,11 @@ __device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Ex
   } else {
     a.mx = nanmax(a.mx, unit_max<ES>(v));
   }
+  float g = 0.f;
+  if (MAX) g = ES == 2 ? nanmax(bf16_lo(um), bf16_hi(um)) : unit_max<ES>(v);
   float us = unit_sumexp<ES>(v, x, a.R);
   if (!(us <= kRaiseAbove)) {
-    const float g = ES == 2 ? nanmax(bf16_lo(um), bf16_hi(um)) : unit_max<ES>(v);
+    if (!MAX) g = ES == 2 ? nanmax(bf16_lo(um), bf16_hi(um)) : unit_max<ES>(v);
     const float gc = g * x.chi;
     if (gc > a.R) {
       acc_raise(a, ceilf(gc));
@@ -366,6 +372,7 @@ __device__ __forceinline__ void sampled_unit(RowAcc& a, const uint4& v, const Ex
     }
   }
   a.pend += us;
+  return g;
 }
 
 __device__ __forceinline__ void sampled_elem(RowAcc& a, float z, const Expo& x) {
@@ -422,26 +429,62 @@ __device__ __forceinline__ uint4 ldg_unit(const RowSlice<ES>& rs, int u) {
   return __ldg(reinterpret_cast<const uint4*>(rs.base16 + 16 * (uintptr_t)u));
 }
 
+// ---------------------------------------------------------------------------
+// Per-thread candidate lists (top-p instances).  During the row pass each
+// thread keeps, per row, the kListLen largest logits it admitted (key and
+// index, keys descending; key 0 = empty slot) in shared memory, slot k of row
+// r at lst[(r * kListLen + k) * kThreads + tid].  A logit is admitted only if
+// it is strictly larger than the thread's last entry (once its list is full)
+// and than the CTA's floor T (sh.lth[r]): the largest last-entry key any full
+// list of the CTA has had, raised with atomicMax as lists fill.  T only grows,
+// so every logit left out has a key <= the final T; with theta = the largest
+// final T over the cluster's CTAs, the lists together hold EVERY token of the
+// row whose key exceeds theta.  A top-p selection pass whose key window lies
+// above theta can therefore read the lists instead of the row (at most
+// kListLen entries per thread).
+// ---------------------------------------------------------------------------
+constexpr int kListLen = 4;
+
+// value of a key, -inf for key 0 (no floor yet)
 template <int ES>
-__device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, int u, int ub0,
-                                           int ub1, const uint4& v, bool greedy, const Expo& x) {
-  constexpr int EPU = 16 / ES;
-  const int eb = rs.ebase0 + u * EPU;
-  if (u >= ub0 && u < ub1) {
-    if (greedy)
-      greedy_unit<ES>(a, v, eb);
-    else
-      sampled_unit<ES>(a, v, x);
-  } else if (u < rs.n_units) {
-    for (int j = 0; j < EPU; ++j) {
-      const int e = eb + j;
-      if (e < rs.e0 || e >= rs.e1) continue;
-      const float z = rs.elem(e);
-      if (greedy)
-        greedy_elem(a, z, e);
-      else
-        sampled_elem(a, z, x);
+__device__ __forceinline__ float key_val(uint32_t k) {
+  return k ? bits_val<ES>(key_bits<ES>(k)) : -INFINITY;
+}
+
+// Insert one logit (bit pattern, index) into this thread's list of row r;
+// returns the list's floor key (its last entry's key once full, else 0).
+template <int ES>
+__device__ __forceinline__ uint32_t list_add(uint2* lst, int r, uint32_t bits, int idx) {
+  uint2 cur = make_uint2(okey<ES>(bits), (uint32_t)idx);
+  uint2* base = lst + (size_t)r * kListLen * kThreads + threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < kListLen; ++k) {  // insertion from the top (empty slots hold key 0)
+    const uint2 e = base[k * kThreads];
+    if (cur.x > e.x) {
+      base[k * kThreads] = cur;
+      cur = e;
     }
+  }
+  return base[(kListLen - 1) * kThreads].x;
+}
+
+// Slots of a full unit whose value is strictly above thr (bit j = slot j).
+template <int ES>
+__device__ __forceinline__ uint32_t above_mask(const uint4& v, float thr) {
+  if (ES == 2) {
+    const uint32_t tb = __float_as_uint(thr) >> 16;  // (thr is a bf16 value or -inf)
+    const uint32_t t2 = tb | (tb << 16);
+    const __nv_bfloat162 f = *reinterpret_cast<const __nv_bfloat162*>(&t2);
+    const uint32_t m0 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.x), f);
+    const uint32_t m1 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.y), f);
+    const uint32_t m2 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.z), f);
+    const uint32_t m3 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.w), f);
+    const uint32_t m = (m0 & 0x10001u) | ((m1 & 0x10001u) << 2) | ((m2 & 0x10001u) << 4) |
+                       ((m3 & 0x10001u) << 6);
+    return (m | (m >> 15)) & 0xffu;
+  } else {
+    return (__uint_as_float(v.x) > thr ? 1u : 0u) | (__uint_as_float(v.y) > thr ? 2u : 0u) |
+           (__uint_as_float(v.z) > thr ? 4u : 0u) | (__uint_as_float(v.w) > thr ? 8u : 0u);
   }
 }
 
@@ -668,9 +711,15 @@ constexpr int kHistBytes = 2 * kHistRowBytes;
 constexpr int kSelLoads = 4;  // units per thread per step of a selection pass
 constexpr int kStageBytes = kThreads * kSelLoads * 16;  // each thread's units of a step
 constexpr int kSelSmemBytes = kHistBytes + kStageBytes;
+// candidate lists (top-p instances): after the row pass's ring and the
+// selection's histograms and staging, alive from the row pass to the cut
+constexpr int kListOff = ((kSelSmemBytes > kRingBytes ? kSelSmemBytes : kRingBytes) + 255) / 256 * 256;
+constexpr int kListBytes = 2 * kListLen * kThreads * 8;
+constexpr int kToppSmemBytes = kListOff + kListBytes;
 constexpr int kMaxSelPasses = 12;
 
 struct TopSel {
+  uint32_t lth;       // the cluster's list floor: the lists hold every key above it
   uint32_t lo, hi;    // window of the next pass
   uint32_t flo, fhi;  // keys that may still hold the cut
   int mode;           // 0 resolved, 1 count pass next, 2 locator pass next
@@ -712,6 +761,8 @@ struct Shared {
   RowAcc row_t, row_d;
   DF S_w, rem;
   int skip, moot;
+  uint32_t lth[2];          // this CTA's largest candidate-list floor per row
+  uint32_t g_th[kCmax][2];  // all-gather of every CTA's lth
   int fin;
   int owner, rsel;
   int x;
@@ -719,6 +770,10 @@ struct Shared {
   float dq[3];  // p'(x), q'(x) and their ratio, for the diagnostics
   uint32_t eb;  // the item's verdict: error bits, rejection
   int rej;
+  // the item's two row slices (the same in every thread of the CTA), for the
+  // out-of-line selection and tie helpers: read through a pointer, they take
+  // no per-thread stack copies; both element sizes share one layout
+  RowSlice<4> rsl[2];
 };
 
 // An earlier position of the sequence has been rejected (or failed) in the
@@ -912,31 +967,59 @@ __device__ __forceinline__ uint32_t window_mask(const uint4& v, const SelP& p) {
 // ones above the window to *above.  Count pass: count their keys in the
 // window, return how many have the draft token's key at a smaller index.
 // Locator pass: add their masses to the bins.
+// One element (bit pattern, index) of a selection pass: its mass goes to
+// *above if its key lies above the window; in the window it is counted (count
+// pass) or its mass binned (locator pass).  Returns 1 if a count pass saw the
+// draft token's key at a smaller index.
+template <int ES>
+__device__ __forceinline__ uint32_t sel_key(const SelP& p, unsigned char* h, uint32_t bits, int idx,
+                                            int x, const Expo& X, DF* above) {
+  const uint32_t key = okey<ES>(bits);
+  const uint32_t d = key - p.lo;
+  const float z = bits_val<ES>(bits);
+  if (d > p.span) {
+    if (key > p.lo) df_acc(*above, e2(z, X, -p.R));
+  } else if (p.counts) {
+    atomicAdd(reinterpret_cast<uint32_t*>(h) + d, 1u);
+  } else {
+    int bin = (int)(d >> p.shift);
+    if (p.vbins)  // bins numbered upward in value, like key bins
+      bin = max(0, kNB - 1 - (int)((p.tmax - __fmaf_rn(z, p.chi, -p.R)) * p.inv));
+    atomicAdd(reinterpret_cast<float*>(h) + bin, e2(z, X, -p.R));
+  }
+  return (p.counts && key == p.kx && idx < x) ? 1u : 0u;
+}
+
 template <int ES>
 __device__ __forceinline__ uint32_t sel_bits(const SelP& p, unsigned char* h, const uint4& v, int eb,
                                              uint32_t mask, int x, const Expo& X, DF* above) {
-  uint32_t* hc = reinterpret_cast<uint32_t*>(h);
-  float* hm = reinterpret_cast<float*>(h);
   uint32_t lt = 0;
   while (mask) {
     const int j = __ffs(mask) - 1;
     mask &= mask - 1u;
-    const uint32_t bits = unit_bits<ES>(v, j);
-    const uint32_t key = okey<ES>(bits);
-    const uint32_t d = key - p.lo;
-    const float z = bits_val<ES>(bits);
-    if (d > p.span) {
-      if (key > p.lo) df_acc(*above, e2(z, X, -p.R));
-    } else if (p.counts) {
-      atomicAdd(hc + d, 1u);
-    } else {
-      int bin = (int)(d >> p.shift);
-      if (p.vbins)  // bins numbered upward in value, like key bins
-        bin = max(0, kNB - 1 - (int)((p.tmax - __fmaf_rn(z, p.chi, -p.R)) * p.inv));
-      atomicAdd(hm + bin, e2(z, X, -p.R));
-    }
-    if (p.counts) lt += (key == p.kx && eb + j < x) ? 1u : 0u;
+    lt += sel_key<ES>(p, h, unit_bits<ES>(v, j), eb + j, x, X, above);
   }
+  return lt;
+}
+
+// A selection pass over this thread's candidate list of row r (the window
+// lies above the cluster's list floor, so the lists hold every token of the
+// window and above it).
+template <int ES>
+__device__ __noinline__ uint32_t sel_list(const TopSel* tp, unsigned char* h, const uint2* lst, int r,
+                                          int x, float chi, float clo, DF* above) {
+  const SelP p = sel_params(*tp, ES);
+  const Expo X{chi, clo};
+  uint32_t lt = 0;
+  DF ab = *above;
+  const uint2* base = lst + (size_t)r * kListLen * kThreads + threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < kListLen; ++k) {
+    const uint2 e = base[k * kThreads];
+    if (e.x == 0u) break;  // (keys descend; the rest is empty)
+    lt += sel_key<ES>(p, h, key_bits<ES>(e.x), (int)e.y, x, X, &ab);
+  }
+  *above = ab;
   return lt;
 }
 
@@ -1269,10 +1352,11 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
 // Every CTA of the cluster ends with the same sh.ts[] results.
 template <int ES>
 __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsigned char* hist,
-                                         cg::cluster_group& cluster, int C, int b, int i, int kb,
-                                         bool two, const Expo X, const RowSlice<ES>& st,
-                                         const RowSlice<ES>& sd, const RowAcc& row_t,
-                                         const RowAcc& row_d) {
+                                         int C, int b, int i, int kb, bool two, const Expo X,
+                                         const RowAcc& row_t, const RowAcc& row_d) {
+  const RowSlice<ES>& st = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[0]);
+  const RowSlice<ES>& sd = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[1]);
+  cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 2 && (tid == 0 || two)) {
     const int r = tid;
@@ -1285,6 +1369,8 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     const RowAcc& row = r ? row_d : row_t;
     const RowSlice<ES>& rs = r ? sd : st;
     TopSel t;
+    t.lth = 0u;
+    for (int q = 0; q < C; ++q) t.lth = max(t.lth, sh.g_th[q][r]);
     t.R = row.R;
     t.S = row.s;
     t.thr = df_mul_f(row.s, P.top_p);
@@ -1299,6 +1385,9 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     t.lo = min(lo, t.hi);
     t.flo = t.lo;
     t.fhi = t.hi;
+    // the lists hold every token above the floor: start with the window
+    // above it (if it leaves any key), whose passes read only the lists
+    if (t.lth < t.hi && t.lth >= t.lo) t.lo = t.lth + 1u;
     t.chi = X.chi;
     sel_set_mode<ES>(t, true);
     t.kx = x >= 0 ? okey<ES>(rs.bits(x)) : 0u;
@@ -1326,8 +1415,15 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     DF ab0{0.f, 0.f}, ab1{0.f, 0.f};
     unsigned char* h1 = hist + kHistRowBytes;
     uint4* stage = reinterpret_cast<uint4*>(hist + kHistBytes);
-    if (a0) l0 = sel_stream<ES>(&sh.ts[0], hist, stage, st, x, X.chi, X.clo, &ab0);
-    if (a1) l1 = sel_stream<ES>(&sh.ts[1], h1, stage, sd, x, X.chi, X.clo, &ab1);
+    // (whether a row reads its lists is uniform in the cluster: every CTA
+    // holds the same window and floor)
+    const uint2* lst = reinterpret_cast<const uint2*>(hist + kListOff);
+    if (a0)
+      l0 = sh.ts[0].lo > sh.ts[0].lth ? sel_list<ES>(&sh.ts[0], hist, lst, 0, x, X.chi, X.clo, &ab0)
+                                      : sel_stream<ES>(&sh.ts[0], hist, stage, st, x, X.chi, X.clo, &ab0);
+    if (a1)
+      l1 = sh.ts[1].lo > sh.ts[1].lth ? sel_list<ES>(&sh.ts[1], h1, lst, 1, x, X.chi, X.clo, &ab1)
+                                      : sel_stream<ES>(&sh.ts[1], h1, stage, sd, x, X.chi, X.clo, &ab1);
     // the CTA's lt count (count passes) and mass above the window (fixed order)
     if (c0 && l0) atomicAdd(reinterpret_cast<uint32_t*>(hist) + kSlotLt, l0);
     if (c1 && l1) atomicAdd(reinterpret_cast<uint32_t*>(h1) + kSlotLt, l1);
@@ -1367,8 +1463,10 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
 // of its slice; the CTA holding token nk finds its round, unit and element
 // and writes the index into every CTA.  0x7fffffff if the row has <= nk.
 template <int ES>
-__device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group& cluster, int C,
-                                    int rank, const RowSlice<ES>& rs, uint32_t kk, int nk) {
+__device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, int C, int rank, int which,
+                                    uint32_t kk, int nk) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const RowSlice<ES>& rs = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[which]);
   constexpr int EPU = 16 / ES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NU = rs.n_units, rounds = (NU + kThreads - 1) / kThreads;
@@ -1464,11 +1562,12 @@ __device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, cg::cluster_group&
 // stored for the sequence's outputs.
 // ---------------------------------------------------------------------------
 template <int ES, bool TOPP, bool SAMPLE = false>
-__device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals,
-                                    cg::cluster_group& cluster, int C, int rank, int b, int kb,
+__device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals, int C, int rank,
+                                    int b, int kb,
                                     float T, int j, float uK, int e0, int e1, float Rt, float Rd,
                                     DF S_t, DF S_d, uint32_t kt, int nkt, int cntt, uint32_t kd,
                                     int nkd, int cntd) {
+  cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool bonus = (j == kb);
   const Expo X = make_expo(T);
@@ -1494,12 +1593,17 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   W.vkt = -INFINITY;
   if (TOPP) {  // (S_t, S_d are the kept masses here)
     uint32_t* iv = reinterpret_cast<uint32_t*>(vals);
+    if (tid == 0) {
+      sh.rsl[0] = *reinterpret_cast<const RowSlice<4>*>(&pr.st);
+      sh.rsl[1] = *reinterpret_cast<const RowSlice<4>*>(&pr.sd);
+    }
+    __syncthreads();
     W.kt = kt;
     if (kt != 0u) W.vkt = bits_val<ES>(key_bits<ES>(kt));
-    if (nkt < cntt) W.ct = tie_cut<ES>(sh, iv, cluster, C, rank, pr.st, kt, nkt);
+    if (nkt < cntt) W.ct = tie_cut<ES>(sh, iv, C, rank, 0, kt, nkt);
     if (!bonus) {
       W.kd = kd;
-      if (nkd < cntd) W.cd = tie_cut<ES>(sh, iv, cluster, C, rank, pr.sd, kd, nkd);
+      if (nkd < cntd) W.cd = tie_cut<ES>(sh, iv, C, rank, 1, kd, nkd);
     }
   }
   const int NU = pr.st.n_units;
@@ -1751,16 +1855,80 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
   return (!was && now) ? 1 : 0;
 }
 
+// The elements of a full unit above thr go into the list of row r; thr
+// becomes the list's floor value once the list is full, and a higher floor is
+// published to the CTA's floor T.  (Out of line: reached by a few units.)
+template <int ES>
+__device__ __noinline__ float list_add_unit(Shared& sh, uint2* lst, int r, uint4 v, int eb, float thr) {
+  uint32_t m = above_mask<ES>(v, thr);
+  uint32_t f = 0;
+  while (m) {
+    const int j = __ffs(m) - 1;
+    m &= m - 1u;
+    const uint32_t b = unit_bits<ES>(v, j);
+    if (bits_val<ES>(b) > thr) f = list_add<ES>(lst, r, b, eb + j);  // (thr may have risen)
+    if (f) thr = fmaxf(thr, key_val<ES>(f));
+  }
+  if (f) atomicMax(&sh.lth[r], f);
+  return thr;
+}
+
+template <int ES, bool LISTS = false>
+__device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, int u, int ub0,
+                                           int ub1, const uint4& v, bool greedy, const Expo& x,
+                                           Shared* sh = nullptr, uint2* lst = nullptr, int r = 0,
+                                           float* thr = nullptr) {
+  constexpr int EPU = 16 / ES;
+  const int eb = rs.ebase0 + u * EPU;
+  if (u >= ub0 && u < ub1) {
+    if (greedy) {
+      greedy_unit<ES>(a, v, eb);
+    } else {
+      const float g = sampled_unit<ES, LISTS>(a, v, x);
+      if (LISTS && g > *thr) *thr = list_add_unit<ES>(*sh, lst, r, v, eb, *thr);
+    }
+  } else if (u < rs.n_units) {
+    for (int j = 0; j < EPU; ++j) {
+      const int e = eb + j;
+      if (e < rs.e0 || e >= rs.e1) continue;
+      const float z = rs.elem(e);
+      if (greedy) {
+        greedy_elem(a, z, e);
+      } else {
+        sampled_elem(a, z, x);
+        if (LISTS && z > *thr) {
+          const uint32_t f = list_add<ES>(lst, r, rs.bits(e), e);
+          if (f) {
+            atomicMax(&sh->lth[r], f);
+            *thr = fmaxf(*thr, key_val<ES>(f));
+          }
+        }
+      }
+    }
+  }
+}
+
 // Streams this CTA's slices of both rows through the per-thread cp.async ring
 // and reduces them into at / ad (row pass of a1 and a3).  With MOOT, every
 // other step each thread looks at the sequence word and stops reading once
 // an earlier position of the sequence is rejected (it then sets sh.moot).
-template <int ES, bool MOOT>
+// With LISTS (top-p instances, sampled rows), each thread also keeps its
+// candidate lists in lst, and sh.lth[r] ends as the CTA's floor of row r.
+template <int ES, bool MOOT, bool LISTS = false>
 __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh, float* vals,
                                               const RowSlice<ES>& st, const RowSlice<ES>& sd,
                                               bool has_draft, bool greedy, bool skip, const Expo& X,
-                                              int b, int i, RowAcc& at, RowAcc& ad) {
+                                              int b, int i, RowAcc& at, RowAcc& ad,
+                                              uint2* lst = nullptr) {
   const int tid = threadIdx.x;
+  const bool lists = LISTS && !greedy;
+  // list admission thresholds (values); the draft row keeps no list when
+  // the call leaves the draft untruncated
+  float thr0 = -INFINITY, thr1 = P.topp_draft ? -INFINITY : INFINITY;
+  if (lists) {
+#pragma unroll
+    for (int k = 0; k < 2 * kListLen; ++k) lst[k * kThreads + tid] = make_uint2(0u, 0u);
+  }
   {
     // Each thread keeps kRingStages steps of its units in flight in its own
     // shared-memory slots (slot k of stage s: ring[(s*2L + k)*kThreads + tid],
@@ -1809,6 +1977,10 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     // the sequence word, read two steps before it is looked at (no stall)
     unsigned long long wseen = (MOOT && i > 0 && !skip) ? __ldcg(P.words + b) : 0ull;
     for (int n = 0; n < nsteps; ++n) {
+      if (LISTS && lists) {  // the CTA's floors may have risen: admit only above them
+        thr0 = fmaxf(thr0, key_val<ES>(sh.lth[0]));
+        thr1 = fmaxf(thr1, key_val<ES>(sh.lth[1]));
+      }
       // every other step each thread looks again whether an earlier
       // position has been rejected meanwhile; if so it stops reading (the
       // item is then moot, and the cluster drops it after the combine).  A
@@ -1831,24 +2003,32 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
 #pragma unroll
         for (int k = 0; k < L; ++k) {
           const uint4 vt = slot[k * kThreads];
-          if (greedy)
+          if (greedy) {
             greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
-          else
-            sampled_unit<ES>(at, vt, X);
+          } else {
+            const float g = sampled_unit<ES, LISTS>(at, vt, X);
+            if (LISTS && g > thr0)
+              thr0 = list_add_unit<ES>(sh, lst, 0, vt, st.ebase0 + (u0 + k * kThreads) * EPU, thr0);
+          }
         }
         if (has_draft) {
 #pragma unroll
-          for (int k = 0; k < L; ++k) sampled_unit<ES>(ad, slot[(L + k) * kThreads], X);
+          for (int k = 0; k < L; ++k) {
+            const uint4 vd = slot[(L + k) * kThreads];
+            const float g = sampled_unit<ES, LISTS>(ad, vd, X);
+            if (LISTS && g > thr1)
+              thr1 = list_add_unit<ES>(sh, lst, 1, vd, sd.ebase0 + (u0 + k * kThreads) * EPU, thr1);
+          }
         }
       } else {
 #pragma unroll
         for (int k = 0; k < L; ++k) {
           const int u = u0 + k * kThreads;
           const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
-          row_unit_v<ES>(at, st, u, tb0, tb1, vt, greedy, X);
+          row_unit_v<ES, LISTS>(at, st, u, tb0, tb1, vt, greedy, X, &sh, lst, 0, &thr0);
           if (has_draft) {
             const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
-            row_unit_v<ES>(ad, sd, u, db0, db1, vd, false, X);
+            row_unit_v<ES, LISTS>(ad, sd, u, db0, db1, vd, false, X, &sh, lst, 1, &thr1);
           }
         }
       }
@@ -1894,16 +2074,22 @@ __device__ __forceinline__ bool combine_rows(Shared& sh, cg::cluster_group& clus
     // this CTA's moot flag: the word it saw at the start, or at the last
     // step it looked (any thread)
     const int m = (sh.skip | sh.moot) ? 1 : 0;
+    const uint32_t th0 = sh.lth[0], th1 = sh.lth[1];  // (complete: the barrier above)
     if (C > 1) {
       if (lane < C) {
         *cluster.map_shared_rank(&sh.g_t[rank], lane) = ct;
         *cluster.map_shared_rank(&sh.g_d[rank], lane) = cd;
         *cluster.map_shared_rank(&sh.g_m[rank], lane) = m;
+        uint32_t* g = cluster.map_shared_rank(&sh.g_th[rank][0], lane);
+        g[0] = th0;
+        g[1] = th1;
       }
     } else if (lane == 0) {
       sh.row_t = ct;
       sh.row_d = cd;
       sh.g_m[0] = m;
+      sh.g_th[0][0] = th0;
+      sh.g_th[0][1] = th1;
     }
   }
   if (C > 1) cluster.sync();
@@ -1931,7 +2117,7 @@ __device__ __forceinline__ bool combine_rows(Shared& sh, cg::cluster_group& clus
 }
 
 template <int ES, bool TOPP>
-__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_constant__ VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -1978,6 +2164,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
   if (tid == 0) {
     sh.skip = word_moot(w0, i) ? 1 : 0;
     sh.moot = 0;
+    sh.lth[0] = sh.lth[1] = 0u;
   }
   __syncthreads();
   const bool skip = sh.skip != 0;
@@ -2007,17 +2194,25 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
     sh.zd_x = zd;
   }
   RowAcc at = acc_init(), ad = acc_init();
-  stream_slices<ES, true>(P, sh, vals, st, sd, has_draft, greedy, skip, X, b, i, at, ad);
+  stream_slices<ES, true, TOPP>(P, sh, vals, st, sd, has_draft, greedy, skip, X, b, i, at, ad,
+                                reinterpret_cast<uint2*>(reinterpret_cast<char*>(vals) + kListOff));
   if (combine_rows(sh, cluster, C, rank, at, ad, greedy, has_draft, skip)) return;  // (moot: uniform)
-  const RowAcc row_t = sh.row_t, row_d = sh.row_d;
-  // Row validity: no NaN, no +inf, not all -inf, exponent range finite.
-  const bool bad_t = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
-                     (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
-  const bool bad_d = has_draft && (!(row_d.mx > -INFINITY && row_d.mx < INFINITY) ||
-                                   !(row_d.R > kRnone && row_d.R < INFINITY));
-  if (TOPP && !greedy && !bad_t && !bad_d)
-    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, kb,
-                    has_draft && P.topp_draft, X, st, sd, sh.row_t, sh.row_d);
+  // Row validity: no NaN, no +inf, not all -inf, exponent range finite.  (The
+  // row statistics are read from shared memory from here on: nothing of them
+  // stays in registers across the out-of-line calls below.)
+  const bool bad_t = !(sh.row_t.mx > -INFINITY && sh.row_t.mx < INFINITY) ||
+                     (!greedy && !(sh.row_t.R > kRnone && sh.row_t.R < INFINITY));
+  const bool bad_d = has_draft && (!(sh.row_d.mx > -INFINITY && sh.row_d.mx < INFINITY) ||
+                                   !(sh.row_d.R > kRnone && sh.row_d.R < INFINITY));
+  if (TOPP && !greedy && !bad_t && !bad_d) {
+    if (tid == 0) {
+      sh.rsl[0] = *reinterpret_cast<const RowSlice<4>*>(&st);
+      sh.rsl[1] = *reinterpret_cast<const RowSlice<4>*>(&sd);
+    }
+    __syncthreads();
+    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), C, b, i, kb,
+                    has_draft && P.topp_draft, X, sh.row_t, sh.row_d);
+  }
 
   // ---- verdict (every CTA), publication (rank 0, one thread) ----
   if (tid == 0) judge<ES, TOPP>(P, sh, i, kb, greedy, has_draft, X, sh.row_t, sh.row_d, bad_t, bad_d, sh.dq);
@@ -2040,7 +2235,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
         write_outputs(P, b, 0, -1, true);
         atomicOr(P.flags, ebj);
       } else if (greedy) {
-        const int a = j1 == i ? row_t.amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j1].argmax);
+        const int a = j1 == i ? sh.row_t.amax : __ldcg(&P.stats[(size_t)b * (P.K + 1) + j1].argmax);
         write_outputs(P, b, j1, a, false);
       } else {
         prefix_resolved(P, b, j1);
@@ -2061,7 +2256,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
 
   // ======================= this item's draw =======================
   const float uK = sh.uK;
-  DF S_t = row_t.s, S_d = row_d.s;
+  DF S_t = sh.row_t.s, S_d = sh.row_d.s;
   uint32_t kt = 0u, kd = 0u;
   int nkt = 0x7fffffff, cntt = 0, nkd = 0x7fffffff, cntd = 0;
   if (TOPP) {  // kept masses and cuts of this item's rows
@@ -2076,7 +2271,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
       cntd = sh.ts[1].cstar;
     }
   }
-  finish<ES, TOPP>(P, sh, vals, cluster, C, rank, b, kb, T, i, uK, e0, e1, row_t.R, row_d.R, S_t, S_d,
+  finish<ES, TOPP>(P, sh, vals, C, rank, b, kb, T, i, uK, e0, e1, sh.row_t.R, sh.row_d.R, S_t, S_d,
                    kt, nkt, cntt, kd, nkd, cntd);
 }
 
@@ -2089,7 +2284,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const VerifyParams 
 // P.K positions per sequence; uniforms and outputs are [B][K].
 // ---------------------------------------------------------------------------
 template <int ES, bool TOPP>
-__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_constant__ VerifyParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -2125,11 +2320,13 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyParams 
   if (tid == 0) {
     sh.skip = 0;
     sh.moot = 0;
+    sh.lth[0] = sh.lth[1] = 0u;
   }
   if (tid == 32) sh.uK = greedy ? 0.f : P.unif[(size_t)b * P.K + i];
   __syncthreads();
   RowAcc at = acc_init(), ad = acc_init();
-  stream_slices<ES, false>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad);
+  stream_slices<ES, false, TOPP>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
+                                 reinterpret_cast<uint2*>(reinterpret_cast<char*>(vals) + kListOff));
   combine_rows(sh, cluster, C, rank, at, ad, greedy, false, false);  // (never moot here)
   const RowAcc row_t = sh.row_t;
   const bool bad = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
@@ -2148,15 +2345,20 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const VerifyParams 
   uint32_t kt = 0u;
   int nkt = 0x7fffffff, cntt = 0;
   if (TOPP) {  // (kb = i: no draft token of this row enters the tie count)
-    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), cluster, C, b, i, i, false, X,
-                    st, st, sh.row_t, sh.row_d);
+    if (tid == 0) {
+      sh.rsl[0] = *reinterpret_cast<const RowSlice<4>*>(&st);
+      sh.rsl[1] = sh.rsl[0];
+    }
+    __syncthreads();
+    topp_select<ES>(P, sh, reinterpret_cast<unsigned char*>(vals), C, b, i, i, false, X, sh.row_t,
+                    sh.row_d);
     S_t = sh.ts[0].E;
     kt = sh.ts[0].kstar;
     nkt = sh.ts[0].nk;
     cntt = sh.ts[0].cstar;
   }
   // j = k_b = i: the draw's weights are p' alone, as for a bonus token
-  finish<ES, TOPP, true>(P, sh, vals, cluster, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
+  finish<ES, TOPP, true>(P, sh, vals, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
                          S_t, kt, nkt, cntt, 0u, 0x7fffffff, 0);
 }
 
@@ -2267,7 +2469,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   const bool topp = L.top_p < 1.0f;
   size_t smem = (size_t)rounds * kThreads * sizeof(float);  // the draw's unit sums
   if (smem < (size_t)kRingBytes) smem = kRingBytes;          // the row pass's ring
-  if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
+  if (topp && smem < (size_t)kToppSmemBytes) smem = kToppSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   if (!g_configured[gi]) {
@@ -2349,7 +2551,7 @@ int sample_launch(const SampleLaunch& L, std::string* err) {
   const bool topp = L.top_p < 1.0f;
   size_t smem = (size_t)rounds * kThreads * sizeof(float);
   if (smem < (size_t)kRingBytes) smem = kRingBytes;
-  if (topp && smem < (size_t)kSelSmemBytes) smem = kSelSmemBytes;
+  if (topp && smem < (size_t)kToppSmemBytes) smem = kToppSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   if (!g_configured_sample[gi]) {
