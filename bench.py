@@ -9,9 +9,8 @@ rotated over three identical copies (3.3 GB > the 129 MB L2) so no step
 reuses data cached by the previous one.  ``--workload c1|c3`` times the
 other batch workloads the same way (c3: half greedy, top_p = 0.9);
 ``--workload c4`` times the layer-skip step: draft and target logits from
-hidden states through sv_lmhead_rmsnorm (tcgen05 GEMM), then verify + commit;
-it runs on one GPU per process only and exits with an error under a
-multi-rank launch.  On one GPU the headline run (c2) then also times the
+hidden states through sv_lmhead_rmsnorm (tcgen05 GEMM), then verify + commit.
+On one GPU the headline run (c2) then also times the
 LM head (c4), the top-p batch (c3) and the draft sampler (s2) in the same
 process and reports them under "secondary" (``--no-secondary`` skips them).
 
@@ -431,24 +430,24 @@ def _c4_oracle_step(x, tokens, knobs, B, K):
     return int(knobs["k_per_row"].sum())
 
 
-C4_ONE_GPU = ("c4 runs sv_lmhead_rmsnorm, whose GEMM multicasts W tiles between the CTAs of a "
-              "cluster: it is run on one GPU per process only (--gpus 1, WORLD_SIZE unset or 1)")
-
-
 def run_gpu_c4(args):
     import numpy as np
     import torch
 
     world, rank, local = dist_setup(args)
-    if world > 1 or args.gpus > 1:
-        # refused before anything is built or launched
-        sys.stderr.write("bench.py: " + C4_ONE_GPU + "\n")
-        sys.exit(2)
     torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
     from speculative_decoding_verification_47_gb300 import binding as sb
     from speculative_decoding_verification_47_gb300 import build as bld
     from speculative_decoding_verification_47_gb300 import workloads as wl
-    bld.build()
+    if rank == 0 or not os.path.exists(bld.LIB):
+        bld.build()
+    if pg is not None:
+        pg.barrier()
     B, K = 64, 7
     x = wl.lmhead_inputs()
     M, H, V = x.M, x.H, x.V
@@ -514,6 +513,8 @@ def run_gpu_c4(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
+    if pg is not None:
+        pg.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -522,8 +523,10 @@ def run_gpu_c4(args):
         step(it)
     t_end.record(stream)
     torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
     clk = clocks.stop()
-    ms, total_positions = t_start.elapsed_time(t_end), positions
+    ms, total_positions = reduce_timing(t_start.elapsed_time(t_end), positions, pg, dev)
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b in ev[:args.steps])
     ms_step = ms / args.steps
     value = total_positions / (ms_step * 1e-3)
@@ -561,9 +564,13 @@ def run_gpu_c4(args):
         b.record(stream)
         torch.cuda.synchronize()
         ems = a.elapsed_time(b)
+        if pg is not None:
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            ems = float(t.item())
         h2d = (h_h.numel() + h_ht.numel()) * 2 + sum(t_.numel() * t_.element_size() for t_ in h_small)
         d2h = (o_out.numel() + o_n.numel() + o_seq.numel()) * 4
-        e2e = {"value": positions / (ems / steps_e2e * 1e-3), "unit": "positions/s",
+        e2e = {"value": positions * world / (ems / steps_e2e * 1e-3), "unit": "positions/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps_e2e}
 
     tpeak, tsrc = tensor_peak()
@@ -571,7 +578,7 @@ def run_gpu_c4(args):
         "metric": METRIC,
         "value": value,
         "unit": "positions/s",
-        "n_gpus": 1,
+        "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_step,
@@ -582,7 +589,7 @@ def run_gpu_c4(args):
         "data": "synthetic",
         "config": {"workload": WORKLOADS["c4"], "name": "c4", "B": B, "K": K, "V": V, "M": M, "H": H,
                    "l2": "W (262 MB) > 129 MB L2, streamed from HBM by every LM-head call",
-                   "parallelism": "one GPU (the LM head is run on one GPU per process)"},
+                   "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
                      "frac": achieved / tpeak, "traffic": traffic_for("c4", args.traffic),
                      "kernel": "sv_lmhead_rmsnorm (rmsnorm_kernel + lmhead_gemm_kernel), draft call",
@@ -593,7 +600,9 @@ def run_gpu_c4(args):
         "clocks": clk,
         "device_flags": list(flags),
     }
-    return line
+    if pg is not None:
+        pg.destroy_process_group()
+    return line if rank == 0 else None
 
 
 def run_gpu_s2(args):
@@ -1274,7 +1283,9 @@ def main():
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "c4":
-        print(json.dumps(run_gpu_c4(args)), flush=True)
+        line = run_gpu_c4(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
     elif args.workload == "s2":
         line = run_gpu_s2(args)
         if line is not None:

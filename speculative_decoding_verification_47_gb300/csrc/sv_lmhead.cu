@@ -66,14 +66,22 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// The same box delivered to every CTA of the cluster in `mask` (same smem
-// offset, same mbarrier offset in each)
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t mask) {
+// The address of `p` (in this CTA's shared memory) in the CTA of cluster rank
+// `rank`, as a shared::cluster address.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+// A box into THIS CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (bar: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 
@@ -108,13 +116,33 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
-// ... arriving at the barrier of the same offset in every CTA of `mask`
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(mask)
-      : "memory");
+// Pair form: one arrival on the barrier at shared::cluster address `bar` (in
+// either CTA of the pair) once every tcgen05 operation this thread issued is
+// done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Arrival on a barrier of another CTA of the cluster, releasing this thread's
+// earlier operations at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (for arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint32_t limit = 2048) {
+  for (uint32_t it = 0; it < limit; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(500000u)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes
@@ -218,29 +246,73 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint16_t* _
     scale(*reinterpret_cast<const uint4*>(hr + k), k);
 }
 
+// Epilogue of one accumulator: this thread's TMEM lane is output row `row`
+// (32 lanes per warp), columns n0 .. n0 + BNT - 1, read 32 at a time.
+template <int BNT>
+__device__ __forceinline__ void store_tile(void* out, int out_f32, int M, int N, int row, int n0,
+                                           uint32_t tbase) {
+#pragma unroll 1
+  for (int c = 0; c < BNT; c += 32) {
+    uint32_t v[32];
+    tmem_ld32(tbase + (uint32_t)c, v);
+    const int n = n0 + c;
+    if (row >= M || n >= N) continue;
+    if (out_f32) {
+      float* o = static_cast<float*>(out) + (size_t)row * N + n;
+      if (n + 32 <= N) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<uint4*>(o)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (q < N - n) o[q] = __uint_as_float(v[q]);
+      }
+    } else {
+      uint16_t* o = static_cast<uint16_t*>(out) + (size_t)row * N + n;
+      uint32_t pk[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+      if (n + 32 <= N) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          reinterpret_cast<uint4*>(o)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          if (q < N - n) o[q] = (uint16_t)((q & 1) ? (pk[q >> 1] >> 16) : (pk[q >> 1] & 0xffffu));
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
-// 2. The tcgen05 GEMM: persistent CTAs (one per SM) in clusters of CM along
-//    M.  The CTAs of a cluster compute the CM row tiles of one column block
-//    together: each loads its own y tile and 1/CM of the W tiles, which the
-//    TMA engine multicasts to every CTA of the cluster, so W crosses the L2
-//    interface once per cluster instead of once per CTA.  A stage may be
-//    refilled once every CTA's MMAs have released it (tcgen05.commit
-//    multicast to the stage's barrier in each CTA).  Warp 0 streams operand
+// 2. The tcgen05 GEMM, persistent (one CTA per SM).  Warp 0 streams operand
 //    tiles, warp 1 issues the MMAs into one of two TMEM accumulators (512
 //    columns: tile i uses half i & 1), warps 2-5 drain the other accumulator
 //    to global memory while the next tile accumulates.
+//
+//    2a. lmhead_gemm_kernel: 128 x BN tiles, one CTA each (M <= 128).
+//    2b. lmhead_gemm_pair_kernel: 256 x BN tiles on a CTA pair (a cluster of
+//        two).  The pair's leader issues tcgen05.mma.cta_group::2 (M = 256):
+//        each CTA stages its own 128 rows of y and HALF of the tile's W
+//        columns (BN / 2), and the tensor cores of the two SMs exchange the W
+//        halves, so each SM's shared memory feeds half the W operand it
+//        would feed alone - the traffic (TMA fill plus operand reads) that
+//        capped the single-CTA kernel.  Both CTAs' TMA loads complete on the
+//        leader's stage barrier; the leader's commits free the stage in each
+//        CTA; each CTA's epilogue reads its own TMEM rows and reports to the
+//        leader before its accumulator is reused.
 // ---------------------------------------------------------------------------
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemAlloc = 512;
 
-template <int BNT, int CM>
+template <int BNT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        void* __restrict__ out, int out_f32, int M, int N, int K, uint32_t* flags) {
   static_assert(BNT % 16 == 0 && BNT >= 64 && BNT <= 256, "MMA N");
-  static_assert(CM == 1 || CM == 2 || CM == 4, "cluster size");
   constexpr int kAtoms = (BNT + 63) / 64;  // W tiles of 64 columns per stage
-  constexpr uint16_t kMask = (uint16_t)((1u << CM) - 1u);
   constexpr uint32_t kTx = (uint32_t)(kABytes + kAtoms * kBAtomBytes);
   constexpr uint32_t kIdescT = (kIdesc & ~(0x3Fu << 17)) | ((uint32_t)(BNT >> 3) << 17);
   extern __shared__ uint8_t smem_raw[];
@@ -250,9 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = (M + BM - 1) / BM, nt = (N + BNT - 1) / BNT;
-  const int mg = (mt + CM - 1) / CM;      // row groups of CM tiles
-  const int tiles = mg * nt;              // cluster tiles
-  const int rank = (int)(blockIdx.x % CM), cid = (int)(blockIdx.x / CM), ncl = (int)(gridDim.x / CM);
+  const int tiles = mt * nt;
   const int KB = K / BK;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -260,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CM);  // released by the MMAs of every CTA of the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
@@ -279,8 +349,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  if (CM > 1) cg::this_cluster().sync();  // every CTA's barriers exist before any multicast
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   // The launch may overlap the RMSNorm kernel before it (programmatic stream
@@ -292,18 +361,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {  // ---- TMA producer: one stage counter across all tiles ----
       int g = 0;
       bool ok = true;
-      for (int t = cid; t < tiles && ok; t += ncl) {
-        const int m0 = ((t % mg) * CM + rank) * BM, n0 = (t / mg) * BNT;
-        // this CTA's share of the W boxes of the first k blocks, into L2
-        for (int kb = 0; kb < kPrefetch && kb < KB; ++kb)
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t % mt) * BM, n0 = (t / mt) * BNT;
+        for (int kb = 0; kb < kPrefetch && kb < KB; ++kb)  // W boxes of the first k blocks into L2
 #pragma unroll
-          for (int j = 0; j < kAtoms; ++j)
-            if (j % CM == rank) tma_prefetch_2d(&tmB, n0 + 64 * j, kb * BK);
+          for (int j = 0; j < kAtoms; ++j) tma_prefetch_2d(&tmB, n0 + 64 * j, kb * BK);
         for (int kb = 0; kb < KB; ++kb, ++g) {
           if (kb + kPrefetch < KB) {
 #pragma unroll
-            for (int j = 0; j < kAtoms; ++j)
-              if (j % CM == rank) tma_prefetch_2d(&tmB, n0 + 64 * j, (kb + kPrefetch) * BK);
+            for (int j = 0; j < kAtoms; ++j) tma_prefetch_2d(&tmB, n0 + 64 * j, (kb + kPrefetch) * BK);
           }
           const int s = g % kStages, use = g / kStages;
           if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) {
@@ -315,20 +381,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&full[s], kTx);
           tma_load_2d(a, &tmA, kb * BK, m0, &full[s]);
 #pragma unroll
-          for (int j = 0; j < kAtoms; ++j) {
-            if (CM == 1) tma_load_2d(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s]);
-            else if (j % CM == rank)
-              tma_load_2d_mc(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s], kMask);
-          }
+          for (int j = 0; j < kAtoms; ++j) tma_load_2d(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, &full[s]);
         }
       }
       issued = g;
-      // wait until every stage has been released by all the cluster's MMAs:
-      // no arrival from another CTA is then still on its way to this one
-      for (int i = 0; i < kStages && ok; ++i) {
-        const int gg = g + i, s = gg % kStages, use = gg / kStages;
-        if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) ok = false;
-      }
       if (!ok) {
         atomicOr(flags, SV_FLAG_TIMEOUT);
         failed = 1;
@@ -338,7 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {  // ---- MMA issuer ----
       int g = 0, i = 0;
       bool ok = true;
-      for (int t = cid; t < tiles && ok; t += ncl, ++i) {
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
         const int b = i & 1, ub = i >> 1;
         if (ub > 0 && !mbar_wait_bounded(&acce[b], (uint32_t)((ub - 1) & 1))) {
           ok = false;
@@ -366,8 +422,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 "l"(ad), "l"(bd), "r"(kIdescT), "r"(acc)
                 : "memory");
           }
-          if (CM == 1) tc_commit(&empty[s]);
-          else tc_commit_mc(&empty[s], kMask);
+          tc_commit(&empty[s]);
         }
         if (!ok) break;
         tc_commit(&accf[b]);  // accumulator b complete
@@ -382,7 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---- epilogue warps 2..5: TMEM lanes 32*(warp % 4) .. +31 ----
     const int lg = warp & 3;
     int i = 0;
-    for (int t = cid; t < tiles; t += ncl, ++i) {
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1, ub = i >> 1;
       const bool ok = mbar_wait_bounded(&accf[b], (uint32_t)(ub & 1));
       if (!__all_sync(0xffffffffu, ok)) {
@@ -390,42 +445,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int m0 = ((t % mg) * CM + rank) * BM, n0 = (t / mg) * BNT;
-      const int row = m0 + lg * 32 + lane;
-      const uint32_t tbase = tmem + (uint32_t)(b * 256) + ((uint32_t)(lg * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BNT; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tbase + (uint32_t)c, v);
-        const int n = n0 + c;
-        if (row >= M || n >= N) continue;
-        if (out_f32) {
-          float* o = static_cast<float*>(out) + (size_t)row * N + n;
-          if (n + 32 <= N) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              reinterpret_cast<uint4*>(o)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (q < N - n) o[q] = __uint_as_float(v[q]);
-          }
-        } else {
-          uint16_t* o = static_cast<uint16_t*>(out) + (size_t)row * N + n;
-          uint32_t pk[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-          if (n + 32 <= N) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              reinterpret_cast<uint4*>(o)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (q < N - n) o[q] = (uint16_t)((q & 1) ? (pk[q >> 1] >> 16) : (pk[q >> 1] & 0xffffu));
-          }
-        }
-      }
+      const int m0 = (t % mt) * BM, n0 = (t / mt) * BNT;
+      store_tile<BNT>(out, out_f32, M, N, m0 + lg * 32 + lane, n0,
+                      tmem + (uint32_t)(b * 256) + ((uint32_t)(lg * 32) << 16));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[b]);  // accumulator b may be overwritten
@@ -439,10 +461,205 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int g = consumed; g < issued; ++g)
       (void)mbar_wait_bounded(&full[g % kStages], (uint32_t)((g / kStages) & 1), 64);
   }
-  if (CM > 1) cg::this_cluster().sync();  // no CTA leaves while another may still write to it
-  else __syncthreads();
+  __syncthreads();
   if (warp == 0) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemAlloc)
+                 : "memory");
+  }
+}
+
+// Pair tiles: MS sub-tiles of 256 rows (MS = 1 or 2) x BNT columns.  Each
+// CTA stages, per k block, its 128 rows of every sub-tile and its half of the
+// W columns, so a W tile is staged once for up to 512 rows.  TMEM holds two
+// 256-column accumulators: two tiles in flight with one sub-tile (the
+// epilogue of one overlaps the MMAs of the next), or one tile of two.
+constexpr int kPairStageMax = 2 * kABytes + 2 * kBAtomBytes;  // 48 KB
+constexpr int kPairSmemBytes = 4 * kPairStageMax + 1024;       // + slack to align to 1 KB
+
+template <int MS>
+struct PairShape {
+  static constexpr int kStageBytes = MS * kABytes + 2 * kBAtomBytes;
+  static constexpr int kStages = (kPairSmemBytes - 1024) / kStageBytes;  // 6 (MS 1) or 4 (MS 2)
+  static constexpr int kBufs = 2 / MS;                                   // accumulator sets
+};
+
+template <int BNT, int MS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            void* __restrict__ out, int out_f32, int M, int N, int K, uint32_t* flags) {
+  static_assert(BNT % 32 == 0 && BNT >= 128 && BNT <= 256, "pair MMA N (halves of 64..128 columns)");
+  static_assert(MS == 1 || MS == 2, "sub-tiles per pair tile");
+  using PS = PairShape<MS>;
+  constexpr int kSt = PS::kStages, kSB = PS::kStageBytes, NB = PS::kBufs;
+  constexpr int BH = BNT / 2;                  // W columns staged by each CTA of the pair
+  constexpr int kAtomsH = (BH + 63) / 64;      // W boxes of 64 columns per CTA per stage
+  static_assert(MS * kABytes + kAtomsH * kBAtomBytes <= kSB, "stage size");
+  constexpr uint32_t kTxPair = 2u * (uint32_t)(MS * kABytes + kAtomsH * kBAtomBytes);  // both CTAs
+  // M = 256 (two CTAs of 128 rows), N = BNT
+  constexpr uint32_t kIdescP = (kIdesc & ~((0x3Fu << 17) | (0x1Fu << 24))) | ((uint32_t)(BNT >> 3) << 17) |
+                               ((uint32_t)(256 >> 4) << 24);
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kSt], empty[kSt], accf[NB], acce[NB];
+  __shared__ uint32_t tmem_base;
+  __shared__ int issued, consumed, failed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t half = blockIdx.x & 1u;  // cluster rank; 0 is the pair's leader
+  const int pid = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  constexpr int TR = MS * 2 * BM;  // rows of a pair tile
+  const int mt2 = (M + TR - 1) / TR, nt = (N + BNT - 1) / BNT;
+  const int tiles = mt2 * nt;  // pair tiles, numbered M-fastest
+  const int KB = K / BK;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  if (tid == 0) {
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(&full[s], 1);   // (the leader's: its arrival + both CTAs' bytes)
+      mbar_init(&empty[s], 1);  // one commit from the leader's MMA thread
+    }
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 8);  // (the leader's: four epilogue warps in each CTA)
+    }
+    issued = consumed = failed = 0;
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 0) {  // one warp of each CTA of the pair allocates, together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(kTmemAlloc)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cg::this_cluster().sync();  // both CTAs' barriers and TMEM exist before any remote use
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer (both CTAs): own y rows, own half of W ----
+      int g = 0;
+      bool ok = true;
+      for (int t = pid; t < tiles && ok; t += npairs) {
+        const int m0 = (t % mt2) * TR + (int)half * BM;  // + 256 per sub-tile
+        const int n0 = (t / mt2) * BNT + (int)half * BH;
+        for (int kb = 0; kb < kPrefetch && kb < KB; ++kb)
+#pragma unroll
+          for (int j = 0; j < kAtomsH; ++j) tma_prefetch_2d(&tmB, n0 + 64 * j, kb * BK);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          if (kb + kPrefetch < KB) {
+#pragma unroll
+            for (int j = 0; j < kAtomsH; ++j) tma_prefetch_2d(&tmB, n0 + 64 * j, (kb + kPrefetch) * BK);
+          }
+          const int s = g % kSt, use = g / kSt;
+          if (use > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((use - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + s * kSB;
+          uint8_t* b = a + MS * kABytes;
+          if (half == 0) mbar_arrive_expect_tx(&full[s], kTxPair);
+          const uint32_t fb = cluster_addr(&full[s], 0u);  // the leader's stage barrier
+#pragma unroll
+          for (int ms = 0; ms < MS; ++ms) tma_load_2d_pair(a + ms * kABytes, &tmA, kb * BK, m0 + ms * 2 * BM, fb);
+#pragma unroll
+          for (int j = 0; j < kAtomsH; ++j) tma_load_2d_pair(b + j * kBAtomBytes, &tmB, n0 + 64 * j, kb * BK, fb);
+        }
+      }
+      issued = g;
+      if (!ok) {
+        atomicOr(flags, SV_FLAG_TIMEOUT);
+        failed = 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && half == 0) {  // ---- MMA issuer: the leader only ----
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = pid; t < tiles && ok; t += npairs, ++i) {
+        const int b = i % NB, ub = i / NB;
+        if (ub > 0 && !mbar_wait_cluster_bounded(&acce[b], (uint32_t)((ub - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % kSt, use = g / kSt;
+          if (!mbar_wait_bounded(&full[s], (uint32_t)(use & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_addr(smem + s * kSB);
+          const uint32_t bb = a + MS * kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bd = desc_sw128(bb + 2048u * kk, (uint32_t)kBAtomBytes, 1024u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+#pragma unroll
+            for (int ms = 0; ms < MS; ++ms) {
+              const uint64_t ad = desc_sw128(a + (uint32_t)(ms * kABytes) + 32u * kk, 16u, 1024u);
+              const uint32_t d = tmem + (uint32_t)((b * MS + ms) * 256);
+              asm volatile(
+                  "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                  " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+                  "l"(ad), "l"(bd), "r"(kIdescP), "r"(acc)
+                  : "memory");
+            }
+          }
+          // the stage is free in both CTAs once these MMAs are done
+          tc_commit_pair(cluster_addr(&empty[s], 0u));
+          tc_commit_pair(cluster_addr(&empty[s], 1u));
+        }
+        if (!ok) break;
+        tc_commit_pair(cluster_addr(&accf[b], 0u));  // accumulators complete in both CTAs
+        tc_commit_pair(cluster_addr(&accf[b], 1u));
+      }
+      consumed = g;
+      if (!ok) {
+        atomicOr(flags, SV_FLAG_TIMEOUT);
+        failed = 1;
+      }
+    }
+  } else {
+    // ---- epilogue warps 2..5 (both CTAs): this CTA's 128 rows of each sub-tile ----
+    const int lg = warp & 3;
+    int i = 0;
+    for (int t = pid; t < tiles; t += npairs, ++i) {
+      const int b = i % NB, ub = i / NB;
+      const bool ok = mbar_wait_bounded(&accf[b], (uint32_t)(ub & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) atomicOr(flags, SV_FLAG_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int m0 = (t % mt2) * TR + (int)half * BM, n0 = (t / mt2) * BNT;
+#pragma unroll 1
+      for (int ms = 0; ms < MS; ++ms)
+        store_tile<BNT>(out, out_f32, M, N, m0 + ms * 2 * BM + lg * 32 + lane, n0,
+                        tmem + (uint32_t)((b * MS + ms) * 256) + ((uint32_t)(lg * 32) << 16));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(cluster_addr(&acce[b], 0u));  // (the leader's barrier)
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && failed && half == 0) {
+    // a wait ran out: let the copies already issued (by both CTAs, counted on
+    // the leader's barriers) land before the pair exits
+    for (int g = consumed; g < issued; ++g)
+      (void)mbar_wait_bounded(&full[g % kSt], (uint32_t)((g / kSt) & 1), 64);
+  }
+  cg::this_cluster().sync();  // no CTA leaves while its peer may still signal or read it
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemAlloc)
                  : "memory");
   }
 }
@@ -511,72 +728,89 @@ struct GemmArgs {
   uint32_t* flags;
 };
 
-static void cluster_cfg(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int cm,
-                        cudaStream_t st) {
+// Launch configuration of the persistent GEMM: clusters of `cm` CTAs (1: no
+// cluster; 2: the pair kernel), `smem` dynamic bytes.
+static void gemm_cfg(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, int cm, int smem,
+                     cudaStream_t st) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3((unsigned)grid, 1, 1);
   cfg->blockDim = dim3(kGemmThreads, 1, 1);
-  cfg->dynamicSmemBytes = kSmemBytes;
+  cfg->dynamicSmemBytes = (size_t)smem;
   cfg->stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cm;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  int n = 0;
+  if (cm > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cm;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg->attrs = attr;
-  cfg->numAttrs = 1;
+  cfg->numAttrs = (unsigned)n;
 }
 
-// Clusters of CM that can be resident at once (the grid of the persistent
-// kernel); 0 if the query fails.
-template <int BNT, int CM>
-static int active_clusters() {
+// Work units (CTAs, or CTA pairs for PAIR) that can be resident at once: the
+// grid of the persistent kernel.  0 if the query fails.
+template <int BNT, int MS>  // MS 0: the single-CTA kernel; 1, 2: pair tiles of MS sub-tiles
+static int resident_units() {
+  constexpr bool PAIR = MS > 0;
   static int n = -1;
   if (n < 0) {
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    cluster_cfg(&cfg, attr, CM * 64, CM, nullptr);
+    auto k = PAIR ? lmhead_gemm_pair_kernel<BNT, MS ? MS : 1> : lmhead_gemm_kernel<BNT>;
+    const int smem = PAIR ? kPairSmemBytes : kSmemBytes;
     int c = 0;
-    if (cudaFuncSetAttribute(lmhead_gemm_kernel<BNT, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&c, lmhead_gemm_kernel<BNT, CM>, &cfg) != cudaSuccess)
-      c = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+      if (PAIR) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        gemm_cfg(&cfg, attr, 2 * 64, 2, smem, nullptr);
+        if (cudaOccupancyMaxActiveClusters(&c, k, &cfg) != cudaSuccess) c = 0;
+      } else {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kGemmThreads, smem) == cudaSuccess)
+          c = per_sm * num_sms();
+      }
+    }
     n = c;
   }
   return n;
 }
 
-template <int BNT, int CM>
+template <int BNT, int MS>
 static cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int* grid_out) {
-  const int mt = (g.M + BM - 1) / BM;
-  const int tiles = ((mt + CM - 1) / CM) * ((g.N + BNT - 1) / BNT);
-  int act = active_clusters<BNT, CM>();
-  if (act <= 0) act = num_sms() / CM;
-  const int clusters = tiles < act ? tiles : act;
+  constexpr bool PAIR = MS > 0;
+  const int rows = PAIR ? MS * 2 * BM : BM;
+  const int tiles = ((g.M + rows - 1) / rows) * ((g.N + BNT - 1) / BNT);
+  int act = resident_units<BNT, MS>();
+  if (act <= 0) act = PAIR ? num_sms() / 2 : num_sms();
+  const int units = tiles < act ? tiles : act;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cluster_cfg(&cfg, attr, clusters * CM, CM, st);
+  gemm_cfg(&cfg, attr, units * (PAIR ? 2 : 1), PAIR ? 2 : 1, PAIR ? kPairSmemBytes : kSmemBytes, st);
   // the set-up (barriers, TMEM, tensor maps) overlaps the RMSNorm kernel
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.numAttrs = 2;
-  *grid_out = clusters * CM;
-  return cudaLaunchKernelEx(&cfg, lmhead_gemm_kernel<BNT, CM>, g.a, g.b, g.out, g.out_f32, g.M, g.N, g.K,
-                            g.flags);
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs += 1;
+  *grid_out = units * (PAIR ? 2 : 1);
+  return cudaLaunchKernelEx(&cfg, PAIR ? lmhead_gemm_pair_kernel<BNT, MS ? MS : 1> : lmhead_gemm_kernel<BNT>,
+                            g.a, g.b, g.out, g.out_f32, g.M, g.N, g.K, g.flags);
 }
 
-template <int CM>
-static cudaError_t launch_cm(const GemmArgs& g, cudaStream_t st, int* grid_out) {
-  // tile width: the fewest rounds of cluster tiles over the resident
-  // clusters, weighted by the width (columns one CTA computes), then the widest
-  const int mt = (g.M + BM - 1) / BM, mg = (mt + CM - 1) / CM;
+// Tile width: the fewest rounds of tiles over the resident units, weighted
+// by the width (the columns one tile computes), then the widest.
+template <int MS>
+static cudaError_t launch_widest(const GemmArgs& g, cudaStream_t st, int* grid_out) {
+  constexpr bool PAIR = MS > 0;
+  const int rows = PAIR ? MS * 2 * BM : BM;
+  const int mt = (g.M + rows - 1) / rows;
   const int widths[5] = {256, 224, 192, 160, 128};
-  const int acts[5] = {active_clusters<256, CM>(), active_clusters<224, CM>(), active_clusters<192, CM>(),
-                       active_clusters<160, CM>(), active_clusters<128, CM>()};
+  const int acts[5] = {resident_units<256, MS>(), resident_units<224, MS>(), resident_units<192, MS>(),
+                       resident_units<160, MS>(), resident_units<128, MS>()};
   int best = 0;
   long long best_cost = -1;
   for (int i = 0; i < 5; ++i) {
-    const long long act = acts[i] > 0 ? acts[i] : num_sms() / CM;
-    const long long tiles = (long long)mg * ((g.N + widths[i] - 1) / widths[i]);
+    const long long act = acts[i] > 0 ? acts[i] : (PAIR ? num_sms() / 2 : num_sms());
+    const long long tiles = (long long)mt * ((g.N + widths[i] - 1) / widths[i]);
     const long long cost = ((tiles + act - 1) / act) * widths[i];
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
@@ -584,11 +818,11 @@ static cudaError_t launch_cm(const GemmArgs& g, cudaStream_t st, int* grid_out) 
     }
   }
   switch (widths[best]) {
-    case 224: return launch_gemm<224, CM>(g, st, grid_out);
-    case 192: return launch_gemm<192, CM>(g, st, grid_out);
-    case 160: return launch_gemm<160, CM>(g, st, grid_out);
-    case 128: return launch_gemm<128, CM>(g, st, grid_out);
-    default: return launch_gemm<256, CM>(g, st, grid_out);
+    case 224: return launch_gemm<224, MS>(g, st, grid_out);
+    case 192: return launch_gemm<192, MS>(g, st, grid_out);
+    case 160: return launch_gemm<160, MS>(g, st, grid_out);
+    case 128: return launch_gemm<128, MS>(g, st, grid_out);
+    default: return launch_gemm<256, MS>(g, st, grid_out);
   }
 }
 
@@ -622,14 +856,13 @@ int lmhead_launch(const void* hidden, const void* norm_w, float eps, const void*
     *err = std::string("rmsnorm launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
   }
-  // cluster of CM row tiles sharing the W tiles (CM divides the row tiles)
-  const int mt = (M + BM - 1) / BM;
+  // more than one row tile: tiles of 256 (M <= 256) or 512 rows on CTA pairs
+  // (tcgen05 cta_group::2)
   int grid = 0;
   {
     std::lock_guard<std::mutex> lock(g_mutex);  // one-time attribute setup inside
-    if (mt % 4 == 0) e = launch_cm<4>(g, st, &grid);
-    else if (mt % 2 == 0) e = launch_cm<2>(g, st, &grid);
-    else e = launch_cm<1>(g, st, &grid);
+    e = M > 2 * BM ? launch_widest<2>(g, st, &grid)
+                   : (M > BM ? launch_widest<1>(g, st, &grid) : launch_widest<0>(g, st, &grid));
   }
   if (e != cudaSuccess) {
     *err = std::string("lmhead launch: ") + cudaGetErrorString(e);

@@ -93,19 +93,15 @@ def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
     assert bench.traffic_for("c2", None) is None
 
 
-@pytest.mark.parametrize("env,argv", [
-    ({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}, ()),
-    ({}, ("--gpus", "2")),
-])
-def test_c4_refuses_a_multi_gpu_launch(env, argv):
-    """The LM head's GEMM multicasts W tiles inside a cluster: bench.py runs
-    it on one GPU per process only and refuses a multi-rank or --gpus > 1
-    launch before it builds or launches anything (so this needs no GPU)."""
-    e = dict(os.environ)
-    e.update(env)
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "c4",
-                        "--steps", "1", "--warmup", "3", *argv], cwd=ROOT, env=e,
-                       capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0
-    assert "one GPU per process only" in r.stderr
-    assert r.stdout.strip() == ""
+def test_no_cluster_multicast_in_the_sources():
+    """No kernel of the library uses a cluster-multicast form (TMA loads or
+    tcgen05 commits): the LM head's CTA pairs stage their own rows and their
+    own half of each W tile, so nothing restricts a process or a replica run
+    to one GPU."""
+    import glob
+    srcs = glob.glob(os.path.join(ROOT, "speculative_decoding_verification_47_gb300", "csrc", "*"))
+    assert srcs
+    for p in srcs:
+        with open(p) as f:
+            text = f.read()
+        assert "multicast" not in text, p
