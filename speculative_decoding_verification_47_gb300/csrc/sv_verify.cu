@@ -430,18 +430,19 @@ __device__ __forceinline__ uint4 ldg_unit(const RowSlice<ES>& rs, int u) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-thread candidate lists (top-p instances).  During the row pass each
-// thread keeps, per row, the kListLen largest logits it admitted (key and
-// index, keys descending; key 0 = empty slot) in shared memory, slot k of row
-// r at lst[(r * kListLen + k) * kThreads + tid].  A logit is admitted only if
-// it is strictly larger than the thread's last entry (once its list is full)
-// and than the CTA's floor T (sh.lth[r]): the largest last-entry key any full
-// list of the CTA has had, raised with atomicMax as lists fill.  T only grows,
-// so every logit left out has a key <= the final T; with theta = the largest
-// final T over the cluster's CTAs, the lists together hold EVERY token of the
-// row whose key exceeds theta.  A top-p selection pass whose key window lies
-// above theta can therefore read the lists instead of the row (at most
-// kListLen entries per thread).
+// Per-thread unit lists (top-p instances).  During the row pass each thread
+// keeps, per row, the kListLen units of its slice with the largest maxima
+// (the max's key and the unit's index, keys descending; key 0 = empty slot)
+// in shared memory, slot k of row r at lst[(r * kListLen + k) * kThreads +
+// tid].  A unit is recorded only if its max is strictly larger than the
+// thread's last entry (once the list is full) and than the CTA's floor T
+// (sh.lth[r]): the largest last-entry key any full list of the CTA has had,
+// raised with atomicMax as lists fill.  T only grows, so every unit left out
+// (or pushed out later) has a max key <= the final T; with theta = the
+// largest final T over the cluster's CTAs, every token of the row whose key
+// exceeds theta lies in a recorded unit.  The selection re-reads just those
+// units to collect the candidates above theta (at most kListLen units per
+// thread and row).
 // ---------------------------------------------------------------------------
 constexpr int kListLen = 4;
 
@@ -451,42 +452,6 @@ __device__ __forceinline__ float key_val(uint32_t k) {
   return k ? bits_val<ES>(key_bits<ES>(k)) : -INFINITY;
 }
 
-// Insert one logit (bit pattern, index) into this thread's list of row r;
-// returns the list's floor key (its last entry's key once full, else 0).
-template <int ES>
-__device__ __forceinline__ uint32_t list_add(uint2* lst, int r, uint32_t bits, int idx) {
-  uint2 cur = make_uint2(okey<ES>(bits), (uint32_t)idx);
-  uint2* base = lst + (size_t)r * kListLen * kThreads + threadIdx.x;
-#pragma unroll
-  for (int k = 0; k < kListLen; ++k) {  // insertion from the top (empty slots hold key 0)
-    const uint2 e = base[k * kThreads];
-    if (cur.x > e.x) {
-      base[k * kThreads] = cur;
-      cur = e;
-    }
-  }
-  return base[(kListLen - 1) * kThreads].x;
-}
-
-// Slots of a full unit whose value is strictly above thr (bit j = slot j).
-template <int ES>
-__device__ __forceinline__ uint32_t above_mask(const uint4& v, float thr) {
-  if (ES == 2) {
-    const uint32_t tb = __float_as_uint(thr) >> 16;  // (thr is a bf16 value or -inf)
-    const uint32_t t2 = tb | (tb << 16);
-    const __nv_bfloat162 f = *reinterpret_cast<const __nv_bfloat162*>(&t2);
-    const uint32_t m0 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.x), f);
-    const uint32_t m1 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.y), f);
-    const uint32_t m2 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.z), f);
-    const uint32_t m3 = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&v.w), f);
-    const uint32_t m = (m0 & 0x10001u) | ((m1 & 0x10001u) << 2) | ((m2 & 0x10001u) << 4) |
-                       ((m3 & 0x10001u) << 6);
-    return (m | (m >> 15)) & 0xffu;
-  } else {
-    return (__uint_as_float(v.x) > thr ? 1u : 0u) | (__uint_as_float(v.y) > thr ? 2u : 0u) |
-           (__uint_as_float(v.z) > thr ? 4u : 0u) | (__uint_as_float(v.w) > thr ? 8u : 0u);
-  }
-}
 
 // Combine row accumulators over groups of W lanes of a warp (W a power of
 // two; lanes with valid == false contribute nothing): xor butterflies over
@@ -716,6 +681,13 @@ constexpr int kSelSmemBytes = kHistBytes + kStageBytes;
 constexpr int kListOff = ((kSelSmemBytes > kRingBytes ? kSelSmemBytes : kRingBytes) + 255) / 256 * 256;
 constexpr int kListBytes = 2 * kListLen * kThreads * 8;
 constexpr int kToppSmemBytes = kListOff + kListBytes;
+// candidates above the cluster's floor (top-p instances): this CTA's at the
+// start of the dynamic area, the cluster's gathered after them, and the
+// cluster's in rank order over the unit lists once those are read
+constexpr int kUOwn = 512;   // candidates one CTA may contribute per row
+constexpr int kUCap = 1024;  // candidates per row over the cluster
+constexpr int kUAllOff = 2 * kUOwn * 8;
+static_assert(kUAllOff + 2 * kUCap * 8 <= kListOff && 2 * kUCap * 8 <= kListBytes, "candidate areas");
 constexpr int kMaxSelPasses = 12;
 
 struct TopSel {
@@ -761,8 +733,15 @@ struct Shared {
   RowAcc row_t, row_d;
   DF S_w, rem;
   int skip, moot;
-  uint32_t lth[2];          // this CTA's largest candidate-list floor per row
+  uint32_t lth[2];          // this CTA's floor of the unit lists, per row
   uint32_t g_th[kCmax][2];  // all-gather of every CTA's lth
+  // candidates above the cluster's floor (top-p): this CTA's count, every
+  // CTA's offset, the total, whether the exact cut came from them, the cut's
+  // rank and the key range of the cut key; the draw's location
+  uint32_t ucnt[2], uoff[2][kCmax], utot[2];
+  int uok[2], ubelow[2], ucut[2], ua[2], ub[2], ult[2];
+  DF uE[2];
+  int ypos, ylast;
   int fin;
   int owner, rsel;
   int x;
@@ -1002,26 +981,6 @@ __device__ __forceinline__ uint32_t sel_bits(const SelP& p, unsigned char* h, co
   return lt;
 }
 
-// A selection pass over this thread's candidate list of row r (the window
-// lies above the cluster's list floor, so the lists hold every token of the
-// window and above it).
-template <int ES>
-__device__ __noinline__ uint32_t sel_list(const TopSel* tp, unsigned char* h, const uint2* lst, int r,
-                                          int x, float chi, float clo, DF* above) {
-  const SelP p = sel_params(*tp, ES);
-  const Expo X{chi, clo};
-  uint32_t lt = 0;
-  DF ab = *above;
-  const uint2* base = lst + (size_t)r * kListLen * kThreads + threadIdx.x;
-#pragma unroll
-  for (int k = 0; k < kListLen; ++k) {
-    const uint2 e = base[k * kThreads];
-    if (e.x == 0u) break;  // (keys descend; the rest is empty)
-    lt += sel_key<ES>(p, h, key_bits<ES>(e.x), (int)e.y, x, X, &ab);
-  }
-  *above = ab;
-  return lt;
-}
 
 // A partial unit at a slice end, as a 16-byte unit: the slots of elements in
 // [e0, e1) are set in *valid, the others are zero.
@@ -1348,6 +1307,210 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
   __syncthreads();
 }
 
+// Rank order of candidates (key, index): by key descending, then index
+// ascending; "ranked before" is a larger composite.
+__device__ __forceinline__ unsigned long long cand_order(uint2 e) {
+  return ((unsigned long long)e.x << 32) | (unsigned long long)(~e.y);
+}
+
+// Candidates of a segment sorted in rank order that are ranked before e.
+__device__ __forceinline__ int cand_before(const uint2* seg, int n, unsigned long long ce) {
+  int lo = 0, hi = n;  // the first position whose candidate is not ranked before e
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cand_order(seg[mid]) > ce) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Exact top-p cut of each row from its candidates: every token whose key
+// exceeds the cluster's list floor theta (sh.ts[r].lth).  Each CTA collects
+// the candidates of its slice from the units its threads recorded, every CTA
+// gathers all of them (at most kUCap per row; each CTA sorts its own first, so
+// a candidate's rank is its place in its own sorted list plus a binary search
+// in each other one), and walks their masses from the top [FS §3.2]: the first candidate
+// whose mass ranked before it exceeds top_p * S is the first dropped token.
+// Rows resolved this way get mode 0 and keep the ranked candidates (the kept
+// ones are ranks 0 .. ucut - 1) for the draw.  A row whose candidates overflow
+// keeps its full window; a row whose candidates are all kept (the cut lies
+// at or below theta) gets the window [flo, theta]; both go to the passes.
+template <int ES>
+__device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, unsigned char* dyn, int C,
+                                             int nrows, const Expo X) {
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int EPU = 16 / ES;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint2* own = reinterpret_cast<uint2*>(dyn);
+  uint2* all = reinterpret_cast<uint2*>(dyn + kUAllOff);
+  uint2* srt = reinterpret_cast<uint2*>(dyn + kListOff);  // (the unit lists until step 4)
+  const uint2* lst = srt;
+  if (tid < 2) {
+    sh.ucnt[tid] = 0u;
+    sh.ucut[tid] = 0x7fffffff;
+    sh.ua[tid] = 0x7fffffff;
+    sh.ub[tid] = 0;
+    sh.ult[tid] = 0;
+    sh.uok[tid] = 0;
+    sh.ubelow[tid] = 0;
+  }
+  __syncthreads();
+  // 1. the elements above the floor in this thread's recorded units
+  for (int r = 0; r < nrows; ++r) {
+    const uint32_t th = sh.ts[r].lth;
+    const RowSlice<ES>& rs = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[r]);
+    const int b0 = rs.ub0(), b1 = rs.ub1();
+#pragma unroll 1
+    for (int k = 0; k < kListLen; ++k) {
+      const uint2 e = lst[(r * kListLen + k) * kThreads + tid];
+      if (e.x <= th) break;  // (keys descend; empty slots hold 0)
+      const int u = (int)e.y, eb = rs.ebase0 + u * EPU;
+      uint32_t valid = (1u << EPU) - 1u;
+      const uint4 v = (u >= b0 && u < b1) ? ldg_unit(rs, u) : edge_unit<ES>(rs, eb, &valid);
+#pragma unroll 1
+      for (int j = 0; j < EPU; ++j) {
+        if (!((valid >> j) & 1u)) continue;
+        const uint32_t key = okey<ES>(unit_bits<ES>(v, j));
+        if (key > th) {
+          const uint32_t pos = atomicAdd(&sh.ucnt[r], 1u);
+          if (pos < (uint32_t)kUOwn) own[r * kUOwn + pos] = make_uint2(key, (uint32_t)(eb + j));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // 1b. this CTA's candidates in rank order (through the gather area, which
+  //     is not used before the next cluster barrier)
+  for (int r = 0; r < nrows; ++r) {
+    const int n = (int)min(sh.ucnt[r], (uint32_t)kUOwn);
+    const uint2* o = own + r * kUOwn;
+    for (int i = tid; i < n; i += kThreads) {
+      const uint2 e = o[i];
+      const unsigned long long ce = cand_order(e);
+      int before = 0;
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) before += cand_order(o[j]) > ce ? 1 : 0;
+      all[r * kUCap + before] = e;
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < nrows; ++r) {
+    const int n = (int)min(sh.ucnt[r], (uint32_t)kUOwn);
+    for (int i = tid; i < n; i += kThreads) own[r * kUOwn + i] = all[r * kUCap + i];
+  }
+  csync(cluster, C);  // every CTA's candidates are complete, in rank order
+  // 2. every CTA's count: offsets, total, overflow (the same in every CTA)
+  if (tid < nrows) {
+    uint32_t tot = 0u;
+    bool ovf = false;
+    for (int q = 0; q < C; ++q) {
+      const uint32_t c = *remote(cluster, C, &sh.ucnt[tid], q);
+      sh.uoff[tid][q] = tot;
+      tot += c;
+      ovf |= c > (uint32_t)kUOwn;
+    }
+    sh.utot[tid] = tot;
+    sh.uok[tid] = (!ovf && tot <= (uint32_t)kUCap) ? 1 : 0;
+  }
+  __syncthreads();
+  // 3. gather every CTA's candidates (in rank order of the CTAs)
+  for (int r = 0; r < nrows; ++r) {
+    if (!sh.uok[r]) continue;
+    for (int q = 0; q < C; ++q) {
+      const uint32_t o = sh.uoff[r][q], c = (q + 1 < C ? sh.uoff[r][q + 1] : sh.utot[r]) - o;
+      const uint2* src = remote(cluster, C, own, q) + r * kUOwn;
+      for (uint32_t i = tid; i < c; i += kThreads) all[r * kUCap + o + i] = src[i];
+    }
+  }
+  __syncthreads();
+  // 4. rank: tokens ranked before a candidate have a larger key, or the same
+  //    key at a smaller index; each CTA's segment of the gathered candidates
+  //    is in rank order (the lists are read: their area takes the ranks)
+  for (int r = 0; r < nrows; ++r) {
+    if (!sh.uok[r]) continue;
+    const int n = (int)sh.utot[r];
+    const uint2* a = all + r * kUCap;
+    int q0 = 0;
+    for (int i = tid; i < n; i += kThreads) {
+      while (q0 + 1 < C && (uint32_t)i >= sh.uoff[r][q0 + 1]) ++q0;  // (i only grows)
+      const uint2 e = a[i];
+      const unsigned long long ce = cand_order(e);
+      int before = i - (int)sh.uoff[r][q0];
+      for (int q = 0; q < C; ++q) {
+        if (q == q0) continue;
+        const int o = (int)sh.uoff[r][q], c = (q + 1 < C ? (int)sh.uoff[r][q + 1] : n) - o;
+        before += cand_before(a + o, c, ce);
+      }
+      srt[r * kUCap + before] = e;
+    }
+  }
+  __syncthreads();
+  // 5. masses in rank order: the first candidate whose exclusive prefix
+  //    exceeds top_p * S is the first dropped token
+  const int x = sh.xtok;
+  for (int r = 0; r < nrows; ++r) {
+    if (!sh.uok[r]) continue;  // (uniform in the cluster)
+    const int n = (int)sh.utot[r];
+    const TopSel& t = sh.ts[r];
+    const uint2* a = srt + r * kUCap;
+    const int c = kThreads - 1 - tid;  // chunk: ranks 4c .. 4c+3 (the suffix over threads is the prefix over chunks)
+    float m[4];
+    DF loc{0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 4 * c + q;
+      m[q] = i < n ? e2(bits_val<ES>(key_bits<ES>(a[i].x)), X, -t.R) : 0.f;
+      df_acc(loc, m[q]);
+    }
+    const DF pre = block_suffix_excl(loc, sh.scan, lane, warp);
+    DF run = pre;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 4 * c + q;
+      if (i < n && df_gt(run, t.thr)) {
+        atomicMin(&sh.ucut[r], i);
+        break;
+      }
+      run = df_add(run, DF{m[q], 0.f});
+    }
+    __syncthreads();
+    const int rc = sh.ucut[r];
+    if (rc != 0x7fffffff) {
+      const uint32_t kk = a[rc].x;
+      if (rc >= 4 * c && rc < 4 * c + 4) {  // this thread's chunk holds the cut: its kept mass
+        DF ex = pre;
+        for (int q = 0; q < rc - 4 * c; ++q) ex = df_add(ex, DF{m[q], 0.f});
+        sh.uE[r] = ex;
+      }
+      for (int i = tid; i < n; i += kThreads) {
+        const uint2 e = a[i];
+        if (e.x == kk) {
+          atomicMin(&sh.ua[r], i);
+          atomicMax(&sh.ub[r], i + 1);
+        }
+        if (x >= 0 && e.x == t.kx && (int)e.y < x) atomicAdd(&sh.ult[r], 1);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      TopSel& w = sh.ts[r];
+      if (rc == 0x7fffffff) {  // every candidate kept: the cut lies at or below theta
+        sh.uok[r] = 0;
+        sh.ubelow[r] = 1;
+      } else {
+        w.kstar = a[rc].x;
+        w.cstar = sh.ub[r] - sh.ua[r];
+        w.nk = rc - sh.ua[r];
+        w.lt = sh.ult[r];
+        w.E = sh.uE[r];
+        w.mode = 0;
+      }
+    }
+    __syncthreads();
+  }
+  csync(cluster, C);  // every CTA has read this CTA's candidates
+}
+
 // Top-p cut of the target row (and of the draft row when `two`) of one item.
 // Every CTA of the cluster ends with the same sh.ts[] results.
 template <int ES>
@@ -1385,9 +1548,6 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     t.lo = min(lo, t.hi);
     t.flo = t.lo;
     t.fhi = t.hi;
-    // the lists hold every token above the floor: start with the window
-    // above it (if it leaves any key), whose passes read only the lists
-    if (t.lth < t.hi && t.lth >= t.lo) t.lo = t.lth + 1u;
     t.chi = X.chi;
     sel_set_mode<ES>(t, true);
     t.kx = x >= 0 ? okey<ES>(rs.bits(x)) : 0u;
@@ -1397,6 +1557,19 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     t.lt = 0;
     t.E = row.s;
     sh.ts[r] = t;
+  }
+  __syncthreads();
+  // The exact cut from the candidates above the lists' floor; the rows it
+  // leaves open search by passes over the slices.
+  topp_candidates<ES>(P, sh, hist, C, two ? 2 : 1, X);
+  if (tid < 2 && (tid == 0 || two) && !sh.uok[tid]) {
+    TopSel& t = sh.ts[tid];
+    if (sh.ubelow[tid] && t.lth >= t.flo && t.lth < t.fhi) {  // every candidate kept: the cut is at or below theta
+      t.fhi = t.lth;
+      t.hi = t.lth;
+    }
+    t.lo = t.flo;
+    sel_set_mode<ES>(t, true);
   }
   __syncthreads();
   for (int pass = 0; pass < kMaxSelPasses; ++pass) {
@@ -1415,15 +1588,8 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     DF ab0{0.f, 0.f}, ab1{0.f, 0.f};
     unsigned char* h1 = hist + kHistRowBytes;
     uint4* stage = reinterpret_cast<uint4*>(hist + kHistBytes);
-    // (whether a row reads its lists is uniform in the cluster: every CTA
-    // holds the same window and floor)
-    const uint2* lst = reinterpret_cast<const uint2*>(hist + kListOff);
-    if (a0)
-      l0 = sh.ts[0].lo > sh.ts[0].lth ? sel_list<ES>(&sh.ts[0], hist, lst, 0, x, X.chi, X.clo, &ab0)
-                                      : sel_stream<ES>(&sh.ts[0], hist, stage, st, x, X.chi, X.clo, &ab0);
-    if (a1)
-      l1 = sh.ts[1].lo > sh.ts[1].lth ? sel_list<ES>(&sh.ts[1], h1, lst, 1, x, X.chi, X.clo, &ab1)
-                                      : sel_stream<ES>(&sh.ts[1], h1, stage, sd, x, X.chi, X.clo, &ab1);
+    if (a0) l0 = sel_stream<ES>(&sh.ts[0], hist, stage, st, x, X.chi, X.clo, &ab0);
+    if (a1) l1 = sel_stream<ES>(&sh.ts[1], h1, stage, sd, x, X.chi, X.clo, &ab1);
     // the CTA's lt count (count passes) and mass above the window (fixed order)
     if (c0 && l0) atomicAdd(reinterpret_cast<uint32_t*>(hist) + kSlotLt, l0);
     if (c1 && l1) atomicAdd(reinterpret_cast<uint32_t*>(h1) + kSlotLt, l1);
@@ -1553,6 +1719,124 @@ __device__ __noinline__ int tie_cut(Shared& sh, uint32_t* iv, int C, int rank, i
 }
 
 // ---------------------------------------------------------------------------
+// Draw of a top-p item whose cuts came from the candidates (one CTA): the
+// kept target tokens are the target's ranked candidates 0 .. ucut[0] - 1, so
+// the residual max(0, p' - q') (or p' alone) is non-zero on them only.  Each
+// takes its weight w = max(0, e_t - rho * e_d) as the row draw computes it
+// (e_d from the draft's logit at the token, 0 if the draft's cut drops it),
+// and the draw is the inverse CDF of w in index order with the uniform uK.
+// ---------------------------------------------------------------------------
+template <int ES, bool SAMPLE>
+__device__ __noinline__ void draw_candidates(const VerifyParams& P, Shared& sh, unsigned char* dyn, int b,
+                                             int kb, int j, float uK, float T, float Rt, float Rd, DF S_t,
+                                             DF S_d) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool bonus = (j == kb);
+  const Expo X = make_expo(T);
+  const uint2* srt = reinterpret_cast<const uint2*>(dyn + kListOff);
+  float* wv = reinterpret_cast<float*>(dyn);         // weight of kept candidate i (rank order)
+  uint2* byi = reinterpret_cast<uint2*>(dyn + 4 * kUCap);  // (index, weight) in index order
+  const int n = sh.ucut[0];
+  bool p_only = bonus;
+  float rho_hi = 0.f, rho_lo = 0.f;
+  if (!p_only) {
+    const DF rho = df_div(S_t, S_d);
+    rho_hi = rho.hi;
+    rho_lo = rho.lo;
+  }
+  // the draft's cut: key kd, and the first dropped index cd among its tokens
+  const bool dcut = !p_only && P.topp_draft;
+  const uint32_t kd = dcut ? sh.ts[1].kstar : 0u;
+  const int cd = dcut ? (int)srt[kUCap + sh.ucut[1]].y : 0x7fffffff;
+  const char* drow = p_only ? nullptr : P.drf + (long long)b * P.d_seq + (long long)j * P.d_pos;
+  DF loc{0.f, 0.f};
+  for (int i = tid; i < n; i += kThreads) {
+    const uint2 e = srt[i];
+    const float a = e2(bits_val<ES>(key_bits<ES>(e.x)), X, -Rt);
+    float w = a;
+    if (!p_only) {
+      const uint32_t bd = ES == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(drow + (size_t)e.y * 2)
+                                  : *reinterpret_cast<const uint32_t*>(drow + (size_t)e.y * 4);
+      const uint32_t kyd = okey<ES>(bd);
+      const bool keptd = !dcut || kyd > kd || (kyd == kd && (int)e.y < cd);
+      const float q = keptd ? e2(bits_val<ES>(bd), X, -Rd) : 0.f;
+      w = fmaxf(0.f, __fmaf_rn(-rho_lo, q, __fmaf_rn(-rho_hi, q, a)));
+    }
+    wv[i] = w;
+    df_acc(loc, w);
+  }
+  DF tot = df_warp_sum(loc);
+  if (lane == 0) sh.scan[warp] = tot;
+  __syncthreads();
+  tot = DF{0.f, 0.f};
+  for (int w_ = 0; w_ < kWarps; ++w_) tot = df_add(tot, sh.scan[w_]);
+  if (!df_pos(tot) && !p_only) {  // residual all zero: draw from p  [SSD §4.3]
+    p_only = true;
+    loc = DF{0.f, 0.f};
+    __syncthreads();  // (every thread has read sh.scan)
+    for (int i = tid; i < n; i += kThreads) {
+      const float a = e2(bits_val<ES>(key_bits<ES>(srt[i].x)), X, -Rt);
+      wv[i] = a;
+      df_acc(loc, a);
+    }
+    tot = df_warp_sum(loc);
+    if (lane == 0) sh.scan[warp] = tot;
+    __syncthreads();
+    tot = DF{0.f, 0.f};
+    for (int w_ = 0; w_ < kWarps; ++w_) tot = df_add(tot, sh.scan[w_]);
+  }
+  // index order: the position of candidate i among the kept ones
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t v = srt[i].y;
+    int before = 0;
+#pragma unroll 4
+    for (int k = 0; k < n; ++k) before += srt[k].y < v ? 1 : 0;
+    byi[before] = make_uint2(v, __float_as_uint(wv[i]));
+  }
+  if (tid == 0) {
+    sh.ypos = 0x7fffffff;
+    sh.ylast = -1;
+  }
+  __syncthreads();
+  // inclusive prefix in index order; y = the first token whose prefix passes u * sum(w)
+  const DF tgt = df_mul_f(tot, uK);
+  const int c = kThreads - 1 - tid;  // chunk: positions 4c .. 4c+3
+  float wq[4];
+  DF lsum{0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = 4 * c + q;
+    wq[q] = i < n ? __uint_as_float(byi[i].y) : 0.f;
+    df_acc(lsum, wq[q]);
+  }
+  DF run = block_suffix_excl(lsum, sh.scan, lane, warp);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int i = 4 * c + q;
+    if (i < n && wq[q] > 0.f) {
+      run = df_add(run, DF{wq[q], 0.f});
+      atomicMax(&sh.ylast, i);
+      if (df_gt(run, tgt)) {
+        atomicMin(&sh.ypos, i);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int pos = sh.ypos;
+    if (pos == 0x7fffffff) pos = sh.ylast;  // past the end by rounding: the last positive weight
+    const int y = pos >= 0 ? (int)byi[pos].x : -1;
+    if (!SAMPLE && P.diag) {
+      float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
+      dg[SV_DIAG_S_W] = p_only ? 1.f : df_to_float(df_div(tot, S_t));
+    }
+    if (SAMPLE) P.out[(size_t)b * P.K + j] = y;
+    else draw_ready(P, b, j, kb, y);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Draw of the resample (or bonus) token of sequence b at position j with the
 // uniform uK, made by item j itself right after its verdict.  Every CTA of
 // the cluster takes part.  One pass over both rows puts each thread's unit
@@ -1570,6 +1854,14 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool bonus = (j == kb);
+  if (TOPP && sh.uok[0] && (bonus || !P.topp_draft || sh.uok[1])) {
+    // the cuts came from the candidates, which hold every kept token: one CTA
+    // draws from them (no row is read again)
+    if (rank == 0)
+      draw_candidates<ES, SAMPLE>(P, sh, reinterpret_cast<unsigned char*>(vals), b, kb, j, uK, T, Rt, Rd,
+                                  S_t, S_d);
+    return;
+  }
   const Expo X = make_expo(T);
   PairRead<ES> pr;
   pr.st.init(P.tgt + (long long)b * P.t_seq + (long long)j * P.t_pos, e0, e1);
@@ -1855,21 +2147,26 @@ __device__ __noinline__ int publish(const VerifyParams& P, Shared& sh, int i, in
   return (!was && now) ? 1 : 0;
 }
 
-// The elements of a full unit above thr go into the list of row r; thr
-// becomes the list's floor value once the list is full, and a higher floor is
-// published to the CTA's floor T.  (Out of line: reached by a few units.)
+// Record unit u, whose max has key `key`, in this thread's list of row r; a
+// full list's floor goes to the CTA's floor T.  Returns the thread's new
+// admission threshold (value).
 template <int ES>
-__device__ __noinline__ float list_add_unit(Shared& sh, uint2* lst, int r, uint4 v, int eb, float thr) {
-  uint32_t m = above_mask<ES>(v, thr);
-  uint32_t f = 0;
-  while (m) {
-    const int j = __ffs(m) - 1;
-    m &= m - 1u;
-    const uint32_t b = unit_bits<ES>(v, j);
-    if (bits_val<ES>(b) > thr) f = list_add<ES>(lst, r, b, eb + j);  // (thr may have risen)
-    if (f) thr = fmaxf(thr, key_val<ES>(f));
+__device__ __forceinline__ float list_unit(Shared& sh, uint2* lst, int r, uint32_t key, int u, float thr) {
+  uint2 cur = make_uint2(key, (uint32_t)u);
+  uint2* base = lst + (size_t)r * kListLen * kThreads + threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < kListLen; ++k) {  // insertion from the top (empty slots hold key 0)
+    const uint2 e = base[k * kThreads];
+    if (cur.x > e.x) {
+      base[k * kThreads] = cur;
+      cur = e;
+    }
   }
-  if (f) atomicMax(&sh.lth[r], f);
+  const uint32_t f = base[(kListLen - 1) * kThreads].x;
+  if (f) {
+    atomicMax(&sh.lth[r], f);
+    thr = fmaxf(thr, key_val<ES>(f));
+  }
   return thr;
 }
 
@@ -1885,9 +2182,10 @@ __device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, in
       greedy_unit<ES>(a, v, eb);
     } else {
       const float g = sampled_unit<ES, LISTS>(a, v, x);
-      if (LISTS && g > *thr) *thr = list_add_unit<ES>(*sh, lst, r, v, eb, *thr);
+      if (LISTS && g > *thr) *thr = list_unit<ES>(*sh, lst, r, okey<ES>(val_bits<ES>(g)), u, *thr);
     }
   } else if (u < rs.n_units) {
+    float g = -INFINITY;  // (a partial unit's max over its valid elements)
     for (int j = 0; j < EPU; ++j) {
       const int e = eb + j;
       if (e < rs.e0 || e >= rs.e1) continue;
@@ -1896,15 +2194,10 @@ __device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, in
         greedy_elem(a, z, e);
       } else {
         sampled_elem(a, z, x);
-        if (LISTS && z > *thr) {
-          const uint32_t f = list_add<ES>(lst, r, rs.bits(e), e);
-          if (f) {
-            atomicMax(&sh->lth[r], f);
-            *thr = fmaxf(*thr, key_val<ES>(f));
-          }
-        }
+        g = fmaxf(g, z);
       }
     }
+    if (LISTS && !greedy && g > *thr) *thr = list_unit<ES>(*sh, lst, r, okey<ES>(val_bits<ES>(g)), u, *thr);
   }
 }
 
@@ -2007,8 +2300,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
             greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
           } else {
             const float g = sampled_unit<ES, LISTS>(at, vt, X);
-            if (LISTS && g > thr0)
-              thr0 = list_add_unit<ES>(sh, lst, 0, vt, st.ebase0 + (u0 + k * kThreads) * EPU, thr0);
+            if (LISTS && g > thr0) thr0 = list_unit<ES>(sh, lst, 0, okey<ES>(val_bits<ES>(g)), u0 + k * kThreads, thr0);
           }
         }
         if (has_draft) {
@@ -2016,8 +2308,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
           for (int k = 0; k < L; ++k) {
             const uint4 vd = slot[(L + k) * kThreads];
             const float g = sampled_unit<ES, LISTS>(ad, vd, X);
-            if (LISTS && g > thr1)
-              thr1 = list_add_unit<ES>(sh, lst, 1, vd, sd.ebase0 + (u0 + k * kThreads) * EPU, thr1);
+            if (LISTS && g > thr1) thr1 = list_unit<ES>(sh, lst, 1, okey<ES>(val_bits<ES>(g)), u0 + k * kThreads, thr1);
           }
         }
       } else {
