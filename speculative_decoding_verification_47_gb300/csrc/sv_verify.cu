@@ -1327,9 +1327,8 @@ __device__ __forceinline__ int cand_before(const uint2* seg, int n, unsigned lon
 // Exact top-p cut of each row from its candidates: every token whose key
 // exceeds the cluster's list floor theta (sh.ts[r].lth).  Each CTA collects
 // the candidates of its slice from the units its threads recorded, every CTA
-// gathers all of them (at most kUCap per row; each CTA sorts its own first, so
-// a candidate's rank is its place in its own sorted list plus a binary search
-// in each other one), and walks their masses from the top [FS §3.2]: the first candidate
+// gathers all of them (at most kUCap per row), ranks them by (key desc, index
+// asc) and walks their masses from the top [FS §3.2]: the first candidate
 // whose mass ranked before it exceeds top_p * S is the first dropped token.
 // Rows resolved this way get mode 0 and keep the ranked candidates (the kept
 // ones are ranks 0 .. ucut - 1) for the draw.  A row whose candidates overflow
@@ -1339,6 +1338,7 @@ template <int ES>
 __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, unsigned char* dyn, int C,
                                              int nrows, const Expo X) {
   cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
   constexpr int EPU = 16 / ES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint2* own = reinterpret_cast<uint2*>(dyn);
@@ -1355,50 +1355,69 @@ __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, 
     sh.ubelow[tid] = 0;
   }
   __syncthreads();
-  // 1. the elements above the floor in this thread's recorded units
-  for (int r = 0; r < nrows; ++r) {
+  // 1. the elements above the floor in this thread's recorded units (all of
+  //    them are requested before any is examined)
+  uint2 e[2][kListLen];
+  uint4 v[2][kListLen];
+  uint32_t valid[2][kListLen];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
     const uint32_t th = sh.ts[r].lth;
     const RowSlice<ES>& rs = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[r]);
-    const int b0 = rs.ub0(), b1 = rs.ub1();
-#pragma unroll 1
+#pragma unroll
     for (int k = 0; k < kListLen; ++k) {
-      const uint2 e = lst[(r * kListLen + k) * kThreads + tid];
-      if (e.x <= th) break;  // (keys descend; empty slots hold 0)
-      const int u = (int)e.y, eb = rs.ebase0 + u * EPU;
-      uint32_t valid = (1u << EPU) - 1u;
-      const uint4 v = (u >= b0 && u < b1) ? ldg_unit(rs, u) : edge_unit<ES>(rs, eb, &valid);
-#pragma unroll 1
-      for (int j = 0; j < EPU; ++j) {
-        if (!((valid >> j) & 1u)) continue;
-        const uint32_t key = okey<ES>(unit_bits<ES>(v, j));
-        if (key > th) {
-          const uint32_t pos = atomicAdd(&sh.ucnt[r], 1u);
-          if (pos < (uint32_t)kUOwn) own[r * kUOwn + pos] = make_uint2(key, (uint32_t)(eb + j));
-        }
+      e[r][k] = r < nrows ? lst[(r * kListLen + k) * kThreads + tid] : make_uint2(0u, 0u);  // (keys descend; 0 = empty)
+      valid[r][k] = 0u;
+      v[r][k] = make_uint4(0u, 0u, 0u, 0u);
+      const int u = (int)e[r][k].y;
+      if (e[r][k].x > th && u >= rs.ub0() && u < rs.ub1()) {
+        v[r][k] = ldg_unit(rs, u);
+        valid[r][k] = (1u << EPU) - 1u;
       }
     }
   }
-  __syncthreads();
-  // 1b. this CTA's candidates in rank order (through the gather area, which
-  //     is not used before the next cluster barrier)
-  for (int r = 0; r < nrows; ++r) {
-    const int n = (int)min(sh.ucnt[r], (uint32_t)kUOwn);
-    const uint2* o = own + r * kUOwn;
-    for (int i = tid; i < n; i += kThreads) {
-      const uint2 e = o[i];
-      const unsigned long long ce = cand_order(e);
-      int before = 0;
-#pragma unroll 4
-      for (int j = 0; j < n; ++j) before += cand_order(o[j]) > ce ? 1 : 0;
-      all[r * kUCap + before] = e;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t th = sh.ts[r].lth;
+    const RowSlice<ES>& rs = *reinterpret_cast<const RowSlice<ES>*>(&sh.rsl[r]);
+    // which elements qualify (bit 8k + j: element j of unit k), then one
+    // atomic per warp reserves the warp's places
+    uint32_t m[kListLen];
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < kListLen; ++k) {
+      m[k] = 0u;
+      if (e[r][k].x <= th) continue;
+      const int u = (int)e[r][k].y;
+      if (!(u >= rs.ub0() && u < rs.ub1())) v[r][k] = edge_unit<ES>(rs, rs.ebase0 + u * EPU, &valid[r][k]);
+#pragma unroll
+      for (int j = 0; j < EPU; ++j)
+        if (((valid[r][k] >> j) & 1u) && okey<ES>(unit_bits<ES>(v[r][k], j)) > th) m[k] |= 1u << j;
+      cnt += __popc(m[k]);
+    }
+    int inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nb = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += nb;
+    }
+    uint32_t base = 0u;
+    if (lane == 31 && inc) base = atomicAdd(&sh.ucnt[r], (uint32_t)inc);
+    base = __shfl_sync(0xffffffffu, base, 31) + (uint32_t)(inc - cnt);
+#pragma unroll
+    for (int k = 0; k < kListLen; ++k) {
+      const int eb = rs.ebase0 + (int)e[r][k].y * EPU;
+      uint32_t mk = m[k];
+      while (mk) {
+        const int j = __ffs(mk) - 1;
+        mk &= mk - 1u;
+        if (base < (uint32_t)kUOwn)
+          own[r * kUOwn + base] = make_uint2(okey<ES>(unit_bits<ES>(v[r][k], j)), (uint32_t)(eb + j));
+        ++base;
+      }
     }
   }
-  __syncthreads();
-  for (int r = 0; r < nrows; ++r) {
-    const int n = (int)min(sh.ucnt[r], (uint32_t)kUOwn);
-    for (int i = tid; i < n; i += kThreads) own[r * kUOwn + i] = all[r * kUCap + i];
-  }
-  csync(cluster, C);  // every CTA's candidates are complete, in rank order
+  csync(cluster, C);  // every CTA's candidates are complete
   // 2. every CTA's count: offsets, total, overflow (the same in every CTA)
   if (tid < nrows) {
     uint32_t tot = 0u;
@@ -1413,38 +1432,71 @@ __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, 
     sh.uok[tid] = (!ovf && tot <= (uint32_t)kUCap) ? 1 : 0;
   }
   __syncthreads();
-  // 3. gather every CTA's candidates (in rank order of the CTAs)
+  // 3. gather every CTA's candidates (in rank order of the CTAs; padded with
+  //    key 0, which no candidate has, to an even count)
   for (int r = 0; r < nrows; ++r) {
     if (!sh.uok[r]) continue;
-    for (int q = 0; q < C; ++q) {
-      const uint32_t o = sh.uoff[r][q], c = (q + 1 < C ? sh.uoff[r][q + 1] : sh.utot[r]) - o;
-      const uint2* src = remote(cluster, C, own, q) + r * kUOwn;
-      for (uint32_t i = tid; i < c; i += kThreads) all[r * kUCap + o + i] = src[i];
-    }
-  }
-  __syncthreads();
-  // 4. rank: tokens ranked before a candidate have a larger key, or the same
-  //    key at a smaller index; each CTA's segment of the gathered candidates
-  //    is in rank order (the lists are read: their area takes the ranks)
-  for (int r = 0; r < nrows; ++r) {
-    if (!sh.uok[r]) continue;
-    const int n = (int)sh.utot[r];
-    const uint2* a = all + r * kUCap;
-    int q0 = 0;
-    for (int i = tid; i < n; i += kThreads) {
-      while (q0 + 1 < C && (uint32_t)i >= sh.uoff[r][q0 + 1]) ++q0;  // (i only grows)
-      const uint2 e = a[i];
-      const unsigned long long ce = cand_order(e);
-      int before = i - (int)sh.uoff[r][q0];
-      for (int q = 0; q < C; ++q) {
-        if (q == q0) continue;
-        const int o = (int)sh.uoff[r][q], c = (q + 1 < C ? (int)sh.uoff[r][q + 1] : n) - o;
-        before += cand_before(a + o, c, ce);
+    const int n = (int)sh.utot[r], n32 = (n + 1) & ~1;
+    for (int i0 = tid; i0 < n32; i0 += kThreads * 2) {
+      uint2 got[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // two remote loads in flight per thread
+        const int i = i0 + h * kThreads;
+        got[h] = make_uint2(0u, 0u);
+        if (i < n) {
+          int q = 0;
+          while (q + 1 < C && (uint32_t)i >= sh.uoff[r][q + 1]) ++q;
+          got[h] = remote(cluster, C, own, q)[r * kUOwn + (i - (int)sh.uoff[r][q])];
+        }
       }
-      srt[r * kUCap + before] = e;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (i0 + h * kThreads < n32) all[r * kUCap + i0 + h * kThreads] = got[h];
     }
   }
   __syncthreads();
+  // 4. rank: the tokens ranked before a candidate have a larger key, or the
+  //    same key at a smaller index.  Each CTA counts them for the candidates
+  //    it contributed (at most kUOwn), against all of them, and places each
+  //    in every CTA's rank array (the lists are read: their area takes it).
+  {
+    // work: this CTA's candidates of both rows, G adjacent threads each (G
+    // divides 32), each counting over a share of the gathered ones
+    int cr[2], orr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int n = (int)sh.utot[r];
+      orr[r] = r < nrows && sh.uok[r] ? (int)sh.uoff[r][rank] : 0;
+      cr[r] = r < nrows && sh.uok[r] ? (rank + 1 < C ? (int)sh.uoff[r][rank + 1] : n) - orr[r] : 0;
+    }
+    const int items = cr[0] + cr[1];
+    int G = 1;
+    while (G < 8 && items * G * 2 <= kThreads) G <<= 1;
+    for (int base = 0; base < items * G; base += kThreads) {  // (uniform in the CTA)
+      const int wi = base + tid, item = wi / G, part = wi % G;
+      const bool act = item < items;
+      const int r = (act && item >= cr[0]) ? 1 : 0;
+      const int n = (int)sh.utot[r], n2 = (n + 1) >> 1, chunk = (n2 + G - 1) / G;
+      uint2 e_ = make_uint2(0u, 0u);
+      int before = 0;
+      if (act) {
+        e_ = all[r * kUCap + orr[r] + (r ? item - cr[0] : item)];
+        const unsigned long long ce = cand_order(e_);
+        const uint4* a2 = reinterpret_cast<const uint4*>(all + r * kUCap);  // two candidates per load
+        const int j1 = min(n2, (part + 1) * chunk);
+#pragma unroll 4
+        for (int j = part * chunk; j < j1; ++j) {
+          const uint4 f = a2[j];
+          before += cand_order(make_uint2(f.x, f.y)) > ce ? 1 : 0;
+          before += cand_order(make_uint2(f.z, f.w)) > ce ? 1 : 0;  // (padding: key 0, never before)
+        }
+      }
+      for (int o = 1; o < G; o <<= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+      if (act && part == 0 && before < n)  // (always < n: the candidates are distinct)
+        for (int q = 0; q < C; ++q) remote(cluster, C, srt, q)[r * kUCap + before] = e_;
+    }
+  }
+  csync(cluster, C);  // every rank is placed in every CTA
   // 5. masses in rank order: the first candidate whose exclusive prefix
   //    exceeds top_p * S is the first dropped token
   const int x = sh.xtok;
@@ -1523,9 +1575,9 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < 2 && (tid == 0 || two)) {
     const int r = tid;
-    int x = -1;
+    int x = -1;  // the draft token and its logits, as warp 1 fetched them while the rows streamed
     if (i < kb) {
-      x = P.tokens[(size_t)b * P.K + i];
+      x = sh.x;
       if (x < 0 || x >= P.V) x = -1;
     }
     if (r == 0) sh.xtok = x;
@@ -1550,7 +1602,7 @@ __device__ __noinline__ void topp_select(const VerifyParams& P, Shared& sh, unsi
     t.fhi = t.hi;
     t.chi = X.chi;
     sel_set_mode<ES>(t, true);
-    t.kx = x >= 0 ? okey<ES>(rs.bits(x)) : 0u;
+    t.kx = x >= 0 ? okey<ES>(val_bits<ES>(r ? sh.zd_x : sh.zt_x)) : 0u;
     t.kstar = 0u;
     t.cstar = 0;
     t.nk = 0x7fffffff;
@@ -1754,7 +1806,7 @@ __device__ __noinline__ void draw_candidates(const VerifyParams& P, Shared& sh, 
     const uint2 e = srt[i];
     const float a = e2(bits_val<ES>(key_bits<ES>(e.x)), X, -Rt);
     float w = a;
-    if (!p_only) {
+    if (!p_only && e.y < (uint32_t)P.V) {
       const uint32_t bd = ES == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(drow + (size_t)e.y * 2)
                                   : *reinterpret_cast<const uint32_t*>(drow + (size_t)e.y * 4);
       const uint32_t kyd = okey<ES>(bd);
@@ -2331,6 +2383,18 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
   }
   if (!greedy) acc_finish_max<ES>(at);
   if (has_draft) acc_finish_max<ES>(ad);
+  if (lists) {  // the recorded units come back in the selection: have them in L2
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const RowSlice<ES>& rs = r ? sd : st;
+#pragma unroll
+      for (int k = 0; k < kListLen; ++k) {
+        const uint2 e = lst[(r * kListLen + k) * kThreads + tid];
+        if (e.x != 0u && (r == 0 || has_draft) && (int)e.y >= rs.ub0() && (int)e.y < rs.ub1())
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rs.base16 + 16 * (uintptr_t)e.y));
+      }
+    }
+  }
 }
 
 // Combines the row accumulators: lanes, warps, then the CTAs of the cluster
