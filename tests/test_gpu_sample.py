@@ -1,11 +1,13 @@
 """GPU parity of sv_draft_sample (the draft-side sampler) against the float64
 oracle, through the C ABI.  Tokens must match bit for bit, except at a
 position whose inverse-CDF (or top-p cut) margin is below 1e-6.  Such
-disagreements have their own budget (reading R22): at most 2e-3 of the
-sampled tokens of the session.  A draw that lands among the tail tokens of a
-128K vocabulary at T = 1 has margins of 1e-9..1e-7, below the float32
-accuracy of the per-token weights (ex2.approx, 2 ulp), and flips there at a
-measured rate of about 1e-3 of all draws.
+disagreements have their own budget (reading R22): at most 5e-4 of the
+sampled tokens of the session.  Over a 128K vocabulary at T = 1 about 2% of
+draws land within 1e-7 of a CDF boundary; the per-token weights are float32
+exponentials (ex2.approx), whose summed error reaches ~2e-9 of the row mass,
+and a draw flips when its margin is smaller than that.  The headline batch's
+draft rows are drawn under ten uniform seeds (12830 draws, the oracle in a
+spawn pool): 2 flips were measured there (1.6e-4), both at margins ~2e-9.
 
 Cases: the headline batch's draft rows at full size (B=256, K=8, V=128256
 bf16, ragged k_b, per-row temperature), both dtypes with and without top-p,
@@ -27,7 +29,7 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
 
 MARGIN = 1e-6
-RATE = 2e-3
+RATE = 5e-4
 SAMPLE_BUDGET = vh.SAMPLE_BUDGET
 
 
@@ -71,18 +73,52 @@ def _compare(got, flags, logits, dtype, B, K, V, kpr, temp, top_p, unif, mode, r
     return tok
 
 
+def _oracle_rows(args):
+    """Oracle tokens of some sequences of the headline batch (a spawn worker)."""
+    import sys, os
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from speculative_decoding_verification_47_gb300 import workloads as wl_
+    from oracle import sample as osm_
+    seqs, unif = args
+    w = wl_.config_by_name("c2")
+    out = []
+    for b in seqs:
+        tok, mg, _ = osm_.sample_tokens(w.draft[b:b + 1], w.dtype, 1, w.K, w.V, w.k_per_row[b:b + 1],
+                                        w.temperature[b:b + 1], 1.0, unif[b:b + 1], w.mode[b:b + 1])
+        out.append((b, tok[0], mg[0]))
+    return out
+
+
 def test_headline_draft_rows_full_size():
     """B=256, K=8, V=128256 bf16: the draft rows of the headline verify batch,
-    sampled with its ragged k_b and per-row temperatures, all 1283 tokens
-    checked against the oracle."""
+    sampled with its ragged k_b and per-row temperatures under ten uniform
+    seeds; all 12830 tokens checked against the oracle."""
+    import multiprocessing as mp
     w = wl.config_by_name("c2")
-    unif = _uniforms(w.B, w.K, 5150)
-    got, flags = _run(w.draft, w.dtype, w.B, w.K, w.V, w.k_per_row, w.temperature, 1.0, unif, w.mode)
-    assert flags == 0
-    for b in range(w.B):
-        assert np.all(got[b, w.k_per_row[b]:] == -1) and np.all(got[b, :w.k_per_row[b]] >= 0)
-    _compare(got, flags, w.draft, w.dtype, w.B, w.K, w.V, w.k_per_row, w.temperature, 1.0, unif,
-             w.mode)
+    seeds = [5150 + s for s in range(10)]
+    unifs = [_uniforms(w.B, w.K, s) for s in seeds]
+    nproc = max(1, min(16, (mp.cpu_count() or 1)))
+    with mp.get_context("spawn").Pool(nproc) as pool:  # (spawn: this process already uses CUDA)
+        jobs = [pool.map_async(_oracle_rows, [(list(range(i, w.B, nproc)), u) for i in range(nproc)])
+                for u in unifs]
+        results = [sum(j.get(), []) for j in jobs]
+    for unif, res in zip(unifs, results):
+        got, flags = _run(w.draft, w.dtype, w.B, w.K, w.V, w.k_per_row, w.temperature, 1.0, unif, w.mode)
+        assert flags == 0
+        for b in range(w.B):
+            assert np.all(got[b, w.k_per_row[b]:] == -1) and np.all(got[b, :w.k_per_row[b]] >= 0)
+        tok = np.full((w.B, w.K), -1, np.int32)
+        margins = np.full((w.B, w.K), np.inf)
+        for b, t, m in res:
+            tok[b], margins[b] = t, m
+        diff = got != tok
+        low = margins < MARGIN
+        assert not np.any(diff & ~low), np.argwhere(diff & ~low)[:10]
+        SAMPLE_BUDGET["draws"] += int(np.sum(tok >= 0))
+        SAMPLE_BUDGET["disagreements"] += int(np.sum(diff))
+        SAMPLE_BUDGET["low_margin"] += int(np.sum(low & (tok >= 0)))
+        for b, i in np.argwhere(diff):
+            SAMPLE_BUDGET["log"].append((int(b), int(i), float(margins[b, i])))
 
 
 CASES = [
