@@ -64,10 +64,12 @@ COPIES = 3
 # from the ncu captures summarised in profiles/; reported only while the
 # kernel source still has the hash it had when the counters were taken.
 MEASURED_TRAFFIC = {
-    "c2": ("sv_verify.cu", "ada7189908273a41", 491.741952e6 + 8.305664e6),
-    "c3": ("sv_verify.cu", "ada7189908273a41", 479.986688e6 + 64.891904e6),
-    "c4": ("sv_lmhead.cu", "0e369d20a97eb4be", 272.628736e6 + 21.940224e6),
-    "s2": ("sv_verify.cu", "ada7189908273a41", 359.430656e6 + 3.582720e6),
+    "c2": ("sv_verify.cu", "cdd9b791abe775ad", 491.297792e6 + 8.119296e6),
+    "c1": ("sv_verify.cu", "cdd9b791abe775ad", 39.709696e6 + 0.009728e6),
+    "c3": ("sv_verify.cu", "cdd9b791abe775ad", 250.422528e6 + 17.120512e6),
+    "c3t": ("sv_verify.cu", "cdd9b791abe775ad", 250.713088e6 + 16.993024e6),
+    "c4": ("sv_lmhead.cu", "66c9865faaa0c60e", 271.447040e6 + 20.719360e6),
+    "s2": ("sv_verify.cu", "cdd9b791abe775ad", 357.755904e6 + 3.587072e6),
 }
 
 

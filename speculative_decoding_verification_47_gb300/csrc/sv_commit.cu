@@ -75,25 +75,32 @@ __device__ __forceinline__ bool paged_ok(int L, int n, int k, int max_pages, int
   return k >= 0 && (long long)L + k <= (long long)max_pages * P && n >= 0 && n <= k && L >= 0;
 }
 
+// One warp per sequence: the lanes read its block-table row together (lane
+// q holds entries q, q + 32, ...), so the row is read coalesced and counted by
+// ballots.
 __global__ void paged_count_kernel(const int32_t* __restrict__ seq_lens,
                                    const int32_t* __restrict__ n_accepted,
                                    const int32_t* __restrict__ k_per_row,
                                    const int32_t* __restrict__ table, int max_pages, int P, int B,
                                    const int32_t* __restrict__ free_top, uint32_t* ws) {
   pdl_wait();  // the launch may overlap the kernel that wrote n_accepted
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b == 0) ws[2] = (uint32_t)*free_top;
-  if (b >= B) return;
+  const int lane = threadIdx.x & 31;
+  const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (b == 0 && lane == 0) ws[2] = (uint32_t)*free_top;
+  if (b >= B) return;  // (whole warps)
   const int L = seq_lens[b], n = n_accepted[b], k = k_per_row[b];
   if (!paged_ok(L, n, k, max_pages, P)) {
-    atomicOr(ws, SV_FLAG_BAD_N);
+    if (lane == 0) atomicOr(ws, SV_FLAG_BAD_N);
     return;
   }
   const int keep = (L + n + P - 1) / P;
   const int32_t* row = table + (size_t)b * max_pages;
   uint32_t c = 0;
-  for (int j = keep; j < max_pages; ++j) c += row[j] >= 0 ? 1u : 0u;
-  if (c) atomicAdd(ws + 1, c);
+  for (int j0 = keep; j0 < max_pages; j0 += 32) {
+    const int j = j0 + lane;
+    c += __popc(__ballot_sync(0xffffffffu, j < max_pages && row[j] >= 0));
+  }
+  if (lane == 0 && c) atomicAdd(ws + 1, c);
 }
 
 __global__ void paged_apply_kernel(int32_t* __restrict__ seq_lens,
@@ -101,24 +108,34 @@ __global__ void paged_apply_kernel(int32_t* __restrict__ seq_lens,
                                    const int32_t* __restrict__ k_per_row, int32_t* __restrict__ table,
                                    int max_pages, int P, int B, int32_t* __restrict__ free_pages,
                                    int32_t* __restrict__ free_top, int free_capacity, uint32_t* ws) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int b = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if ((long long)ws[2] + ws[1] > (long long)free_capacity) {  // (the same test in every thread)
-    if (b == 0) atomicOr(ws, SV_FLAG_CAPACITY);
+    if (b == 0 && lane == 0) atomicOr(ws, SV_FLAG_CAPACITY);
     return;
   }
-  if (b >= B) return;
+  if (b >= B) return;  // (whole warps)
   const int L = seq_lens[b], n = n_accepted[b], k = k_per_row[b];
   if (!paged_ok(L, n, k, max_pages, P)) return;
   const int keep = (L + n + P - 1) / P;
   int32_t* row = table + (size_t)b * max_pages;
   int c = 0;
-  for (int j = keep; j < max_pages; ++j) c += row[j] >= 0 ? 1 : 0;
-  int pos = c ? atomicAdd(free_top, c) : 0;
-  for (int j = keep; j < max_pages; ++j) {
-    if (row[j] >= 0) free_pages[pos++] = row[j];
-    row[j] = -1;
+  for (int j0 = keep; j0 < max_pages; j0 += 32) {
+    const int j = j0 + lane;
+    c += __popc(__ballot_sync(0xffffffffu, j < max_pages && row[j] >= 0));
   }
-  seq_lens[b] = L + n;
+  int pos = 0;
+  if (lane == 0 && c) pos = atomicAdd(free_top, c);  // this sequence's places on the stack
+  pos = __shfl_sync(0xffffffffu, pos, 0);
+  for (int j0 = keep; j0 < max_pages; j0 += 32) {
+    const int j = j0 + lane;
+    const int32_t id = j < max_pages ? row[j] : -1;
+    const unsigned m = __ballot_sync(0xffffffffu, id >= 0);
+    if (id >= 0) free_pages[pos + __popc(m & ((1u << lane) - 1u))] = id;
+    if (j < max_pages) row[j] = -1;
+    pos += __popc(m);
+  }
+  if (lane == 0) seq_lens[b] = L + n;
 }
 
 int paged_commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int32_t* k_per_row,
@@ -127,7 +144,7 @@ int paged_commit_launch(int32_t* seq_lens, const int32_t* n_accepted, const int3
                         std::string* err) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws + 1, 0, sizeof(uint32_t), st);  // the release count
-  const int threads = 256, blocks = (B + threads - 1) / threads;
+  const int threads = 256, blocks = (int)(((long long)B * 32 + threads - 1) / threads);  // a warp per sequence
   if (e == cudaSuccess) {
     paged_count_kernel<<<blocks, threads, 0, st>>>(seq_lens, n_accepted, k_per_row, block_table,
                                                   max_pages, page_size, B, free_top, ws);

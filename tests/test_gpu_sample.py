@@ -29,7 +29,7 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
 
 MARGIN = 1e-6
-RATE = 5e-4
+RATE = vh.SAMPLE_RATE
 SAMPLE_BUDGET = vh.SAMPLE_BUDGET
 
 

@@ -39,7 +39,8 @@ PROB_RTOL = 1e-5
 BUDGET = {"decisions": 0, "disagreements": 0, "low_margin": 0, "per_call": {}}
 BUDGET_LOG = []  # (where, sequence, position, kinds, margin) of each disagreement
 SAMPLE_BUDGET = {"draws": 0, "disagreements": 0, "low_margin": 0, "log": []}
-RATE = 1e-4  # allowed share of excused (low-margin) disagreements
+RATE = 1e-4  # allowed share of excused (low-margin) disagreements of verify decisions
+SAMPLE_RATE = 5e-4  # ... of draft-sampler draws (every one of them a draw: reading R22)
 
 
 def record_call(name, decisions, disagreements, low):
@@ -64,7 +65,7 @@ def budget_lines():
     n, x, lo = SAMPLE_BUDGET["draws"], SAMPLE_BUDGET["disagreements"], SAMPLE_BUDGET["low_margin"]
     if n:
         out.append(f"sampler draws={n} disagreements={x} low-margin draws={lo} "
-                   f"rate={x / n:.2e} (limit {RATE:g})")
+                   f"rate={x / n:.2e} (limit {SAMPLE_RATE:g})")
     return out
 
 
