@@ -163,6 +163,19 @@ __device__ __forceinline__ float unit_max(const uint4& v) {
   }
 }
 
+// largest non-NaN logit of a unit (-inf if none)
+template <int ES>
+__device__ __forceinline__ float unit_max_num(const uint4& v) {
+  if (ES == 2) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+    __nv_bfloat162 m2 = __hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3]));
+    return fmaxf(__low2float(m2), __high2float(m2));
+  } else {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
 // c = log2(e)/T as chi + clo with chi <= c (so clo > 0), from float operations
 // only: q1 = hi/T, then the quotient of the exact remainder.  exp((z - m)/T)
 // is then 2^(z*chi + z*clo - m*c), and no rounded reciprocal of T enters it.
@@ -288,10 +301,15 @@ __device__ __forceinline__ void acc_raise(RowAcc& a, float Rn) {
   a.R = Rn;
 }
 
-// A unit whose sum exceeds this has an element more than 2^17 above the
-// reference: the reference is raised (rare after the first unit, which
-// always overflows from kRnone) and the unit recomputed.
-constexpr float kRaiseAbove = 1048576.f;
+// A unit of 8 or fewer weights whose sum exceeds 8 has an element above the
+// reference (2^(z*c - R) > 1): the reference is raised to ceil(max*c) and the
+// unit recomputed.  So R stays within 3 of the thread's largest z*c, and the
+// heaviest weights are formed from arguments in [-1, 3]: the rounding of
+// z*c - R to float grows with its magnitude, and a reference lagging the
+// maximum by ~20 made those weights ~10x less precise, which moved draws that
+// fall within ~1e-8 of a CDF boundary.  (A raise happens once per new
+// running maximum of the thread; the first unit always raises from kRnone.)
+constexpr float kRaiseAbove = 8.f;
 
 __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -352,7 +370,8 @@ __device__ __forceinline__ float unit_sumexp(const uint4& v, const Expo& x, floa
 // lists compare; without, it returns 0 and forms the max only when the
 // reference exponent must rise.
 template <int ES, bool MAX = false>
-__device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
+__device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const Expo& x,
+                                              float* sum_out = nullptr) {
   uint32_t um = 0;
   if (ES == 2) {
     um = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
@@ -372,6 +391,7 @@ __device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const E
     }
   }
   a.pend += us;
+  if (sum_out) *sum_out = us;  // (relative to the reference after any rise)
   return g;
 }
 
@@ -681,6 +701,8 @@ constexpr int kSelSmemBytes = kHistBytes + kStageBytes;
 constexpr int kListOff = ((kSelSmemBytes > kRingBytes ? kSelSmemBytes : kRingBytes) + 255) / 256 * 256;
 constexpr int kListBytes = 2 * kListLen * kThreads * 8;
 constexpr int kToppSmemBytes = kListOff + kListBytes;
+// the draft sampler without top-p: a ring of the target slots, then the unit sums
+constexpr int kSampleSumsOff = kRingBytes / 2;
 // candidates above the cluster's floor (top-p instances): this CTA's at the
 // start of the dynamic area, the cluster's gathered after them, and the
 // cluster's in rank order over the unit lists once those are read
@@ -1897,7 +1919,7 @@ __device__ __noinline__ void draw_candidates(const VerifyParams& P, Shared& sh, 
 // owner of u*total, the round, the unit and the element.  The token is
 // stored for the sequence's outputs.
 // ---------------------------------------------------------------------------
-template <int ES, bool TOPP, bool SAMPLE = false>
+template <int ES, bool TOPP, bool SAMPLE = false, bool VR = false>
 __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals, int C, int rank,
                                     int b, int kb,
                                     float T, int j, float uK, int e0, int e1, float Rt, float Rd,
@@ -1956,7 +1978,8 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   for (int pass = 0; pass < 2; ++pass) {
     if (pass) cluster.sync();  // every CTA has read the first pass's slots
     pr.vec = W.p_only || same_phase;
-    for (int u0 = tid; u0 < rounds * kThreads; u0 += kThreads * kLoadsInFlight) {
+    // (VR: the unit sums of p alone are in vals already, from the row pass)
+    for (int u0 = tid; u0 < (VR && pass == 0 ? 0 : rounds * kThreads); u0 += kThreads * kLoadsInFlight) {
       uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
 #pragma unroll
       for (int k = 0; k < kLoadsInFlight; ++k) {
@@ -2253,19 +2276,71 @@ __device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, in
   }
 }
 
+// The unit sums this thread stored before unit u, times p (a rise of its
+// reference exponent).
+__device__ __noinline__ void uv_rescale(float* uv, int u, float p) {
+  for (int v = u % kThreads; v < u; v += kThreads) uv[v] *= p;
+}
+
+// Sum of 2^(z*c - R) over unit u of a slice (a full unit, or the valid
+// elements of a partial one).
+template <int ES>
+__device__ __forceinline__ float unit_or_edge_sum(const RowSlice<ES>& rs, int u, int ub0, int ub1,
+                                                  const uint4& v, const Expo& x, float R) {
+  if (u >= ub0 && u < ub1) return unit_sumexp<ES>(v, x, R);
+  constexpr int EPU = 16 / ES;
+  const int eb = rs.ebase0 + u * EPU;
+  float s_ = 0.f;
+  for (int j = 0; j < EPU; ++j) {
+    const int e = eb + j;
+    if (e >= rs.e0 && e < rs.e1) s_ += e2(rs.elem(e), x, -R);
+  }
+  return s_;
+}
+
+// Seeds the reference exponent of a sampled row, before anything is summed,
+// from the largest logit among the warp's first-step units (kLoadsInFlight
+// aligned units per lane, in this lane's slots).  Each lane raises its own
+// reference whenever one of its units goes above it; started from kRnone, a
+// lane would raise at most of its first units (a new running maximum is
+// frequent early), and a warp runs the raise path whenever any of its lanes
+// takes it.  From the warp's maximum over 64 units, a later unit rises above
+// the reference rarely.  Every lane of the warp must call this.
+template <int ES>
+__device__ __forceinline__ void seed_reference(RowAcc& a, const uint4* slot, int u0, int ub0, int ub1,
+                                               const Expo& x) {
+  float g = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kLoadsInFlight; ++k) {
+    const int u = u0 + k * kThreads;
+    if (u >= ub0 && u < ub1) g = fmaxf(g, unit_max_num<ES>(slot[k * kThreads]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, o));
+  const float gc = g * x.chi;
+  if (gc > -INFINITY && gc < INFINITY) a.R = ceilf(gc);  // (else kRnone: the units raise it)
+}
+
 // Streams this CTA's slices of both rows through the per-thread cp.async ring
 // and reduces them into at / ad (row pass of a1 and a3).  With MOOT, every
 // other step each thread looks at the sequence word and stops reading once
 // an earlier position of the sequence is rejected (it then sets sh.moot).
 // With LISTS (top-p instances, sampled rows), each thread also keeps its
 // candidate lists in lst, and sh.lth[r] ends as the CTA's floor of row r.
-template <int ES, bool MOOT, bool LISTS = false>
+// With UVALS (the draft sampler: one row, no draft), the ring holds the
+// target slots only and each unit's sum 2^(z*c - R) is kept in uv[u]; a rise
+// of this thread's reference R rescales the sums it stored before.
+template <int ES, bool MOOT, bool LISTS = false, bool UVALS = false>
 __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh, float* vals,
                                               const RowSlice<ES>& st, const RowSlice<ES>& sd,
                                               bool has_draft, bool greedy, bool skip, const Expo& X,
                                               int b, int i, RowAcc& at, RowAcc& ad,
-                                              uint2* lst = nullptr) {
+                                              uint2* lst = nullptr, float* uv = nullptr) {
   const int tid = threadIdx.x;
+  if (UVALS) {  // every unit of the rounds starts at 0 (the slice's tail units stay 0)
+    const int rounds = (st.n_units + kThreads - 1) / kThreads;
+    for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] = 0.f;
+  }
   const bool lists = LISTS && !greedy;
   // list admission thresholds (values); the draft row keeps no list when
   // the call leaves the draft untruncated
@@ -2280,6 +2355,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     // k < L target, k >= L draft) and reduces the oldest step from there.
     constexpr int L = kLoadsInFlight;
     constexpr int kStep = kThreads * L;
+    constexpr int kStage = (UVALS ? 1 : 2) * L * kThreads;  // slots per stage (UVALS: target only)
     uint4* ring = reinterpret_cast<uint4*>(vals);
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
@@ -2292,7 +2368,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     auto interior = [&](int u0) { return u0 >= in0 && u0 + (L - 1) * kThreads < in1; };
     auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
       const int u0 = tid + n * kStep;
-      uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      uint4* slot = ring + (size_t)(n % kRingStages) * kStage + tid;
       if (interior(u0)) {
         const char* pt = gt + (size_t)n * kStep * 16;
 #pragma unroll
@@ -2318,6 +2394,10 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     if (!skip) {
 #pragma unroll
       for (int n = 0; n < kRingStages; ++n) issue(n);
+      // (every lane is here: the references start from the warp's first step)
+      cp_async_wait<kRingStages - 1>();
+      if (!greedy) seed_reference<ES>(at, ring + tid, tid, tb0, tb1, X);
+      if (has_draft) seed_reference<ES>(ad, ring + L * kThreads + tid, tid, db0, db1, X);
     }
     // the sequence word, read two steps before it is looked at (no stall)
     unsigned long long wseen = (MOOT && i > 0 && !skip) ? __ldcg(P.words + b) : 0ull;
@@ -2340,7 +2420,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
       }
       cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
       const int u0 = tid + n * kStep;
-      const uint4* slot = ring + (size_t)(n % kRingStages) * 2 * L * kThreads + tid;
+      const uint4* slot = ring + (size_t)(n % kRingStages) * kStage + tid;
       // units are read from the slots one at a time (the ring, not registers,
       // holds the step)
       if (interior(u0)) {
@@ -2350,6 +2430,12 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
           const uint4 vt = slot[k * kThreads];
           if (greedy) {
             greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
+          } else if (UVALS) {
+            const float R0 = at.R;
+            float us;
+            sampled_unit<ES>(at, vt, X, &us);
+            if (at.R != R0) uv_rescale(uv, u0 + k * kThreads, pow2i(R0 - at.R));  // (rare)
+            uv[u0 + k * kThreads] = us;
           } else {
             const float g = sampled_unit<ES, LISTS>(at, vt, X);
             if (LISTS && g > thr0) thr0 = list_unit<ES>(sh, lst, 0, okey<ES>(val_bits<ES>(g)), u0 + k * kThreads, thr0);
@@ -2368,7 +2454,12 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
         for (int k = 0; k < L; ++k) {
           const int u = u0 + k * kThreads;
           const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
+          const float R0 = at.R;
           row_unit_v<ES, LISTS>(at, st, u, tb0, tb1, vt, greedy, X, &sh, lst, 0, &thr0);
+          if (UVALS && !greedy && u < st.n_units) {  // the unit's sum against the reference it ended with
+            if (at.R != R0) uv_rescale(uv, u, pow2i(R0 - at.R));
+            uv[u] = unit_or_edge_sum<ES>(st, u, tb0, tb1, vt, X, at.R);
+          }
           if (has_draft) {
             const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
             row_unit_v<ES, LISTS>(ad, sd, u, db0, db1, vd, false, X, &sh, lst, 1, &thr1);
@@ -2680,9 +2771,23 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
   if (tid == 32) sh.uK = greedy ? 0.f : P.unif[(size_t)b * P.K + i];
   __syncthreads();
   RowAcc at = acc_init(), ad = acc_init();
-  stream_slices<ES, false, TOPP>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
-                                 reinterpret_cast<uint2*>(reinterpret_cast<char*>(vals) + kListOff));
+  // without top-p the row pass keeps its unit sums for the draw (after a
+  // ring of the target slots only)
+  float* uv = reinterpret_cast<float*>(reinterpret_cast<char*>(vals) + kSampleSumsOff);
+  if (TOPP)
+    stream_slices<ES, false, TOPP>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
+                                   reinterpret_cast<uint2*>(reinterpret_cast<char*>(vals) + kListOff));
+  else
+    stream_slices<ES, false, false, true>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
+                                          nullptr, uv);
   combine_rows(sh, cluster, C, rank, at, ad, greedy, false, false);  // (never moot here)
+  if (!TOPP && !greedy) {  // this thread's unit sums, against the row's reference
+    const float f = at.R > kRnone ? pow2i(at.R - sh.row_t.R) : 0.f;
+    const int rounds = (st.n_units + kThreads - 1) / kThreads;
+    if (f != 1.f)
+      for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] *= f;
+    __syncthreads();
+  }
   const RowAcc row_t = sh.row_t;
   const bool bad = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
                    (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
@@ -2713,7 +2818,7 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
     cntt = sh.ts[0].cstar;
   }
   // j = k_b = i: the draw's weights are p' alone, as for a bonus token
-  finish<ES, TOPP, true>(P, sh, vals, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
+  finish<ES, TOPP, true, !TOPP>(P, sh, TOPP ? vals : uv, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
                          S_t, kt, nkt, cntt, 0u, 0x7fffffff, 0);
 }
 
@@ -2907,6 +3012,7 @@ int sample_launch(const SampleLaunch& L, std::string* err) {
   size_t smem = (size_t)rounds * kThreads * sizeof(float);
   if (smem < (size_t)kRingBytes) smem = kRingBytes;
   if (topp && smem < (size_t)kToppSmemBytes) smem = kToppSmemBytes;
+  if (!topp) smem = (size_t)kSampleSumsOff + (size_t)rounds * kThreads * sizeof(float);  // ring + sums
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   if (!g_configured_sample[gi]) {
