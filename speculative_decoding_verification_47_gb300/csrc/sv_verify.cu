@@ -48,6 +48,8 @@ constexpr int kCmax = 16;
 static_assert((kWarps & (kWarps - 1)) == 0 && kCmax <= 16, "butterfly widths are powers of two up to 16");
 constexpr int kLoadsInFlight = 2;                  // 16-byte units per row per thread per step
 constexpr int kRingStages = 2;                     // steps of units in flight ahead of the one reduced
+constexpr int kSampleRingStages = 2;               // the draft sampler's (one row): more stages cost
+                                                   // a CTA per SM, which is slower
 constexpr int kRingBytes = kRingStages * 2 * kLoadsInFlight * kThreads * 16;  // 32 KB
 constexpr int kMaxRounds = 64;                     // slice <= 64 * 256 units = 256 KB of a row
 constexpr int kWordBits = 21;                      // positions per field of the sequence word
@@ -433,6 +435,22 @@ __device__ __forceinline__ void greedy_elem(RowAcc& a, float z, int e) {
 // (cp.async: the bytes in flight hold no registers).  Units outside the
 // aligned body [ub0, ub1) are read element by element.
 // ---------------------------------------------------------------------------
+// Brings [a, a + bytes) of global memory into L2 with the bulk-copy engine
+// (a and bytes multiples of 16; nothing is written to shared memory).
+__device__ __forceinline__ void l2_prefetch_bulk(uintptr_t a, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(bytes) : "memory");
+}
+
+// The aligned body of a slice back into L2, 16 KB per lane of the calling
+// warp (every lane calls).
+template <int ES>
+__device__ __forceinline__ void l2_prefetch_slice(const RowSlice<ES>& rs, int lane) {
+  constexpr uint32_t kPiece = 16384;
+  const uintptr_t n = rs.a1 - rs.a0;  // (a multiple of 16)
+  for (uintptr_t o = (uintptr_t)lane * kPiece; o < n; o += 32 * (uintptr_t)kPiece)
+    l2_prefetch_bulk(rs.a0 + o, (uint32_t)(n - o < kPiece ? n - o : kPiece));
+}
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
@@ -702,7 +720,7 @@ constexpr int kListOff = ((kSelSmemBytes > kRingBytes ? kSelSmemBytes : kRingByt
 constexpr int kListBytes = 2 * kListLen * kThreads * 8;
 constexpr int kToppSmemBytes = kListOff + kListBytes;
 // the draft sampler without top-p: a ring of the target slots, then the unit sums
-constexpr int kSampleSumsOff = kRingBytes / 2;
+constexpr int kSampleSumsOff = kSampleRingStages * kLoadsInFlight * kThreads * 16;
 // candidates above the cluster's floor (top-p instances): this CTA's at the
 // start of the dynamic area, the cluster's gathered after them, and the
 // cluster's in rank order over the unit lists once those are read
@@ -1919,7 +1937,7 @@ __device__ __noinline__ void draw_candidates(const VerifyParams& P, Shared& sh, 
 // owner of u*total, the round, the unit and the element.  The token is
 // stored for the sequence's outputs.
 // ---------------------------------------------------------------------------
-template <int ES, bool TOPP, bool SAMPLE = false, bool VR = false>
+template <int ES, bool TOPP, bool SAMPLE = false>
 __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* vals, int C, int rank,
                                     int b, int kb,
                                     float T, int j, float uK, int e0, int e1, float Rt, float Rd,
@@ -1978,8 +1996,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
   for (int pass = 0; pass < 2; ++pass) {
     if (pass) cluster.sync();  // every CTA has read the first pass's slots
     pr.vec = W.p_only || same_phase;
-    // (VR: the unit sums of p alone are in vals already, from the row pass)
-    for (int u0 = tid; u0 < (VR && pass == 0 ? 0 : rounds * kThreads); u0 += kThreads * kLoadsInFlight) {
+    for (int u0 = tid; u0 < rounds * kThreads; u0 += kThreads * kLoadsInFlight) {
       uint4 vt[kLoadsInFlight], vd[kLoadsInFlight];
 #pragma unroll
       for (int k = 0; k < kLoadsInFlight; ++k) {
@@ -2350,12 +2367,13 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     for (int k = 0; k < 2 * kListLen; ++k) lst[k * kThreads + tid] = make_uint2(0u, 0u);
   }
   {
-    // Each thread keeps kRingStages steps of its units in flight in its own
+    // Each thread keeps NS steps of its units in flight in its own
     // shared-memory slots (slot k of stage s: ring[(s*2L + k)*kThreads + tid],
     // k < L target, k >= L draft) and reduces the oldest step from there.
     constexpr int L = kLoadsInFlight;
     constexpr int kStep = kThreads * L;
     constexpr int kStage = (UVALS ? 1 : 2) * L * kThreads;  // slots per stage (UVALS: target only)
+    constexpr int NS = UVALS ? kSampleRingStages : kRingStages;  // stages
     uint4* ring = reinterpret_cast<uint4*>(vals);
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
@@ -2366,9 +2384,9 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     const char* gt = reinterpret_cast<const char*>(st.base16) + 16 * (size_t)tid;
     const char* gd = reinterpret_cast<const char*>(sd.base16) + 16 * (size_t)tid;
     auto interior = [&](int u0) { return u0 >= in0 && u0 + (L - 1) * kThreads < in1; };
-    auto issue = [&](int n) {  // copies of step n into stage n % kRingStages (one group)
+    auto issue = [&](int n) {  // copies of step n into stage n % NS (one group)
       const int u0 = tid + n * kStep;
-      uint4* slot = ring + (size_t)(n % kRingStages) * kStage + tid;
+      uint4* slot = ring + (size_t)(n % NS) * kStage + tid;
       if (interior(u0)) {
         const char* pt = gt + (size_t)n * kStep * 16;
 #pragma unroll
@@ -2393,9 +2411,9 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     };
     if (!skip) {
 #pragma unroll
-      for (int n = 0; n < kRingStages; ++n) issue(n);
+      for (int n = 0; n < NS; ++n) issue(n);
       // (every lane is here: the references start from the warp's first step)
-      cp_async_wait<kRingStages - 1>();
+      cp_async_wait<NS - 1>();
       if (!greedy) seed_reference<ES>(at, ring + tid, tid, tb0, tb1, X);
       if (has_draft) seed_reference<ES>(ad, ring + L * kThreads + tid, tid, db0, db1, X);
     }
@@ -2418,9 +2436,9 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
         }
         wseen = __ldcg(P.words + b);
       }
-      cp_async_wait<kRingStages - 1>();  // this thread's step n has landed
+      cp_async_wait<NS - 1>();  // this thread's step n has landed
       const int u0 = tid + n * kStep;
-      const uint4* slot = ring + (size_t)(n % kRingStages) * kStage + tid;
+      const uint4* slot = ring + (size_t)(n % NS) * kStage + tid;
       // units are read from the slots one at a time (the ring, not registers,
       // holds the step)
       if (interior(u0)) {
@@ -2468,7 +2486,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
       }
       if (!greedy) acc_flush(at);
       if (has_draft) acc_flush(ad);
-      issue(n + kRingStages);  // (the slots were consumed above)
+      issue(n + NS);  // (the slots were consumed above)
     }
     cp_async_wait_all();
   }
@@ -2699,6 +2717,15 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
   if (!cand) return;  // (uniform in the cluster: no distributed access follows)
   csync(cluster, C);
   if (!sh.fin) return;
+  // The draw reads this CTA's slices again (both rows, or the target's for a
+  // bonus).  Streamed a while ago, they have mostly left L2; a bulk prefetch
+  // of the whole slice brings them back at once, where the draw's own loads
+  // would take one DRAM round trip per step.  (Top-p draws from the kept
+  // candidates read no row again.)
+  if (!TOPP && tid < 32) {
+    l2_prefetch_slice<ES>(st, tid);
+    if (i < kb) l2_prefetch_slice<ES>(sd, tid);
+  }
 
   // ======================= this item's draw =======================
   const float uK = sh.uK;
@@ -2719,6 +2746,148 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
   }
   finish<ES, TOPP>(P, sh, vals, C, rank, b, kb, T, i, uK, e0, e1, sh.row_t.R, sh.row_d.R, S_t, S_d,
                    kt, nkt, cntt, kd, nkd, cntd);
+}
+
+// ---------------------------------------------------------------------------
+// The draft sampler's draw without top-p (weights p' alone).  The row pass
+// left each thread's unit sums 2^(z*c - R) in uv (R: that thread's own
+// reference), and the combine left every CTA's slice accumulator in sh.g_t.
+// Every CTA finds, from the same values, the slice that holds u*S; the
+// others return at once (nothing distributed follows the combine).  The
+// owner brings its sums to the row's reference Rrow, then finds the round
+// (a warp scan over the round totals, 32 rounds at a time), the unit (a
+// block scan of the round) and the element (that unit read again, its
+// weights 2^(z*c - Rrow) in index order).  The token goes to *out.
+// ---------------------------------------------------------------------------
+// (the slice comes as scalars: row, [e0, e1), n_units, ebase0 as in RowSlice;
+// a struct passed to a call that is not inlined would go through local memory)
+template <int ES>
+__device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank, const char* row, int e0,
+                                         int e1, int n_units, int ebase0, float chi, float clo, float Rthr,
+                                         float Rrow, float uK, int32_t* out) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Expo X{chi, clo};
+  if (warp == 0) {  // the owner of u*S among the slices, in rank order
+    DF v{0.f, 0.f};
+    if (lane < C) {
+      const RowAcc g = C > 1 ? sh.g_t[lane] : sh.row_t;
+      if (g.R > kRnone) {
+        const float p = pow2i(g.R - Rrow);
+        v = DF{g.s.hi * p, g.s.lo * p};
+      }
+    }
+    const DF inc = df_warp_scan(v, lane);
+    const DF tgt = df_mul_f(df_shfl(inc, 31), uK);
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < C && df_pos(v) && df_gt(inc, tgt));
+    const unsigned pos = __ballot_sync(0xffffffffu, lane < C && df_pos(v));
+    const int owner = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const DF v_own = df_shfl(v, owner), inc_own = df_shfl(inc, owner);
+    // past the end by rounding: the last positive slice, just inside its end
+    const DF rem = hit ? df_sub(tgt, df_sub(inc_own, v_own)) : df_mul_f(v_own, 0.999999f);
+    if (lane == 0) {
+      sh.owner = owner;
+      sh.rem = rem;
+    }
+  }
+  __syncthreads();
+  if (sh.owner != rank) return;  // (uniform inside this CTA)
+  const int rounds = (n_units + kThreads - 1) / kThreads;
+  {  // this thread's sums against the row's reference
+    const float f = Rthr > kRnone ? pow2i(Rthr - Rrow) : 0.f;
+    if (f != 1.f)
+      for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] *= f;
+  }
+  __syncthreads();
+  for (int r = warp; r < rounds; r += kWarps) {
+    DF a{0.f, 0.f};
+    for (int t = lane; t < kThreads; t += 32) df_acc(a, uv[r * kThreads + t]);
+    a = df_warp_sum(a);
+    if (lane == 0) sh.rtot[r] = a;
+  }
+  __syncthreads();
+  if (warp == 0) {  // the round: 32 round totals per warp scan
+    DF rem = sh.rem;
+    int rsel = -1, rlast = -1;
+    DF vlast{0.f, 0.f};
+    for (int r0 = 0; r0 < rounds && rsel < 0; r0 += 32) {
+      const int r = r0 + lane;
+      const DF v = r < rounds ? sh.rtot[r] : DF{0.f, 0.f};
+      const DF inc = df_warp_scan(v, lane);
+      const unsigned hit = __ballot_sync(0xffffffffu, r < rounds && df_pos(v) && df_gt(inc, rem));
+      const unsigned pos = __ballot_sync(0xffffffffu, r < rounds && df_pos(v));
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        rsel = r0 + l;
+        rem = df_sub(rem, df_sub(df_shfl(inc, l), df_shfl(v, l)));
+      } else {
+        if (pos) {
+          const int l = 31 - __clz(pos);
+          rlast = r0 + l;
+          vlast = df_shfl(v, l);
+        }
+        rem = df_sub(rem, df_shfl(inc, 31));
+      }
+    }
+    if (rsel < 0) {  // past the end by rounding: the last positive round
+      rsel = rlast < 0 ? 0 : rlast;
+      rem = df_mul_f(vlast, 0.999999f);
+    }
+    if (lane == 0) {
+      sh.rsel = rsel;
+      sh.rem = rem;
+    }
+  }
+  __syncthreads();
+  const int rsel = sh.rsel;
+  const DF rem = sh.rem;
+  // block-wide inclusive prefix of round rsel's unit sums (thread order)
+  const float v = uv[rsel * kThreads + tid];
+  const DF wi = df_warp_scan(DF{v, 0.f}, lane);
+  if (lane == 31) sh.scan[warp] = wi;
+  __syncthreads();
+  DF inc = wi;
+  for (int w = 0; w < warp; ++w) inc = df_add(sh.scan[w], inc);
+  int cand = (v > 0.f && df_gt(inc, rem)) ? tid : 0x7fffffff;
+  int lastpos = v > 0.f ? tid : -1;
+  cand = warp_min(cand);
+  lastpos = -warp_min(-lastpos);
+  __syncthreads();
+  if (lane == 0) {
+    sh.r_i[warp] = cand;
+    sh.scan[warp].hi = __int_as_float(lastpos);
+  }
+  __syncthreads();
+  int tsel = 0x7fffffff, tlast = -1;
+  for (int w = 0; w < kWarps; ++w) {
+    tsel = min(tsel, sh.r_i[w]);
+    tlast = max(tlast, __float_as_int(sh.scan[w].hi));
+  }
+  const bool past_end = tsel == 0x7fffffff;  // rounding: the last positive unit
+  if (past_end) tsel = tlast < 0 ? 0 : tlast;
+  if (tid != tsel) return;
+  constexpr int EPU = 16 / ES;
+  const int u = rsel * kThreads + tid;
+  DF cum = past_end ? DF{0.f, 0.f} : df_sub(inc, DF{v, 0.f});
+  int y = -1, ylast = -1;
+  const int eb = ebase0 + u * EPU;
+  for (int q = 0; q < EPU; ++q) {
+    const int e = eb + q;
+    if (e < e0 || e >= e1) continue;
+    const float z = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2))
+                            : *reinterpret_cast<const float*>(row + (size_t)e * 4);
+    const float wv = e2(z, X, -Rrow);
+    if (wv > 0.f) ylast = e;
+    cum = df_add(cum, DF{wv, 0.f});
+    if (!past_end && wv > 0.f && df_gt(cum, rem)) {
+      y = e;
+      break;
+    }
+  }
+  if (y < 0) y = ylast;
+  // (a unit whose rescaled sum is positive but whose weights against Rrow all
+  // flush to zero holds mass below 2^-126 of the row: its first element)
+  if (y < 0) y = max(eb, e0);
+  *out = y;
 }
 
 // ---------------------------------------------------------------------------
@@ -2781,13 +2950,6 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
     stream_slices<ES, false, false, true>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
                                           nullptr, uv);
   combine_rows(sh, cluster, C, rank, at, ad, greedy, false, false);  // (never moot here)
-  if (!TOPP && !greedy) {  // this thread's unit sums, against the row's reference
-    const float f = at.R > kRnone ? pow2i(at.R - sh.row_t.R) : 0.f;
-    const int rounds = (st.n_units + kThreads - 1) / kThreads;
-    if (f != 1.f)
-      for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] *= f;
-    __syncthreads();
-  }
   const RowAcc row_t = sh.row_t;
   const bool bad = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
                    (!greedy && !(row_t.R > kRnone && row_t.R < INFINITY));
@@ -2799,6 +2961,11 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
       if (bad) atomicOr(P.flags, SV_FLAG_NONFINITE);
       else if (!greedy) atomicOr(P.flags, SV_FLAG_BAD_UNIFORM);
     }
+    return;
+  }
+  if (!TOPP) {  // the unit sums are in uv: no row is read again
+    sample_draw<ES>(sh, uv, C, rank, st.row, st.e0, st.e1, st.n_units, st.ebase0, X.chi, X.clo, at.R,
+                    row_t.R, u, out);
     return;
   }
   DF S_t = row_t.s;
@@ -2818,12 +2985,18 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
     cntt = sh.ts[0].cstar;
   }
   // j = k_b = i: the draw's weights are p' alone, as for a bonus token
-  finish<ES, TOPP, true, !TOPP>(P, sh, TOPP ? vals : uv, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
+  finish<ES, TOPP, true>(P, sh, vals, C, rank, b, i, T, i, u, e0, e1, row_t.R, row_t.R, S_t,
                          S_t, kt, nkt, cntt, 0u, 0x7fffffff, 0);
 }
 
+// Clears the flag word and the sequence words before a verify (or sampler)
+// kernel.  It is launched as a programmatic dependent of whatever kernel
+// precedes it on the stream, so its launch overlaps that kernel's end; it
+// writes nothing until that kernel has completed (griddepcontrol.wait), which
+// may be the previous call on the same workspace.
 __global__ void verify_init_kernel(uint32_t* flags, unsigned long long* words, uint32_t* words2,
                                    int B) {
+  pdl_wait();
   pdl_launch_dependents();  // the verify kernel may start launching
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t == 0) *flags = 0u;
@@ -2854,10 +3027,9 @@ static int g_configured_sample[4] = {0, 0, 0, 0};
 template <int ES, bool TOPP, bool SAMPLE = false>
 static cudaError_t configure() {
   auto k = SAMPLE ? sample_kernel<ES, TOPP> : verify_kernel<ES, TOPP>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxRounds * kThreads * (int)sizeof(float) > kRingBytes
-                                           ? kMaxRounds * kThreads * (int)sizeof(float)
-                                           : kRingBytes);
+  constexpr int kSums = kMaxRounds * kThreads * (int)sizeof(float);
+  constexpr int kMax = (kSums > kRingBytes ? kSums : kRingBytes) + (SAMPLE ? kSampleSumsOff : 0);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMax);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
@@ -2898,6 +3070,20 @@ static int sm_count() {
 // SM about three, but no slice under 32 KB of a row (narrower slices spend
 // more time in the per-item combine and decision than in streaming), and at
 // least wide enough that a slice fits kMaxRounds rounds; at most 16 CTAs.
+static cudaError_t launch_init(uint32_t* flags, unsigned long long* words, uint32_t* words2, int B,
+                               int blocks, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_init_kernel, flags, words, words2, B);
+}
+
 static void choose_geometry(int V, int ES, int B, int* C_out, int* slice_out, int max_rounds = kMaxRounds) {
   const long long row_bytes = (long long)V * ES;
   const long long max_slice = (long long)max_rounds * kThreads * 16 - 64;
@@ -2972,8 +3158,7 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   cudaStream_t stream = static_cast<cudaStream_t>(L.stream);
 
   const int ib = (L.B + 255) / 256;
-  verify_init_kernel<<<ib < 1 ? 1 : ib, 256, 0, stream>>>(P.flags, P.words, P.words2, L.B);
-  e = cudaGetLastError();
+  e = launch_init(P.flags, P.words, P.words2, L.B, ib < 1 ? 1 : ib, stream);
   if (e != cudaSuccess) {
     *err = std::string("init launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
@@ -3040,8 +3225,7 @@ int sample_launch(const SampleLaunch& L, std::string* err) {
   P.flags = static_cast<uint32_t*>(L.workspace);
   P.slice_len = slice;
   cudaStream_t stream = static_cast<cudaStream_t>(L.stream);
-  verify_init_kernel<<<1, 256, 0, stream>>>(P.flags, nullptr, nullptr, 0);  // the flag word only
-  e = cudaGetLastError();
+  e = launch_init(P.flags, nullptr, nullptr, 0, 1, stream);  // the flag word only
   if (e != cudaSuccess) {
     *err = std::string("init launch: ") + cudaGetErrorString(e);
     return SV_ERR_CUDA;
