@@ -1928,6 +1928,44 @@ __device__ __noinline__ void draw_candidates(const VerifyParams& P, Shared& sh, 
   }
 }
 
+// The round that holds rem among sh.rtot[0 .. rounds) (first round whose
+// inclusive prefix exceeds rem; rounds of zero mass never chosen), found by
+// warp 0 with one double-float warp scan per 32 rounds.  Writes sh.rsel and
+// the remainder inside that round to sh.rem.  Past the end by rounding: the
+// last positive round, just inside its end.  Every lane of warp 0 calls it
+// with the same rem.
+__device__ __forceinline__ void locate_round(Shared& sh, int rounds, DF rem, int lane) {
+  int rsel = -1, rlast = -1;
+  DF vlast{0.f, 0.f};
+  for (int r0 = 0; r0 < rounds && rsel < 0; r0 += 32) {
+    const int r = r0 + lane;
+    const DF v = r < rounds ? sh.rtot[r] : DF{0.f, 0.f};
+    const DF inc = df_warp_scan(v, lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, r < rounds && df_pos(v) && df_gt(inc, rem));
+    const unsigned pos = __ballot_sync(0xffffffffu, r < rounds && df_pos(v));
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      rsel = r0 + l;
+      rem = df_sub(rem, df_sub(df_shfl(inc, l), df_shfl(v, l)));
+    } else {
+      if (pos) {
+        const int l = 31 - __clz(pos);
+        rlast = r0 + l;
+        vlast = df_shfl(v, l);
+      }
+      rem = df_sub(rem, df_shfl(inc, 31));
+    }
+  }
+  if (rsel < 0) {
+    rsel = rlast < 0 ? 0 : rlast;
+    rem = df_mul_f(vlast, 0.999999f);
+  }
+  if (lane == 0) {
+    sh.rsel = rsel;
+    sh.rem = rem;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Draw of the resample (or bonus) token of sequence b at position j with the
 // uniform uK, made by item j itself right after its verdict.  Every CTA of
@@ -2036,7 +2074,7 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
     }
     W.p_only = true;  // residual all zero: draw from p  [SSD §4.3]
   }
-  // ---- locate u * total: rank (warp 0), round (one thread), unit, element ----
+  // ---- locate u * total: slice and round (warp 0), unit (block scan), element ----
   const DF tgt = df_mul_f(slice_w, uK);
   if (warp == 0) {
     const DF v = lane < C ? sh.g_w[lane] : DF{0.f, 0.f};
@@ -2051,28 +2089,8 @@ __device__ __noinline__ void finish(const VerifyParams& P, Shared& sh, float* va
       float* dg = P.diag + ((size_t)b * (P.K + 1) + j) * SV_DIAG_FIELDS;
       dg[SV_DIAG_S_W] = W.p_only ? 1.f : df_to_float(df_div(slice_w, S_t));
     }
-    if (lane == 0) {
-      sh.owner = owner;
-      if (owner == rank) {
-        int rsel = -1, rlast = 0;
-        for (int r = 0; r < rounds; ++r) {
-          const DF rv = sh.rtot[r];
-          if (!df_pos(rv)) continue;
-          rlast = r;
-          if (df_gt(rv, rem)) {
-            rsel = r;
-            break;
-          }
-          rem = df_sub(rem, rv);
-        }
-        if (rsel < 0) {
-          rsel = rlast;
-          rem = df_mul_f(sh.rtot[rlast], 0.999999f);
-        }
-        sh.rsel = rsel;
-        sh.rem = rem;
-      }
-    }
+    if (lane == 0) sh.owner = owner;
+    if (owner == rank) locate_round(sh, rounds, rem, lane);  // (owner: uniform in the warp)
   }
   __syncthreads();
   if (sh.owner != rank) return;  // (uniform inside this CTA)
@@ -2688,6 +2706,15 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
   // may still be in L2; it goes unused if an earlier position turns out
   // rejected, and is skipped if one already was when this item published.
   const bool cand = !greedy && eb_i == 0u && (rej || i == kb);
+  // A draw reads this CTA's slices again (both rows, or the target's for a
+  // bonus).  Streamed a while ago, they have mostly left L2: warp 1 starts a
+  // bulk prefetch of the whole slice now, while rank 0 publishes, where the
+  // draw's own loads would take one DRAM round trip per step.  (Top-p draws
+  // from the kept candidates read no row again.)
+  if (!TOPP && cand && (tid >> 5) == 1) {
+    l2_prefetch_slice<ES>(st, tid & 31);
+    if (i < kb) l2_prefetch_slice<ES>(sd, tid & 31);
+  }
   if (rank == 0 && tid == 0) {
     int j1, e1_;
     bool moot_pub;
@@ -2717,15 +2744,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
   if (!cand) return;  // (uniform in the cluster: no distributed access follows)
   csync(cluster, C);
   if (!sh.fin) return;
-  // The draw reads this CTA's slices again (both rows, or the target's for a
-  // bonus).  Streamed a while ago, they have mostly left L2; a bulk prefetch
-  // of the whole slice brings them back at once, where the draw's own loads
-  // would take one DRAM round trip per step.  (Top-p draws from the kept
-  // candidates read no row again.)
-  if (!TOPP && tid < 32) {
-    l2_prefetch_slice<ES>(st, tid);
-    if (i < kb) l2_prefetch_slice<ES>(sd, tid);
-  }
 
   // ======================= this item's draw =======================
   const float uK = sh.uK;
@@ -2805,37 +2823,10 @@ __device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank,
     if (lane == 0) sh.rtot[r] = a;
   }
   __syncthreads();
-  if (warp == 0) {  // the round: 32 round totals per warp scan
-    DF rem = sh.rem;
-    int rsel = -1, rlast = -1;
-    DF vlast{0.f, 0.f};
-    for (int r0 = 0; r0 < rounds && rsel < 0; r0 += 32) {
-      const int r = r0 + lane;
-      const DF v = r < rounds ? sh.rtot[r] : DF{0.f, 0.f};
-      const DF inc = df_warp_scan(v, lane);
-      const unsigned hit = __ballot_sync(0xffffffffu, r < rounds && df_pos(v) && df_gt(inc, rem));
-      const unsigned pos = __ballot_sync(0xffffffffu, r < rounds && df_pos(v));
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        rsel = r0 + l;
-        rem = df_sub(rem, df_sub(df_shfl(inc, l), df_shfl(v, l)));
-      } else {
-        if (pos) {
-          const int l = 31 - __clz(pos);
-          rlast = r0 + l;
-          vlast = df_shfl(v, l);
-        }
-        rem = df_sub(rem, df_shfl(inc, 31));
-      }
-    }
-    if (rsel < 0) {  // past the end by rounding: the last positive round
-      rsel = rlast < 0 ? 0 : rlast;
-      rem = df_mul_f(vlast, 0.999999f);
-    }
-    if (lane == 0) {
-      sh.rsel = rsel;
-      sh.rem = rem;
-    }
+  if (warp == 0) {  // the round
+    const DF rem = sh.rem;
+    __syncwarp();  // (every lane has read sh.rem before lane 0 rewrites it)
+    locate_round(sh, rounds, rem, lane);
   }
   __syncthreads();
   const int rsel = sh.rsel;
