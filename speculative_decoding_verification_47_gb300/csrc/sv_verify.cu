@@ -728,6 +728,12 @@ constexpr int kUOwn = 512;   // candidates one CTA may contribute per row
 constexpr int kUCap = 1024;  // candidates per row over the cluster
 constexpr int kUAllOff = 2 * kUOwn * 8;
 static_assert(kUAllOff + 2 * kUCap * 8 <= kListOff && 2 * kUCap * 8 <= kListBytes, "candidate areas");
+// local ranking of one row's candidates: counts and slot starts of
+// kRankBins value bins, between the gathered candidates and the lists
+constexpr int kRankBins = 1024;
+constexpr int kRankOff = kUAllOff + 2 * kUCap * 8;
+constexpr int kRankGroupMax = 64;  // the most candidates one bin may hold
+static_assert(kRankOff + 2 * kRankBins * 4 <= kListOff, "ranking area");
 constexpr int kMaxSelPasses = 12;
 
 struct TopSel {
@@ -778,7 +784,7 @@ struct Shared {
   // candidates above the cluster's floor (top-p): this CTA's count, every
   // CTA's offset, the total, whether the exact cut came from them, the cut's
   // rank and the key range of the cut key; the draw's location
-  uint32_t ucnt[2], uoff[2][kCmax], utot[2];
+  uint32_t ucnt[2], uoff[2][kCmax], utot[2], ukmax[2];
   int uok[2], ubelow[2], ucut[2], ua[2], ub[2], ult[2];
   DF uE[2];
   int ypos, ylast;
@@ -1387,6 +1393,7 @@ __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, 
   const uint2* lst = srt;
   if (tid < 2) {
     sh.ucnt[tid] = 0u;
+    sh.ukmax[tid] = 0u;
     sh.ucut[tid] = 0x7fffffff;
     sh.ua[tid] = 0x7fffffff;
     sh.ub[tid] = 0;
@@ -1492,22 +1499,116 @@ __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, 
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         if (i0 + h * kThreads < n32) all[r * kUCap + i0 + h * kThreads] = got[h];
+      atomicMax(&sh.ukmax[r], max(got[0].x, got[1].x));  // (padding: key 0)
     }
   }
   __syncthreads();
   // 4. rank: the tokens ranked before a candidate have a larger key, or the
-  //    same key at a smaller index.  Each CTA counts them for the candidates
-  //    it contributed (at most kUOwn), against all of them, and places each
-  //    in every CTA's rank array (the lists are read: their area takes it).
-  {
-    // work: this CTA's candidates of both rows, G adjacent threads each (G
-    // divides 32), each counting over a share of the gathered ones
+  //    same key at a smaller index; each candidate goes to its rank in srt
+  //    (the lists are read: their area takes it).
+  //    Every CTA holds all the candidates and ranks them itself with a
+  //    counting sort: kRankBins bins uniform in value over (theta, max] (bin
+  //    0 the largest values; a bin never holds a candidate ranked after one
+  //    of a later bin, since rounding is monotone), their counts and prefix,
+  //    each candidate placed in its bin's range of slots, then its place in
+  //    the range from a count of the range's candidates ranked before it.
+  //    No DSMEM traffic and no cluster barrier.  A row with a bin of more
+  //    than kRankGroupMax candidates (or a value range that overflows) takes
+  //    the distributed count below.  All of it is decided from values that
+  //    are the same in every CTA.
+  bool loc[2] = {false, false};
+  bool need_dist = false;
+  for (int r = 0; r < nrows; ++r) {
+    if (!sh.uok[r]) continue;  // (uniform in the cluster)
+    const int n = (int)sh.utot[r];
+    if (n == 0) {
+      loc[r] = true;
+      continue;
+    }
+    const uint32_t kmax = sh.ukmax[r], th = sh.ts[r].lth;
+    const float vmax = bits_val<ES>(key_bits<ES>(kmax)), vth = bits_val<ES>(key_bits<ES>(th));
+    const float inv = (float)(kRankBins - 1) / (vmax - vth);
+    if (kmax <= th || !(inv > 0.f && inv < INFINITY)) {
+      need_dist = true;
+      continue;
+    }
+    constexpr int R = kRankBins;
+    auto bin_of = [&](uint32_t key) {
+      const int b_ = (int)((vmax - bits_val<ES>(key_bits<ES>(key))) * inv);
+      return min(max(b_, 0), R - 1);
+    };
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(dyn + kRankOff);
+    uint32_t* st = cnt + kRankBins;
+    const uint2* a = all + r * kUCap;
+    uint2* out = srt + r * kUCap;
+    for (int b_ = tid; b_ < R; b_ += kThreads) cnt[b_] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) atomicAdd(&cnt[bin_of(a[i].x)], 1u);
+    __syncthreads();
+    bool big = false;
+    for (int b_ = tid; b_ < R; b_ += kThreads) big |= cnt[b_] > (uint32_t)kRankGroupMax;
+    if (__syncthreads_or(big)) {
+      need_dist = true;
+      continue;
+    }
+    {  // exclusive prefix of the counts: thread t takes bins 4t .. 4t+3
+      uint32_t v[4], tot_ = 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int b_ = 4 * tid + q;
+        v[q] = b_ < R ? cnt[b_] : 0u;
+        tot_ += v[q];
+      }
+      uint32_t inc = tot_;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) sh.r_i[warp] = (int)inc;
+      __syncthreads();
+      uint32_t off = inc - tot_;
+      for (int w = 0; w < warp; ++w) off += (uint32_t)sh.r_i[w];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int b_ = 4 * tid + q;
+        if (b_ < R) st[b_] = off;
+        off += v[q];
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {  // (st[b] ends at the end of b's range)
+      const uint2 e_ = a[i];
+      out[atomicAdd(&st[bin_of(e_.x)], 1u)] = e_;
+    }
+    __syncthreads();
+    // within a bin's range, the rank of a candidate is the count of the
+    // range's candidates ranked before it; the ranked row goes through the
+    // gathered array (no longer needed) and back
+    uint2* tmp = all + r * kUCap;
+    for (int x1 = tid; x1 < n; x1 += kThreads) {
+      const uint2 v_ = out[x1];
+      const unsigned long long cv = cand_order(v_);
+      const int b_ = bin_of(v_.x), g = (int)cnt[b_], s0 = (int)st[b_] - g;
+      int w_ = s0;
+      for (int y = s0; y < s0 + g; ++y) w_ += cand_order(out[y]) > cv ? 1 : 0;
+      tmp[w_] = v_;
+    }
+    __syncthreads();
+    for (int x1 = tid; x1 < n; x1 += kThreads) out[x1] = tmp[x1];
+    __syncthreads();
+    loc[r] = true;
+  }
+  if (need_dist) {
+    // this CTA's candidates of the remaining rows, G adjacent threads each
+    // (G divides 32), each counting over a share of the gathered ones
     int cr[2], orr[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int n = (int)sh.utot[r];
-      orr[r] = r < nrows && sh.uok[r] ? (int)sh.uoff[r][rank] : 0;
-      cr[r] = r < nrows && sh.uok[r] ? (rank + 1 < C ? (int)sh.uoff[r][rank + 1] : n) - orr[r] : 0;
+      const bool d = r < nrows && sh.uok[r] && !loc[r];
+      orr[r] = d ? (int)sh.uoff[r][rank] : 0;
+      cr[r] = d ? (rank + 1 < C ? (int)sh.uoff[r][rank + 1] : n) - orr[r] : 0;
     }
     const int items = cr[0] + cr[1];
     int G = 1;
@@ -1535,8 +1636,8 @@ __device__ __noinline__ void topp_candidates(const VerifyParams& P, Shared& sh, 
       if (act && part == 0 && before < n)  // (always < n: the candidates are distinct)
         for (int q = 0; q < C; ++q) remote(cluster, C, srt, q)[r * kUCap + before] = e_;
     }
+    csync(cluster, C);  // every rank is placed in every CTA
   }
-  csync(cluster, C);  // every rank is placed in every CTA
   // 5. masses in rank order: the first candidate whose exclusive prefix
   //    exceeds top_p * S is the first dropped token
   const int x = sh.xtok;
