@@ -23,9 +23,10 @@
  *     sequence's outputs become n_accepted = 0 and out_tokens = -1, and a bit
  *     is set in the workspace's flag word (SV_FLAG_*), readable with
  *     sv_read_device_flags.
- *   - A process uses the library on one GPU: the kernels' launch attributes
- *     are set once, on the first device the process launches on, so a call
- *     on another device may fail with SV_ERR_CUDA (it never runs wrongly).
+ *   - Each call runs on the calling thread's current device.  The kernels'
+ *     launch attributes and the device's properties are set up by the first
+ *     call on each device (ordinals 0..63; a call on a higher ordinal
+ *     returns SV_ERR_CUDA), so one process may use several GPUs.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <string>
 
+#include <cuda_runtime.h>
+
 #include "../../include/specverify.h"
 
 namespace sv {
@@ -56,6 +58,15 @@ size_t verify_workspace_bytes(int B, int K);
 // (L.workspace is ignored).
 constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;
 constexpr int kMaxDevices = 64;
+
+// The calling thread's current device, for state kept per device (kernel
+// attributes and device properties are per device in CUDA): -1 if there is
+// none or its ordinal is kMaxDevices or more.
+inline int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
 int verify_launch_noalloc(const VerifyLaunch& L, std::string* err);
 
 size_t dynk_state_bytes(int B);

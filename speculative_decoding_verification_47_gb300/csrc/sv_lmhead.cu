@@ -22,6 +22,7 @@
 //     a W column block run side by side and W streams from HBM about once.
 #include <cuda.h>  // CUtensorMap and the encoder's signature (resolved at run time)
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -675,13 +676,15 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 static std::mutex g_mutex;
 static EncodeTiledFn g_encode = nullptr;
 
+// SM count per device (device properties are per device in CUDA)
 static int num_sms() {
-  static int n = 0;
+  static std::atomic<int> cache[sv::kMaxDevices];
+  const int d = sv::current_device();
+  if (d < 0) return 148;
+  int n = cache[d].load(std::memory_order_relaxed);
   if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n < 1) n = 148;
+    cache[d].store(n, std::memory_order_relaxed);
   }
   return n;
 }
@@ -750,11 +753,15 @@ static void gemm_cfg(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int gri
 }
 
 // Work units (CTAs, or CTA pairs for PAIR) that can be resident at once: the
-// grid of the persistent kernel.  0 if the query fails.
+// grid of the persistent kernel.  0 if the query fails.  Queried once per
+// device (it also sets the kernel's shared-memory attribute there).
 template <int BNT, int MS>  // MS 0: the single-CTA kernel; 1, 2: pair tiles of MS sub-tiles
 static int resident_units() {
   constexpr bool PAIR = MS > 0;
-  static int n = -1;
+  static std::atomic<int> cache[sv::kMaxDevices];  // units + 1; 0: not queried yet
+  const int d = sv::current_device();
+  if (d < 0) return 0;
+  int n = cache[d].load(std::memory_order_acquire) - 1;
   if (n < 0) {
     auto k = PAIR ? lmhead_gemm_pair_kernel<BNT, MS ? MS : 1> : lmhead_gemm_kernel<BNT>;
     const int smem = PAIR ? kPairSmemBytes : kSmemBytes;
@@ -772,6 +779,7 @@ static int resident_units() {
       }
     }
     n = c;
+    cache[d].store(c + 1, std::memory_order_release);
   }
   return n;
 }

@@ -32,6 +32,7 @@
 // outputs are written by whichever comes last of the item that completes the
 // prefix 0..j (j = first rejection, or k_b) and the draw at j, met through a
 // second per-sequence word.  No item ever waits for another one.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -3113,8 +3114,13 @@ size_t ws_layout(int B, int K, size_t* words_off, size_t* words2_off, size_t* st
   return (off + 255) / 256 * 256;
 }
 
-static int g_configured[4] = {0, 0, 0, 0};
-static int g_configured_sample[4] = {0, 0, 0, 0};
+// Launch state per device: the kernels' shared-memory and cluster attributes
+// and the SM count are per device in CUDA, so each device is set up by the
+// first call made on it.
+struct DeviceLaunchState {
+  std::atomic<int> configured[4], configured_sample[4], sms;
+};
+static DeviceLaunchState g_launch[kMaxDevices];
 
 template <int ES, bool TOPP, bool SAMPLE = false>
 static cudaError_t configure() {
@@ -3148,12 +3154,12 @@ static cudaError_t launch(const VerifyParams& P0, int C, int items, size_t smem,
 }
 
 static int sm_count() {
-  static int n = 0;
+  const int d = current_device();
+  if (d < 0) return 148;
+  int n = g_launch[d].sms.load(std::memory_order_relaxed);
   if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n < 1) n = 148;
+    g_launch[d].sms.store(n, std::memory_order_relaxed);
   }
   return n;
 }
@@ -3210,14 +3216,19 @@ int verify_launch(const VerifyLaunch& L, std::string* err) {
   if (topp && smem < (size_t)kToppSmemBytes) smem = kToppSmemBytes;
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
-  if (!g_configured[gi]) {
+  const int dev = current_device();
+  if (dev < 0) {
+    *err = "no current CUDA device, or its ordinal is past the library's limit";
+    return SV_ERR_CUDA;
+  }
+  if (!g_launch[dev].configured[gi].load(std::memory_order_acquire)) {
     e = ES == 2 ? (topp ? configure<2, true>() : configure<2, false>())
                 : (topp ? configure<4, true>() : configure<4, false>());
     if (e != cudaSuccess) {
       *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return SV_ERR_CUDA;
     }
-    g_configured[gi] = 1;
+    g_launch[dev].configured[gi].store(1, std::memory_order_release);
   }
   size_t words_off, words2_off, stats_off;
   ws_layout(L.B, L.K, &words_off, &words2_off, &stats_off);
@@ -3292,14 +3303,19 @@ int sample_launch(const SampleLaunch& L, std::string* err) {
   if (!topp) smem = (size_t)kSampleSumsOff + (size_t)rounds * kThreads * sizeof(float);  // ring + sums
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
-  if (!g_configured_sample[gi]) {
+  const int dev = current_device();
+  if (dev < 0) {
+    *err = "no current CUDA device, or its ordinal is past the library's limit";
+    return SV_ERR_CUDA;
+  }
+  if (!g_launch[dev].configured_sample[gi].load(std::memory_order_acquire)) {
     e = ES == 2 ? (topp ? configure<2, true, true>() : configure<2, false, true>())
                 : (topp ? configure<4, true, true>() : configure<4, false, true>());
     if (e != cudaSuccess) {
       *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
       return SV_ERR_CUDA;
     }
-    g_configured_sample[gi] = 1;
+    g_launch[dev].configured_sample[gi].store(1, std::memory_order_release);
   }
   VerifyParams P = {};
   P.tgt = static_cast<const char*>(L.logits);
