@@ -6,8 +6,9 @@ Cases: the mixed greedy / sampled workload at full size (V=151936, top_p=0.9),
 both logit types over a range of top_p, cuts that fall inside groups of equal
 logits (ties broken by index), a completely flat row, near-degenerate top_p
 (a single kept token; almost everything kept), windows wide enough to need
-the fixed-point mass pass on bf16, and rows whose target and draft copies sit
-at different 16-byte phases."""
+the fixed-point mass pass on bf16, a tie of 300 top tokens that the candidates'
+ranking resolves by index, and rows whose target and draft copies sit at
+different 16-byte phases."""
 
 import numpy as np
 import pytest
@@ -88,6 +89,29 @@ def test_cut_inside_groups_of_equal_logits(dt, top_p):
     w.target = _store(w, np.round(_logits(w, w.target) * 2.0) / 2.0)
     w.draft = _store(w, np.round(_logits(w, w.draft) * 2.0) / 2.0)
     _check(w)
+
+
+@pytest.mark.parametrize("dt", [wl.BF16, wl.F32])
+def test_large_tie_group_among_candidates(dt):
+    """300 tokens at the row's top logit, scattered over a row of N(0,1)
+    logits (131072 bf16 or 32768 fp32 tokens): the cluster's list floor
+    mostly stays far below them, so the cut is taken from a few hundred
+    candidates, and all 300 tied tokens fall into one value bin (more than
+    the local ranking takes), so they are ranked by the distributed count;
+    a row whose floor reaches the tie takes the passes.  top_p = 0.5 cuts
+    inside the tie: which tied tokens are kept is decided by index order."""
+    B, K = 2, 2
+    V = 131072 if dt == wl.BF16 else 32768
+    w = wl.synth_verify("bigtie", B, K, V, dt, K, 1.0, 1.0, 0, top_p=0.5, seeds=(8500, 8501, 8502))
+    r = np.random.default_rng(8503)
+    for a in (w.target, w.draft):
+        z = r.standard_normal(a.shape)
+        for b in range(B):
+            for i in range(a.shape[1]):
+                z[b, i, r.choice(V, size=300, replace=False)] = 10.0
+        a[...] = _store(w, z)
+    (dec, dis), g, o = _check(w)
+    assert dec > 0
 
 
 @pytest.mark.parametrize("dt", [wl.BF16, wl.F32])
