@@ -373,8 +373,7 @@ __device__ __forceinline__ float unit_sumexp(const uint4& v, const Expo& x, floa
 // lists compare; without, it returns 0 and forms the max only when the
 // reference exponent must rise.
 template <int ES, bool MAX = false>
-__device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const Expo& x,
-                                              float* sum_out = nullptr) {
+__device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const Expo& x) {
   uint32_t um = 0;
   if (ES == 2) {
     um = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
@@ -394,7 +393,6 @@ __device__ __forceinline__ float sampled_unit(RowAcc& a, const uint4& v, const E
     }
   }
   a.pend += us;
-  if (sum_out) *sum_out = us;  // (relative to the reference after any rise)
   return g;
 }
 
@@ -776,6 +774,7 @@ struct Shared {
   DF rtot[kMaxRounds];
   DF scan[kWarps];
   int r_i[kWarps];
+  float wR[kWarps];  // draft sampler: each warp's reference exponent after the row pass
   // item scalars, written by one thread and read by the whole CTA
   RowAcc row_t, row_d;
   DF S_w, rem;
@@ -2413,28 +2412,6 @@ __device__ __forceinline__ void row_unit_v(RowAcc& a, const RowSlice<ES>& rs, in
   }
 }
 
-// The unit sums this thread stored before unit u, times p (a rise of its
-// reference exponent).
-__device__ __noinline__ void uv_rescale(float* uv, int u, float p) {
-  for (int v = u % kThreads; v < u; v += kThreads) uv[v] *= p;
-}
-
-// Sum of 2^(z*c - R) over unit u of a slice (a full unit, or the valid
-// elements of a partial one).
-template <int ES>
-__device__ __forceinline__ float unit_or_edge_sum(const RowSlice<ES>& rs, int u, int ub0, int ub1,
-                                                  const uint4& v, const Expo& x, float R) {
-  if (u >= ub0 && u < ub1) return unit_sumexp<ES>(v, x, R);
-  constexpr int EPU = 16 / ES;
-  const int eb = rs.ebase0 + u * EPU;
-  float s_ = 0.f;
-  for (int j = 0; j < EPU; ++j) {
-    const int e = eb + j;
-    if (e >= rs.e0 && e < rs.e1) s_ += e2(rs.elem(e), x, -R);
-  }
-  return s_;
-}
-
 // Seeds the reference exponent of a sampled row, before anything is summed,
 // from the largest logit among the warp's first-step units (kLoadsInFlight
 // aligned units per lane, in this lane's slots).  Each lane raises its own
@@ -2464,20 +2441,13 @@ __device__ __forceinline__ void seed_reference(RowAcc& a, const uint4* slot, int
 // an earlier position of the sequence is rejected (it then sets sh.moot).
 // With LISTS (top-p instances, sampled rows), each thread also keeps its
 // candidate lists in lst, and sh.lth[r] ends as the CTA's floor of row r.
-// With UVALS (the draft sampler: one row, no draft), the ring holds the
-// target slots only and each unit's sum 2^(z*c - R) is kept in uv[u]; a rise
-// of this thread's reference R rescales the sums it stored before.
-template <int ES, bool MOOT, bool LISTS = false, bool UVALS = false>
+template <int ES, bool MOOT, bool LISTS = false>
 __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh, float* vals,
                                               const RowSlice<ES>& st, const RowSlice<ES>& sd,
                                               bool has_draft, bool greedy, bool skip, const Expo& X,
                                               int b, int i, RowAcc& at, RowAcc& ad,
-                                              uint2* lst = nullptr, float* uv = nullptr) {
+                                              uint2* lst = nullptr) {
   const int tid = threadIdx.x;
-  if (UVALS) {  // every unit of the rounds starts at 0 (the slice's tail units stay 0)
-    const int rounds = (st.n_units + kThreads - 1) / kThreads;
-    for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] = 0.f;
-  }
   const bool lists = LISTS && !greedy;
   // list admission thresholds (values); the draft row keeps no list when
   // the call leaves the draft untruncated
@@ -2492,8 +2462,8 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
     // k < L target, k >= L draft) and reduces the oldest step from there.
     constexpr int L = kLoadsInFlight;
     constexpr int kStep = kThreads * L;
-    constexpr int kStage = (UVALS ? 1 : 2) * L * kThreads;  // slots per stage (UVALS: target only)
-    constexpr int NS = UVALS ? kSampleRingStages : kRingStages;  // stages
+    constexpr int kStage = 2 * L * kThreads;  // slots per stage
+    constexpr int NS = kRingStages;           // stages
     uint4* ring = reinterpret_cast<uint4*>(vals);
     const int NU = has_draft ? max(st.n_units, sd.n_units) : st.n_units;
     const int tb0 = st.ub0(), tb1 = st.ub1(), db0 = sd.ub0(), db1 = sd.ub1();
@@ -2568,12 +2538,6 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
           const uint4 vt = slot[k * kThreads];
           if (greedy) {
             greedy_unit<ES>(at, vt, st.ebase0 + (u0 + k * kThreads) * EPU);
-          } else if (UVALS) {
-            const float R0 = at.R;
-            float us;
-            sampled_unit<ES>(at, vt, X, &us);
-            if (at.R != R0) uv_rescale(uv, u0 + k * kThreads, pow2i(R0 - at.R));  // (rare)
-            uv[u0 + k * kThreads] = us;
           } else {
             const float g = sampled_unit<ES, LISTS>(at, vt, X);
             if (LISTS && g > thr0) thr0 = list_unit<ES>(sh, lst, 0, okey<ES>(val_bits<ES>(g)), u0 + k * kThreads, thr0);
@@ -2592,12 +2556,7 @@ __device__ __forceinline__ void stream_slices(const VerifyParams& P, Shared& sh,
         for (int k = 0; k < L; ++k) {
           const int u = u0 + k * kThreads;
           const uint4 vt = (u >= tb0 && u < tb1) ? slot[k * kThreads] : make_uint4(0, 0, 0, 0);
-          const float R0 = at.R;
           row_unit_v<ES, LISTS>(at, st, u, tb0, tb1, vt, greedy, X, &sh, lst, 0, &thr0);
-          if (UVALS && !greedy && u < st.n_units) {  // the unit's sum against the reference it ended with
-            if (at.R != R0) uv_rescale(uv, u, pow2i(R0 - at.R));
-            uv[u] = unit_or_edge_sum<ES>(st, u, tb0, tb1, vt, X, at.R);
-          }
           if (has_draft) {
             const uint4 vd = (u >= db0 && u < db1) ? slot[(L + k) * kThreads] : make_uint4(0, 0, 0, 0);
             row_unit_v<ES, LISTS>(ad, sd, u, db0, db1, vd, false, X, &sh, lst, 1, &thr1);
@@ -2869,22 +2828,148 @@ __global__ void __launch_bounds__(kThreads, 4) verify_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------
+// The draft sampler's row pass (no top-p): this CTA's slice of one row
+// through the per-thread cp.async ring, as in stream_slices, keeping the sum
+// 2^(z*c - R) of every pair of adjacent units.  Unit u = tid + n*kStep +
+// k*kThreads, so units 2p and 2p+1 are read by lanes 2j and 2j+1 of one warp
+// in the same step: the even lane adds its partner's sum (one shuffle) and
+// stores pair p = u/2 in uv.  The warp keeps one reference exponent R, so the
+// two sums of a pair share it: it is seeded from the warp's first step and
+// raised for every lane at once when a unit of any lane sums above
+// kRaiseAbove (to ceil(c * the warp's largest value)), which rescales the
+// pairs the warp stored before.  (One reference per lane pair rounds the
+// weights' arguments a little more finely, but its divergent raise path
+// measured 40% slower.)  Every lane takes the same number of steps (units
+// past the slice are empty), so the warp's shuffles and votes are converged.
+// The warp's final R goes to sh.wR[warp].  Greedy rows keep only their first
+// maximum.
+// ---------------------------------------------------------------------------
+template <int ES>
+__device__ __forceinline__ void stream_pairs(Shared& sh, float* vals, const RowSlice<ES>& st, bool greedy,
+                                             const Expo& X, RowAcc& at, float* uv) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int L = kLoadsInFlight;
+  constexpr int kStep = kThreads * L;
+  constexpr int NS = kSampleRingStages;
+  constexpr int kStage = L * kThreads;
+  constexpr int EPU = 16 / ES;
+  uint4* ring = reinterpret_cast<uint4*>(vals);
+  const int NU = st.n_units;
+  const int nslots = ((NU + 1) / 2 + kThreads - 1) / kThreads * kThreads;
+  for (int q = tid; q < nslots; q += kThreads) uv[q] = 0.f;  // (pairs past the slice stay 0)
+  const int tb0 = st.ub0(), tb1 = st.ub1();
+  const int nsteps = (NU + kStep - 1) / kStep;
+  auto issue = [&](int n) {
+    uint4* slot = ring + (size_t)(n % NS) * kStage + tid;
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const int u = tid + n * kStep + k * kThreads;
+      if (u >= tb0 && u < tb1)
+        cp_async16(slot + k * kThreads, reinterpret_cast<const void*>(st.base16 + 16 * (uintptr_t)u));
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int n = 0; n < NS; ++n) issue(n);
+  cp_async_wait<NS - 1>();
+  if (!greedy) seed_reference<ES>(at, ring + tid, tid, tb0, tb1, X);  // (the same R in every lane)
+  // the sum of unit u (valid elements only) against reference R
+  auto usum = [&](int u, bool full, const uint4& v, float R) {
+    if (full) return unit_sumexp<ES>(v, X, R);
+    float a = 0.f;
+    if (u < NU) {
+      const int eb = st.ebase0 + u * EPU;
+      for (int j = 0; j < EPU; ++j) {
+        const int e = eb + j;
+        if (e >= st.e0 && e < st.e1) a += e2(st.elem(e), X, -R);
+      }
+    }
+    return a;
+  };
+  for (int n = 0; n < nsteps; ++n) {
+    cp_async_wait<NS - 1>();  // this thread's step n has landed
+    const uint4* slot = ring + (size_t)(n % NS) * kStage + tid;
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+      const int u = tid + n * kStep + k * kThreads;
+      const bool full = u >= tb0 && u < tb1;
+      const uint4 v = full ? slot[k * kThreads] : make_uint4(0u, 0u, 0u, 0u);
+      if (greedy) {  // (uniform in the CTA)
+        if (full) {
+          greedy_unit<ES>(at, v, st.ebase0 + u * EPU);
+        } else if (u < NU) {
+          const int eb = st.ebase0 + u * EPU;
+          for (int j = 0; j < EPU; ++j) {
+            const int e = eb + j;
+            if (e >= st.e0 && e < st.e1) greedy_elem(at, st.elem(e), e);
+          }
+        }
+        continue;
+      }
+      // the running max (NaN propagates) and the unit's sum
+      if (full) {
+        if (ES == 2) at.mx2 = bf16x2_max_nan(at.mx2, bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w)));
+        else at.mx = nanmax(at.mx, unit_max<ES>(v));
+      } else if (u < NU) {
+        const int eb = st.ebase0 + u * EPU;
+        for (int j = 0; j < EPU; ++j) {
+          const int e = eb + j;
+          if (e >= st.e0 && e < st.e1) at.mx = nanmax(at.mx, st.elem(e));
+        }
+      }
+      float us = usum(u, full, v, at.R);
+      if (__any_sync(0xffffffffu, !(us <= kRaiseAbove))) {  // some lane is above R (rare)
+        float g = -INFINITY;
+        if (full) {
+          g = unit_max_num<ES>(v);
+        } else if (u < NU) {
+          const int eb = st.ebase0 + u * EPU;
+          for (int j = 0; j < EPU; ++j) {
+            const int e = eb + j;
+            if (e >= st.e0 && e < st.e1) g = fmaxf(g, st.elem(e));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, o));
+        const float gc = g * X.chi;
+        if (gc > at.R) {  // (uniform in the warp)
+          const float p = pow2i(at.R - ceilf(gc));
+          acc_raise(at, ceilf(gc));
+          if (!(lane & 1))  // this lane's pairs so far (slots tid/2 mod kThreads/2)
+            for (int q = tid >> 1; q < nslots; q += kThreads / 2) uv[q] *= p;
+          us = usum(u, full, v, at.R);
+        }
+      }
+      at.pend += us;
+      const float pv = us + __shfl_xor_sync(0xffffffffu, us, 1);
+      if (!(lane & 1) && u < NU) uv[u >> 1] = pv;
+    }
+    if (!greedy) acc_flush(at);
+    issue(n + NS);  // (the slots were consumed above)
+  }
+  cp_async_wait_all();
+  if (!greedy) acc_finish_max<ES>(at);
+  if (lane == 0) sh.wR[tid >> 5] = at.R;
+}
+
+// ---------------------------------------------------------------------------
 // The draft sampler's draw without top-p (weights p' alone).  The row pass
-// left each thread's unit sums 2^(z*c - R) in uv (R: that thread's own
-// reference), and the combine left every CTA's slice accumulator in sh.g_t.
-// Every CTA finds, from the same values, the slice that holds u*S; the
-// others return at once (nothing distributed follows the combine).  The
-// owner brings its sums to the row's reference Rrow, then finds the round
-// (a warp scan over the round totals, 32 rounds at a time), the unit (a
-// block scan of the round) and the element (that unit read again, its
-// weights 2^(z*c - Rrow) in index order).  The token goes to *out.
+// left the sums 2^(z*c - R) of the slice's unit pairs in uv (R: the
+// reference of the warp that stored the pair, sh.wR), and the combine left
+// every CTA's slice accumulator in sh.g_t.  Every CTA finds, from the same
+// values, the slice that holds u*S; the others return at once (nothing
+// distributed follows the combine).  The owner brings its sums to the row's
+// reference Rrow, then finds the round of kThreads pairs (a warp scan over
+// the round totals, 32 rounds at a time), the pair (a block scan of the
+// round) and the element (the pair's two units read again, their weights
+// 2^(z*c - Rrow) in index order).  The token goes to *out.
 // ---------------------------------------------------------------------------
 // (the slice comes as scalars: row, [e0, e1), n_units, ebase0 as in RowSlice;
 // a struct passed to a call that is not inlined would go through local memory)
 template <int ES>
 __device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank, const char* row, int e0,
-                                         int e1, int n_units, int ebase0, float chi, float clo, float Rthr,
-                                         float Rrow, float uK, int32_t* out) {
+                                         int e1, int n_units, int ebase0, float chi, float clo, float Rrow,
+                                         float uK, int32_t* out) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Expo X{chi, clo};
   if (warp == 0) {  // the owner of u*S among the slices, in rank order
@@ -2911,9 +2996,10 @@ __device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank,
   }
   __syncthreads();
   if (sh.owner != rank) return;  // (uniform inside this CTA)
-  const int rounds = (n_units + kThreads - 1) / kThreads;
-  {  // this thread's sums against the row's reference
-    const float f = Rthr > kRnone ? pow2i(Rthr - Rrow) : 0.f;
+  const int rounds = ((n_units + 1) / 2 + kThreads - 1) / kThreads;
+  {  // slots r*kThreads + tid, stored by warp (tid mod 128) / 16: against the row's reference
+    const float Rw = sh.wR[(tid & (kThreads / 2 - 1)) >> 4];
+    const float f = Rw > kRnone ? pow2i(Rw - Rrow) : 0.f;
     if (f != 1.f)
       for (int r = 0; r < rounds; ++r) uv[r * kThreads + tid] *= f;
   }
@@ -2959,11 +3045,11 @@ __device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank,
   if (past_end) tsel = tlast < 0 ? 0 : tlast;
   if (tid != tsel) return;
   constexpr int EPU = 16 / ES;
-  const int u = rsel * kThreads + tid;
+  const int pr = rsel * kThreads + tid;  // the pair: units 2pr and 2pr+1
   DF cum = past_end ? DF{0.f, 0.f} : df_sub(inc, DF{v, 0.f});
   int y = -1, ylast = -1;
-  const int eb = ebase0 + u * EPU;
-  for (int q = 0; q < EPU; ++q) {
+  const int eb = ebase0 + 2 * pr * EPU;
+  for (int q = 0; q < 2 * EPU; ++q) {
     const int e = eb + q;
     if (e < e0 || e >= e1) continue;
     const float z = ES == 2 ? bf16_lo(*reinterpret_cast<const uint16_t*>(row + (size_t)e * 2))
@@ -2977,7 +3063,7 @@ __device__ __noinline__ void sample_draw(Shared& sh, float* uv, int C, int rank,
     }
   }
   if (y < 0) y = ylast;
-  // (a unit whose rescaled sum is positive but whose weights against Rrow all
+  // (a pair whose rescaled sum is positive but whose weights against Rrow all
   // flush to zero holds mass below 2^-126 of the row: its first element)
   if (y < 0) y = max(eb, e0);
   *out = y;
@@ -3033,15 +3119,14 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
   if (tid == 32) sh.uK = greedy ? 0.f : P.unif[(size_t)b * P.K + i];
   __syncthreads();
   RowAcc at = acc_init(), ad = acc_init();
-  // without top-p the row pass keeps its unit sums for the draw (after a
-  // ring of the target slots only)
+  // without top-p the row pass keeps its unit-pair sums for the draw (after
+  // a ring of the row's slots only)
   float* uv = reinterpret_cast<float*>(reinterpret_cast<char*>(vals) + kSampleSumsOff);
   if (TOPP)
     stream_slices<ES, false, TOPP>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
                                    reinterpret_cast<uint2*>(reinterpret_cast<char*>(vals) + kListOff));
   else
-    stream_slices<ES, false, false, true>(P, sh, vals, st, st, false, greedy, false, X, b, i, at, ad,
-                                          nullptr, uv);
+    stream_pairs<ES>(sh, vals, st, greedy, X, at, uv);
   combine_rows(sh, cluster, C, rank, at, ad, greedy, false, false);  // (never moot here)
   const RowAcc row_t = sh.row_t;
   const bool bad = !(row_t.mx > -INFINITY && row_t.mx < INFINITY) ||
@@ -3057,8 +3142,8 @@ __global__ void __launch_bounds__(kThreads, 4) sample_kernel(const __grid_consta
     return;
   }
   if (!TOPP) {  // the unit sums are in uv: no row is read again
-    sample_draw<ES>(sh, uv, C, rank, st.row, st.e0, st.e1, st.n_units, st.ebase0, X.chi, X.clo, at.R,
-                    row_t.R, u, out);
+    sample_draw<ES>(sh, uv, C, rank, st.row, st.e0, st.e1, st.n_units, st.ebase0, X.chi, X.clo, row_t.R,
+                    u, out);
     return;
   }
   DF S_t = row_t.s;
@@ -3287,20 +3372,22 @@ size_t verify_workspace_bytes(int B, int K) {
 int sample_launch(const SampleLaunch& L, std::string* err) {
   const int ES = L.dtype == SV_BF16 ? 2 : 4;
   // every item is independent: clusters as narrow as the slice limit allows
-  // (32 rounds, so the draw's unit sums fit the 32 KB the ring takes)
+  // (without top-p the draw keeps a sum per unit pair, 32 KB for 64 rounds
+  // of units; with top-p, 32 rounds)
+  const bool topp = L.top_p < 1.0f;
   int C, slice;
-  choose_geometry(L.V, ES, L.B * L.K, &C, &slice, 32);
+  choose_geometry(L.V, ES, L.B * L.K, &C, &slice, topp ? 32 : kMaxRounds);
   const long long units = ((long long)slice * ES + 30) / 16 + 1;
   const long long rounds = (units + kThreads - 1) / kThreads;
   if (rounds > kMaxRounds) {
     *err = "vocabulary too large for the cluster slice layout";
     return SV_ERR_SHAPE;
   }
-  const bool topp = L.top_p < 1.0f;
   size_t smem = (size_t)rounds * kThreads * sizeof(float);
   if (smem < (size_t)kRingBytes) smem = kRingBytes;
   if (topp && smem < (size_t)kToppSmemBytes) smem = kToppSmemBytes;
-  if (!topp) smem = (size_t)kSampleSumsOff + (size_t)rounds * kThreads * sizeof(float);  // ring + sums
+  if (!topp)  // ring + pair sums
+    smem = (size_t)kSampleSumsOff + (size_t)(((units + 1) / 2 + kThreads - 1) / kThreads) * kThreads * sizeof(float);
   cudaError_t e;
   const int gi = (ES == 2 ? 0 : 1) + (topp ? 2 : 0);
   const int dev = current_device();

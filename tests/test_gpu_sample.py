@@ -3,11 +3,12 @@ oracle, through the C ABI.  Tokens must match bit for bit, except at a
 position whose inverse-CDF (or top-p cut) margin is below 1e-6.  Such
 disagreements have their own budget (reading R22): at most 5e-4 of the
 sampled tokens of the session.  Over a 128K vocabulary at T = 1 about 2% of
-draws land within 1e-7 of a CDF boundary; the per-token weights are float32
-exponentials (ex2.approx), whose summed error reaches ~2e-9 of the row mass,
-and a draw flips when its margin is smaller than that.  The headline batch's
-draft rows are drawn under ten uniform seeds (12830 draws, the oracle in a
-spawn pool): 2 flips were measured there (1.6e-4), both at margins ~2e-9.
+draws land within 1e-6 of a CDF boundary; the per-token weights are float32
+(an exponential of an argument rounded to float), whose summed error reaches
+a few 1e-9 of the row mass, and a draw flips when its margin is smaller than
+that.  The headline batch's draft rows are drawn under ten uniform seeds
+(12830 draws, the oracle in a spawn pool): 5 flips were measured there
+(3.9e-4), each at an oracle margin below 1e-6 (the excuse this file checks).
 
 Cases: the headline batch's draft rows at full size (B=256, K=8, V=128256
 bf16, ragged k_b, per-row temperature), both dtypes with and without top-p,
