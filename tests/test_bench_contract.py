@@ -105,3 +105,30 @@ def test_no_cluster_multicast_in_the_sources():
         with open(p) as f:
             text = f.read()
         assert "multicast" not in text, p
+
+
+PROFILE_OF = {"c2": "verify_kernel_c2.md", "c1": "verify_kernel_c1.md", "c3": "verify_kernel_c3_topp.md",
+              "c3t": "verify_kernel_c3t.md", "s2": "sample_kernel_s2.md", "c4": "lmhead_gemm_c4.md"}
+
+
+def test_bench_traffic_matches_the_committed_profiles():
+    """Each workload's roofline.traffic in bench.py and the ncu summary under
+    profiles/ describe the same capture: the same source file and hash, and
+    DRAM read + write equal to the bench figure."""
+    import re
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def mbytes(value, unit):
+        return float(value) * {"byte": 1e-6, "Kbyte": 1e-3, "Mbyte": 1.0, "Gbyte": 1e3}[unit]
+
+    for workload, name in PROFILE_OF.items():
+        src, digest, value = bench.MEASURED_TRAFFIC[workload]
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        m = re.search(r"csrc/(\S+), sha256 prefix ([0-9a-f]{16})", text)
+        assert m, name
+        assert (m.group(1), m.group(2)) == (src, digest), (workload, m.groups(), src, digest)
+        rd = re.search(r"DRAM read\s+([0-9.]+) (\w+)", text)
+        wr = re.search(r"DRAM write\s+([0-9.]+) (\w+)", text)
+        got = mbytes(*rd.groups()) + mbytes(*wr.groups())
+        assert abs(got - value / 1e6) < 1e-3, (workload, got, value / 1e6)
