@@ -113,10 +113,6 @@ struct RowSlice {
     n_units = e1 > e0 ? (int)((g1 - base16 + 15) / 16) : 0;
     ebase0 = e0 - (int)((g0 & 15) / ES);
   }
-  __device__ __forceinline__ bool unit_bulk(int u) const {
-    const uintptr_t a = base16 + 16 * (uintptr_t)u;
-    return a >= a0 && a + 16 <= a1;
-  }
     // units [ub0, ub1) are fully inside the aligned body
   __device__ __forceinline__ int ub0() const { return (int)((a0 - base16) / 16); }
   __device__ __forceinline__ int ub1() const { return (int)((a1 - base16) / 16); }
@@ -808,10 +804,6 @@ __device__ __forceinline__ bool word_moot(unsigned long long w, int i) {
   return (R & ((1ull << i) - 1)) != 0;
 }
 
-__device__ __forceinline__ bool item_moot(const unsigned long long* words, int b, int i) {
-  return word_moot(__ldcg(words + b), i);
-}
-
 __device__ bool resolvable(unsigned long long w, int kb, int* j_out, bool* err) {
   const unsigned long long mask = (1ull << kWordBits) - 1;
   const unsigned long long D = w & mask;
@@ -1046,24 +1038,6 @@ __device__ __forceinline__ uint4 edge_unit(const RowSlice<ES>& rs, int eb, uint3
   }
   *valid = m;
   return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// One unit of a selection pass.
-template <int ES>
-__device__ __forceinline__ uint32_t sel_unit(const SelP& p, unsigned char* h, const RowSlice<ES>& rs,
-                                             int u, int ub0, int ub1, const uint4& v, int x,
-                                             const Expo& X, DF* above) {
-  constexpr int EPU = 16 / ES;
-  const int eb = rs.ebase0 + u * EPU;
-  if (u >= ub0 && u < ub1) {
-    const uint32_t mask = window_mask<ES>(v, p);
-    if (mask) return sel_bits<ES>(p, h, v, eb, mask, x, X, above);
-  } else if (u < rs.n_units) {
-    uint32_t valid;
-    const uint4 ve = edge_unit<ES>(rs, eb, &valid);
-    return sel_bits<ES>(p, h, ve, eb, valid, x, X, above);
-  }
-  return 0u;
 }
 
 // One selection pass of this thread's warp over one row slice (out of line:
@@ -1357,17 +1331,6 @@ __device__ void sel_resolve(Shared& sh, int r, const uint32_t (&w)[8], uint32_t 
 // ascending; "ranked before" is a larger composite.
 __device__ __forceinline__ unsigned long long cand_order(uint2 e) {
   return ((unsigned long long)e.x << 32) | (unsigned long long)(~e.y);
-}
-
-// Candidates of a segment sorted in rank order that are ranked before e.
-__device__ __forceinline__ int cand_before(const uint2* seg, int n, unsigned long long ce) {
-  int lo = 0, hi = n;  // the first position whose candidate is not ranked before e
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (cand_order(seg[mid]) > ce) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
 }
 
 // Exact top-p cut of each row from its candidates: every token whose key
